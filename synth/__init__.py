@@ -1,0 +1,152 @@
+"""Seeded synthetic inputs for the joint single_block: token layouts, RoPE
+position ids, random-init weights, activations and modulation vectors.
+
+This module serves both the CUDA path (tests, bench) and the CPU oracle.  It
+holds none of the block's arithmetic: it only draws seeded random numbers and
+lays tokens out the way the pipeline does before the blocks run.
+
+Distributions (random-init stand-ins for the gated checkpoint):
+  weights      N(0, 0.02) rounded to bf16, [out, in], no biases
+  norm scales  1 + N(0, 0.1), float32 [128]
+  activations  N(0, 1) rounded to bf16, held as float32 (the residual stream)
+  modulation   N(0, 0.1) float32, one [3 * 3072] vector per stream
+
+Token layouts follow the pipeline's packing: one token per 16x16-pixel patch
+(a 1024x1024 image is a 64x64 grid), text first, then the noisy image, then
+the references, and the 4-axis ids of the "Positions in four dimensions" table
+of "Welcome FLUX.3 Image Klein in Diffusers": text i -> (0,0,0,i); image
+(row, col) -> (0, row/2, col/2, 0); reference k -> (0, row/2, col/2, -(k+1)).
+"""
+
+from dataclasses import dataclass, field
+import zlib
+
+import numpy as np
+import torch
+
+STREAM_IMAGE = 0
+STREAM_IMAGE_COND = 1
+STREAM_TXT = 2
+STREAM_OF = {"image": STREAM_IMAGE, "image_cond": STREAM_IMAGE_COND, "txt": STREAM_TXT}
+
+HIDDEN = 3072
+MLP_HIDDEN = 9216
+HEAD_DIM = 128
+HEADS = 24
+
+
+@dataclass
+class Layout:
+    """segments: list of (start, length, stream); pos: float32 [T, 4]."""
+    segments: list
+    pos: np.ndarray
+    stream_id: np.ndarray = field(repr=False)
+
+    @property
+    def T(self):
+        return int(self.pos.shape[0])
+
+
+def build_layout(spec, l_offset=0.0):
+    """spec: list of ('txt', n) | ('image', (rows, cols)) | ('image_cond', (rows, cols)).
+    References are numbered k = 0, 1, ... in the order they appear; ``l_offset``
+    is added to every reference's l id (0 keeps the table's -(k+1))."""
+    segments, pos = [], []
+    start, k = 0, 0
+    for kind, size in spec:
+        if kind == "txt":
+            n = int(size)
+            p = np.zeros((n, 4), np.float32)
+            p[:, 3] = np.arange(n, dtype=np.float32)
+        else:
+            rows, cols = size
+            r, c = np.meshgrid(np.arange(rows), np.arange(cols), indexing="ij")
+            n = rows * cols
+            p = np.zeros((n, 4), np.float32)
+            p[:, 1] = r.reshape(-1) * 0.5
+            p[:, 2] = c.reshape(-1) * 0.5
+            if kind == "image_cond":
+                p[:, 3] = -(k + 1.0) + l_offset
+                k += 1
+        if n == 0:
+            continue
+        segments.append((start, n, STREAM_OF[kind]))
+        pos.append(p)
+        start += n
+    pos = np.concatenate(pos, 0) if pos else np.zeros((0, 4), np.float32)
+    sid = np.zeros(start, np.uint8)
+    for s0, n, st in segments:
+        sid[s0:s0 + n] = st
+    return Layout(segments, pos, sid)
+
+
+# The benchmark and parity workloads (text padded to a multiple of 80 by the
+# pipeline is only a sizing rule; these use the stated counts).
+WORKLOADS = {
+    # one block, 32 txt + 8x8 image (128x128 px)
+    "block_t96": dict(spec=[("txt", 32), ("image", (8, 8))], blocks=1, calls=1, wfmt="bf16"),
+    # one block at 1024x1024: 512 txt + 64x64 image
+    "block_1024sq_t4608": dict(spec=[("txt", 512), ("image", (64, 64))], blocks=1, calls=1, wfmt="bf16"),
+    # one block, 1024x1024 target + one 1024x1024 reference
+    "block_1024sq_ref1_t8704": dict(spec=[("txt", 512), ("image", (64, 64)), ("image_cond", (64, 64))],
+                                    blocks=1, calls=1, wfmt="bf16"),
+    # 28-block stack, 1024x1024 + two 512x512 references, 16 calls
+    "stack28_1024sq_2ref512_t6656": dict(spec=[("txt", 512), ("image", (64, 64))] + [("image_cond", (32, 32))] * 2,
+                                         blocks=28, calls=16, wfmt="bf16"),
+    # 28-block stack, NVFP4 weights, 1024x1024 + ten 512x512 references
+    "stack28_nvfp4_1024sq_10ref512_t14848": dict(
+        spec=[("txt", 512), ("image", (64, 64))] + [("image_cond", (32, 32))] * 10,
+        blocks=28, calls=1, wfmt="nvfp4"),
+}
+
+
+def _seed(*parts):
+    return zlib.crc32("/".join(str(p) for p in parts).encode()) & 0x7FFFFFFF
+
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def block_weights(seed, block, device="cpu", hidden=HIDDEN, mlp_hidden=MLP_HIDDEN, head_dim=HEAD_DIM,
+                  std=0.02):
+    """Random-init weights of one block: bf16 [out, in] matrices and float32
+    [head_dim] norm scales.  Values depend on (seed, block, tensor) and on the
+    device the generator runs on."""
+    shapes = {"q_proj": (hidden, hidden), "k_proj": (hidden, hidden), "v_proj": (hidden, hidden),
+              "attn_out": (hidden, hidden), "mlp_in": (2 * mlp_hidden, hidden),
+              "mlp_out": (hidden, mlp_hidden)}
+    w = {}
+    for name, shape in shapes.items():
+        g = _gen(device, _seed(seed, block, name))
+        w[name] = (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
+    for name in ("query_norm", "key_norm"):
+        g = _gen(device, _seed(seed, block, name))
+        w[name] = 1.0 + 0.1 * torch.randn((head_dim,), generator=g, device=device, dtype=torch.float32)
+    return w
+
+
+def activations(seed, T, device="cpu", hidden=HIDDEN, std=1.0):
+    """Residual-stream input: N(0, std) rounded to bf16, returned as float32."""
+    g = _gen(device, _seed(seed, "x", T))
+    return (torch.randn((T, hidden), generator=g, device=device) * std).to(torch.bfloat16).float()
+
+
+def bf16_matrix(seed, rows, cols, device="cpu", std=1.0, tag="m"):
+    """A bf16 [rows, cols] N(0, std) tensor (inputs of single-step tests)."""
+    g = _gen(device, _seed(seed, tag, rows, cols))
+    return (torch.randn((rows, cols), generator=g, device=device) * std).to(torch.bfloat16)
+
+
+def modulation(seed, call=0, device="cpu", hidden=HIDDEN, std=0.1):
+    """Per-stream modulation vectors [3, 3*hidden] float32 (rows: image,
+    image_cond, txt; columns: shift | scale | gate)."""
+    g = _gen(device, _seed(seed, "mod", call))
+    return torch.randn((3, 3 * hidden), generator=g, device=device) * std
+
+
+def to_f64(t):
+    """Exact float64 NumPy copy of a (bf16 or float32) torch tensor."""
+    return t.detach().to("cpu", torch.float64).numpy()
