@@ -1,0 +1,405 @@
+"""Benchmark of the joint single_block forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one joint single_block over one batch of synthetic tokens (default
+the 1024x1024 workload: 512 text + 64x64 image tokens = 4608): stream ids,
+RoPE tables, LayerNorm + modulation, the fused in-projection GEMM (q/k/v with
+QK-RMSNorm + RoPE, SwiGLU), attention, and the out-projection GEMM with the
+gated residual.  Inputs are resident in HBM when the timed region starts;
+L2 is flushed (a 256 MiB write) between timed steps, outside the per-step
+events.  For N > 1 (torchrun) every rank runs an independent replica (the
+path needs no exchange): the value is the tokens of all ranks over the
+slowest rank's time.
+
+One JSON line is printed by rank 0.  `--impl reference` times the CPU oracle
+on the host cores instead (rank 0 only).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "single_block tokens/s and TFLOP/s at 1024² (4608 tok), % of B300 BF16 peak"
+UNIT = "tokens/s"
+
+# Algorithmic FLOPs of one block over T tokens: 2 x (MACs of the six
+# projections) + QK^T + PV = 245,366,784 T + 12,288 T^2.
+def block_flops(T):
+    D, F = 3072, 9216
+    proj = 2 * T * D * (3 * D + 2 * F) + 2 * T * (D + F) * D
+    attn = 4 * T * T * D
+    return proj + attn
+
+
+def kernel_flops(T):
+    return {"in_projection": 2 * T * 3072 * 27648, "attention": 4 * T * T * 3072,
+            "out_projection": 2 * T * 12288 * 3072}
+
+
+def kernel_bytes(T):
+    """Algorithmic HBM bytes per launch of the memory-bound kernels."""
+    return {"ln_modulate": T * (3072 * 4 + 3072 * 2), "rope_tables": T * (16 + 2 * 64 * 4), "stream_ids": T}
+
+
+# DRAM traffic per launch from an ncu capture, valid only for the kernel
+# source it was taken on (sha256 of the file); null otherwise.
+TRAFFIC = {}
+
+
+def src_sha(path):
+    with open(os.path.join(ROOT, path), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6400.0), d.get("bf16_tflops", 1800.0), d.get("bf16_tflops_sustained"), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+class OracleSample:
+    """The CPU oracle on a bounded sample of the workload: the block output for
+    `rows_n` query tokens (keys and values over all T tokens).  A sample's time
+    is scaled to a whole block by the ratio of algorithmic FLOPs (full block /
+    the sample's)."""
+
+    def __init__(self, spec, rows_n=128):
+        import oracle as O
+        import synth
+        self.O = O
+        self.lay = synth.build_layout(spec)
+        T = self.T = self.lay.T
+        w = synth.block_weights(1, 0, device="cpu")
+        self.wf = {k: synth.to_f64(v) for k, v in w.items()}
+        self.x = synth.to_f64(synth.activations(1, T))
+        self.mods = synth.to_f64(synth.modulation(1))
+        self.pos = self.lay.pos.astype(np.float64)
+        self.rows = np.linspace(0, T - 1, rows_n).astype(np.int64)
+        D, F = 3072, 9216
+        sample_flops = 4 * T * D * D + rows_n * (2 * D * D + 4 * D * F + 2 * (D + F) * D + 4 * T * D)
+        self.scale = block_flops(T) / sample_flops
+        self.rows_n = rows_n
+
+    def run(self):
+        """Seconds of one whole block, extrapolated from one timed sample."""
+        t0 = time.perf_counter()
+        self.O.single_block(self.x, self.wf, self.mods, self.lay.stream_id, self.pos, rows=self.rows)
+        return (time.perf_counter() - t0) * self.scale
+
+    def describe(self, reps):
+        return (f"fp64 NumPy oracle: block output for {self.rows_n} of {self.T} query tokens (keys/values over all "
+                f"tokens), {reps} rep(s), time scaled to a whole block by algorithmic FLOPs x{self.scale:.2f}")
+
+
+def host_cores():
+    cores = len(os.sched_getaffinity(0))
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            cores = max(n)
+    except Exception:
+        pass
+    return cores
+
+
+def oracle_baseline(spec, seconds):
+    s = OracleSample(spec)
+    times = []
+    t_end = time.perf_counter() + seconds
+    while not times or (time.perf_counter() < t_end and len(times) < 50):
+        times.append(s.run())
+    t_block = statistics.mean(times)
+    return {"value": s.T / t_block, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": s.describe(len(times))}
+
+
+def run_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import synth
+    spec = synth.WORKLOADS[args.workload]["spec"]
+    s = OracleSample(spec)
+    for _ in range(args.warmup):
+        s.run()
+    t0 = time.perf_counter()
+    times = [s.run() for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    value = s.T / statistics.mean(times)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "T": s.T},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                             "sample": s.describe(args.steps)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s_timed_region": wall}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import diffusion_transformer_block_fwd_b300 as F3
+    import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    F3.lib()   # fail loudly if the library is missing
+    spec = synth.WORKLOADS[args.workload]["spec"]
+    lay = synth.build_layout(spec)
+    T = lay.T
+    w = synth.block_weights(1, 0, device=dev)
+    blocks = F3.Flux3Blocks([w], max_tokens=T)
+    x = synth.activations(1, T, device=dev)
+    mods = synth.modulation(1, device=dev)
+    pos = torch.from_numpy(lay.pos).to(dev)
+    sid = torch.empty(T, dtype=torch.uint8, device=dev)
+    cs = torch.empty((T, 64), device=dev)
+    sn = torch.empty((T, 64), device=dev)
+    h = torch.empty((T, 3072), dtype=torch.bfloat16, device=dev)
+    qkv = torch.empty((T, 9216), dtype=torch.bfloat16, device=dev)
+    cat = torch.empty((T, 12288), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MiB > L2
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    cfg = blocks.cfg
+
+    names = ["prep", "ln_modulate", "in_projection", "attention", "out_projection"]
+
+    def step(evs=None):
+        # exactly the launch sequence of flux3_block_forward, through the step entry points
+        if evs is not None:
+            evs[0].record(stream)
+        F3.flux3_stream_ids(lay.segments, T, sid.data_ptr(), sp)
+        F3.flux3_rope_tables(pos.data_ptr(), T, cfg.rope_theta, cs.data_ptr(), sn.data_ptr(), sp)
+        if evs is not None:
+            evs[1].record(stream)
+        F3.flux3_ln_modulate(x.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), cfg.eps_ln, h.data_ptr(), sp)
+        if evs is not None:
+            evs[2].record(stream)
+        F3.flux3_in_projection(blocks.handle, 0, h.data_ptr(), T, cs.data_ptr(), sn.data_ptr(), qkv.data_ptr(),
+                               cat.data_ptr(), sp)
+        if evs is not None:
+            evs[3].record(stream)
+        F3.flux3_attention(qkv.data_ptr(), T, cat.data_ptr(), sp)
+        if evs is not None:
+            evs[4].record(stream)
+        F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), x.data_ptr(),
+                                sp)
+        if evs is not None:
+            evs[5].record(stream)
+
+    launches_per_step = 6
+    for _ in range(args.warmup):
+        step()
+    st = F3.flux3_check_error(sp)
+    assert st == 0, F3.status_string(st)
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    st = F3.flux3_check_error(sp)
+    assert st == 0, F3.status_string(st)
+
+    per_kernel = {n: statistics.mean(events[i][k].elapsed_time(events[i][k + 1]) for i in range(args.steps))
+                  for k, n in enumerate(names)}
+    step_ms = statistics.mean(events[i][0].elapsed_time(events[i][5]) for i in range(args.steps))
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = world * T / (step_ms * 1e-3)
+    tflops = world * block_flops(T) / (step_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public call, host buffers, copies inside the timed region
+    x_host = synth.activations(2, T, device="cpu").pin_memory()
+    pos_host = torch.from_numpy(lay.pos.copy()).pin_memory()
+    mod_host = synth.modulation(2).pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    xd = torch.empty_like(x_host, device=dev)
+    posd = torch.empty_like(pos_host, device=dev)
+    modd = torch.empty_like(mod_host, device=dev)
+
+    def e2e_step():
+        xd.copy_(x_host, non_blocking=True)
+        posd.copy_(pos_host, non_blocking=True)
+        modd.copy_(mod_host, non_blocking=True)
+        blocks.forward(xd, lay.segments, posd, modd)
+        out_host.copy_(xd, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = x_host.numel() * 4 + pos_host.numel() * 4 + mod_host.numel() * 4
+    d2h = out_host.numel() * 4
+    st = F3.flux3_check_error(sp)
+    assert st == 0, F3.status_string(st)
+
+    hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
+    kf = kernel_flops(T)
+    dominant = max(("in_projection", "attention", "out_projection"), key=lambda n: per_kernel[n])
+    achieved = kf[dominant] / (per_kernel[dominant] * 1e-3) / 1e12
+    tr = TRAFFIC.get(dominant)
+    traffic = None
+    if tr and tr.get("src_sha") == src_sha(tr["src"]) and tr.get("T") == T:
+        traffic = tr["bytes_per_launch"]
+    roofline = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": bf16_burst,
+                "unit": "TFLOP/s", "frac": achieved / bf16_burst, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
+                else "fallback 1.8 PFLOP/s"}
+    kernels = {}
+    for n in names:
+        d = {"ms": per_kernel[n]}
+        if n in kf:
+            d["tflops"] = kf[n] / (per_kernel[n] * 1e-3) / 1e12
+        if n == "ln_modulate":
+            d["gbs"] = kernel_bytes(T)["ln_modulate"] / (per_kernel[n] * 1e-3) / 1e9
+        kernels[n] = d
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init N(0,0.02) bf16 weights)",
+            "config": {"workload": args.workload, "T": T, "segments": lay.segments,
+                       "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
+            "frac_of_bf16_spec_2250": tflops / world / 2250.0,
+            "kernels": kernels, "roofline": roofline,
+            "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "api": "flux3_block_forward with pinned host x/pos/mod, H2D + D2H inside the timed region"},
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+            "wall_s_timed_region": t_wall}
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_baseline(spec, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    blocks.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="block_1024sq_t4608")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+"""Python binding of libflux3.so, the sm_103a library for the FLUX.3 Image
+Klein joint single_block forward pass (C ABI: include/flux3.h).
+
+The functions below carry the C entry points' names and only marshal
+arguments (ctypes); every step of the block runs in the library's CUDA
+kernels.  PyTorch is used for device memory and streams only.  There is no
+fallback: if the library is missing or cannot be loaded, importing the
+binding's functions raises.
+"""
+
+import ctypes
+import os
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libflux3.so")
+
+FLUX3_OK = 0
+FLUX3_ERR_INVALID_ARG = -1
+FLUX3_ERR_UNSUPPORTED = -2
+FLUX3_ERR_ALIGNMENT = -3
+FLUX3_ERR_WORKSPACE = -4
+FLUX3_ERR_CUDA = -5
+FLUX3_ERR_TIMEOUT = -6
+FLUX3_ERR_DEVICE = -7
+
+FLUX3_W_BF16 = 0
+FLUX3_W_NVFP4 = 1
+FLUX3_STREAM_IMAGE = 0
+FLUX3_STREAM_IMAGE_COND = 1
+FLUX3_STREAM_TXT = 2
+FLUX3_MAX_SEGMENTS = 32
+
+EXPORTED = (
+    "flux3_default_config", "flux3_packed_weight_bytes", "flux3_workspace_bytes", "flux3_block_init",
+    "flux3_block_forward", "flux3_stack_forward", "flux3_check_error", "flux3_status_string", "flux3_destroy",
+    "flux3_stream_ids", "flux3_rope_tables", "flux3_ln_modulate", "flux3_in_projection", "flux3_attention",
+    "flux3_out_projection", "flux3_gemm_bf16", "flux3_selftest_wait_timeout",
+)
+
+
+class Flux3Error(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class flux3_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("mlp_hidden", ctypes.c_int), ("n_blocks", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("wfmt", ctypes.c_int), ("rope_theta", ctypes.c_float), ("eps_ln", ctypes.c_float),
+                ("eps_rms", ctypes.c_float)]
+
+
+class flux3_block_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out",
+                                                "query_norm", "key_norm")]
+
+
+class flux3_segment(ctypes.Structure):
+    _fields_ = [("start", ctypes.c_int), ("len", ctypes.c_int), ("stream", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libflux3.so not built ({LIB_PATH}); run "
+                               "python -m diffusion_transformer_block_fwd_b300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        cfgp = ctypes.POINTER(flux3_config)
+        segp = ctypes.POINTER(flux3_segment)
+        sig = {
+            "flux3_default_config": (None, [cfgp]),
+            "flux3_packed_weight_bytes": (sz, [cfgp]),
+            "flux3_workspace_bytes": (sz, [cfgp, i]),
+            "flux3_block_init": (i, [ctypes.POINTER(vp), cfgp, ctypes.POINTER(flux3_block_weights), i, vp, sz, vp]),
+            "flux3_block_forward": (i, [vp, i, vp, i, segp, i, vp, vp, vp, sz, vp]),
+            "flux3_stack_forward": (i, [vp, i, i, vp, i, segp, i, vp, vp, vp, sz, vp]),
+            "flux3_check_error": (i, [vp]),
+            "flux3_status_string": (ctypes.c_char_p, [i]),
+            "flux3_destroy": (None, [vp]),
+            "flux3_stream_ids": (i, [segp, i, i, vp, vp]),
+            "flux3_rope_tables": (i, [vp, i, f, vp, vp, vp]),
+            "flux3_ln_modulate": (i, [vp, i, vp, vp, f, vp, vp]),
+            "flux3_in_projection": (i, [vp, i, vp, i, vp, vp, vp, vp, vp]),
+            "flux3_attention": (i, [vp, i, vp, vp]),
+            "flux3_out_projection": (i, [vp, i, vp, i, vp, vp, vp, vp]),
+            "flux3_gemm_bf16": (i, [vp, vp, vp, i, i, i, vp]),
+            "flux3_selftest_wait_timeout": (i, [i, vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status):
+    return lib().flux3_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status != FLUX3_OK:
+        raise Flux3Error(status, what)
+
+
+def segments_array(segments):
+    """[(start, len, stream), ...] -> ctypes array of flux3_segment."""
+    arr = (flux3_segment * max(1, len(segments)))()
+    for k, (s, n, st) in enumerate(segments):
+        arr[k].start, arr[k].len, arr[k].stream = int(s), int(n), int(st)
+    return arr
+
+
+# ---------------------------------------------------------------- C entry points
+def flux3_default_config():
+    cfg = flux3_config()
+    lib().flux3_default_config(ctypes.byref(cfg))
+    return cfg
+
+
+def flux3_packed_weight_bytes(cfg):
+    return int(lib().flux3_packed_weight_bytes(ctypes.byref(cfg)))
+
+
+def flux3_workspace_bytes(cfg, T):
+    return int(lib().flux3_workspace_bytes(ctypes.byref(cfg), int(T)))
+
+
+def flux3_block_init(cfg, weights, packed_ptr, packed_bytes, stream=0):
+    """weights: list of dicts of device pointers (ints) keyed like
+    flux3_block_weights.  Returns the handle (an int)."""
+    n = len(weights)
+    arr = (flux3_block_weights * n)()
+    for b, w in enumerate(weights):
+        for k, _ in flux3_block_weights._fields_:
+            setattr(arr[b], k, int(w[k]))
+    h = ctypes.c_void_p()
+    _check(lib().flux3_block_init(ctypes.byref(h), ctypes.byref(cfg), arr, n, packed_ptr, packed_bytes, stream),
+           "flux3_block_init")
+    return h.value
+
+
+def flux3_block_forward(h, block_idx, x, T, segments, pos_ids, mod, workspace, ws_bytes, stream=0):
+    segs = segments_array(segments)
+    _check(lib().flux3_block_forward(h, block_idx, x, T, segs, len(segments), pos_ids, mod, workspace, ws_bytes,
+                                     stream), "flux3_block_forward")
+
+
+def flux3_stack_forward(h, first_block, n_blocks, x, T, segments, pos_ids, mod, workspace, ws_bytes, stream=0):
+    segs = segments_array(segments)
+    _check(lib().flux3_stack_forward(h, first_block, n_blocks, x, T, segs, len(segments), pos_ids, mod, workspace,
+                                     ws_bytes, stream), "flux3_stack_forward")
+
+
+def flux3_check_error(stream=0):
+    return int(lib().flux3_check_error(stream))
+
+
+def flux3_destroy(h):
+    lib().flux3_destroy(h)
+
+
+def flux3_stream_ids(segments, T, stream_id, stream=0):
+    segs = segments_array(segments)
+    _check(lib().flux3_stream_ids(segs, len(segments), T, stream_id, stream), "flux3_stream_ids")
+
+
+def flux3_rope_tables(pos_ids, T, theta, cos_tab, sin_tab, stream=0):
+    _check(lib().flux3_rope_tables(pos_ids, T, theta, cos_tab, sin_tab, stream), "flux3_rope_tables")
+
+
+def flux3_ln_modulate(x, T, stream_id, mod, eps, h, stream=0):
+    _check(lib().flux3_ln_modulate(x, T, stream_id, mod, eps, h, stream), "flux3_ln_modulate")
+
+
+def flux3_in_projection(h, block_idx, hmod, T, cos_tab, sin_tab, qkv, cat, stream=0):
+    _check(lib().flux3_in_projection(h, block_idx, hmod, T, cos_tab, sin_tab, qkv, cat, stream),
+           "flux3_in_projection")
+
+
+def flux3_attention(qkv, T, cat, stream=0):
+    _check(lib().flux3_attention(qkv, T, cat, stream), "flux3_attention")
+
+
+def flux3_out_projection(h, block_idx, cat, T, stream_id, mod, x, stream=0):
+    _check(lib().flux3_out_projection(h, block_idx, cat, T, stream_id, mod, x, stream), "flux3_out_projection")
+
+
+def flux3_gemm_bf16(A, B, C, M, N, K, stream=0):
+    _check(lib().flux3_gemm_bf16(A, B, C, M, N, K, stream), "flux3_gemm_bf16")
+
+
+def flux3_selftest_wait_timeout(timeout_us, stream=0):
+    _check(lib().flux3_selftest_wait_timeout(timeout_us, stream), "flux3_selftest_wait_timeout")
+
+
+from .model import Flux3Blocks  # noqa: E402,F401  (torch-owned buffers around the handle)

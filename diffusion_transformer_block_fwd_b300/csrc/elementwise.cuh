@@ -1,0 +1,151 @@
+// Per-call preparation and the memory-bound LayerNorm + modulation kernel.
+//
+//   stream_ids   segment table -> uint8 stream id per token
+//   rope_tables  pos ids [T, 4] -> cos / sin [T, 64] (pair p = 16 a + j of axis a)
+//   ln_modulate  x fp32 [T, 3072] -> h = (1 + scale[s]) * LN(x) + shift[s], bf16
+//
+// ln_modulate is HBM-bound: 12 KB read + 6 KB written per token.  One warp per
+// token row, 16-byte loads, the row held in registers (96 floats per lane),
+// two-pass mean / variance with warp-shuffle reductions.
+
+#pragma once
+
+#include "flux3_internal.h"
+#include "ptx.cuh"
+
+namespace flux3 {
+
+namespace ew_detail {
+
+struct SegTable {
+  int start[FLUX3_MAX_SEGMENTS];
+  int len[FLUX3_MAX_SEGMENTS];
+  int stream[FLUX3_MAX_SEGMENTS];
+  int n;
+};
+
+__global__ void stream_ids_kernel(SegTable tab, int T, uint8_t *sid) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  int s = -1;
+  for (int i = 0; i < tab.n; ++i)
+    if (t >= tab.start[i] && t < tab.start[i] + tab.len[i]) s = tab.stream[i];
+  if (s < 0) {  // the host validated coverage; keep the kernel honest anyway
+    record_error(DEVERR_BOUNDS);
+    s = 0;
+  }
+  sid[t] = (uint8_t)s;
+}
+
+// Angles are formed in double precision (positions reach a few thousand, so a
+// float product would lose ~1e-4 rad); the tables are float32.
+__global__ void rope_tables_kernel(const float *pos, int T, double log2_theta, float *cos_tab, float *sin_tab) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * kRopePairs) return;
+  const int t = i / kRopePairs, p = i % kRopePairs;
+  const int axis = p / 16, j = p % 16;
+  const double freq = exp2(-(2.0 * j / 32.0) * log2_theta);
+  const double ang = (double)pos[(size_t)t * 4 + axis] * freq;
+  double sn, cs;
+  sincos(ang, &sn, &cs);
+  cos_tab[i] = (float)cs;
+  sin_tab[i] = (float)sn;
+}
+
+constexpr int kLnWarps = 8;
+
+__global__ void __launch_bounds__(kLnWarps * 32)
+    ln_modulate_kernel(const float *__restrict__ x, int T, const uint8_t *__restrict__ sid,
+                       const float *__restrict__ mod, float eps, __nv_bfloat16 *__restrict__ h) {
+  constexpr int kVec = kHidden / (32 * 4);  // 24 float4 per lane
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int t = blockIdx.x * kLnWarps + warp;
+  if (t >= T) return;
+  const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)t * kHidden);
+  float4 v[kVec];
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    v[i] = __ldcs(xr + i * 32 + lane);
+    sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float mean = sum * (1.0f / kHidden);
+  float sq = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, d = v[i].w - mean;
+    sq += (a * a + b * b) + (c * c + d * d);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  const float rstd = rsqrtf(sq * (1.0f / kHidden) + eps);
+  const int s = sid[t];
+  const float4 *shift = reinterpret_cast<const float4 *>(mod + (size_t)s * kModLen);
+  const float4 *scale = reinterpret_cast<const float4 *>(mod + (size_t)s * kModLen + kHidden);
+  uint2 *hr = reinterpret_cast<uint2 *>(h + (size_t)t * kHidden);
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const float4 sh = __ldg(shift + i * 32 + lane);
+    const float4 sc = __ldg(scale + i * 32 + lane);
+    const float a = fmaf((v[i].x - mean) * rstd, 1.0f + sc.x, sh.x);
+    const float b = fmaf((v[i].y - mean) * rstd, 1.0f + sc.y, sh.y);
+    const float c = fmaf((v[i].z - mean) * rstd, 1.0f + sc.z, sh.z);
+    const float d = fmaf((v[i].w - mean) * rstd, 1.0f + sc.w, sh.w);
+    hr[i * 32 + lane] = make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
+  }
+}
+
+// Diagnostics: one CTA waits on an mbarrier that nothing arrives at; the
+// bounded wait must give up after timeout_ns and record DEVERR_TIMEOUT.
+__global__ void selftest_wait_kernel(unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort, timeout_ns);
+  __syncthreads();
+}
+
+}  // namespace ew_detail
+
+cudaError_t launch_stream_ids(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, cudaStream_t s) {
+  using namespace ew_detail;
+  SegTable tab{};
+  tab.n = n_segs;
+  for (int i = 0; i < n_segs; ++i) {
+    tab.start[i] = segs[i].start;
+    tab.len[i] = segs[i].len;
+    tab.stream[i] = segs[i].stream;
+  }
+  stream_ids_kernel<<<(T + 255) / 256, 256, 0, s>>>(tab, T, sid);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_tab, float *sin_tab,
+                               cudaStream_t s) {
+  using namespace ew_detail;
+  const int n = T * kRopePairs;
+  rope_tables_kernel<<<(n + 255) / 256, 256, 0, s>>>(pos, T, log2((double)theta), cos_tab, sin_tab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ln_modulate(const float *x, int T, const uint8_t *sid, const float *mod, float eps,
+                               __nv_bfloat16 *h, cudaStream_t s) {
+  using namespace ew_detail;
+  ln_modulate_kernel<<<(T + kLnWarps - 1) / kLnWarps, kLnWarps * 32, 0, s>>>(x, T, sid, mod, eps, h);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(unsigned long long timeout_ns, cudaStream_t s) {
+  using namespace ew_detail;
+  selftest_wait_kernel<<<1, 32, 0, s>>>(timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace flux3

@@ -1,0 +1,426 @@
+// C ABI of the library (include/flux3.h): argument validation, weight
+// packing, workspace carving, tensor-map set-up and the per-block launch
+// sequence.  The kernels are compiled in this one translation unit.
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "flux3_internal.h"
+#include "ptx.cuh"
+
+#include "attention_mma.cuh"
+#include "elementwise.cuh"
+#include "gemm.cuh"
+
+struct flux3_handle {
+  flux3_config cfg;
+  int n_blocks;
+  const __nv_bfloat16 *w_in;   // [n_blocks][kInRows, kHidden]
+  const __nv_bfloat16 *w_out;  // [n_blocks][kHidden, kCatCols]
+  const float *norms;          // [n_blocks][2][kHeadDim]
+  std::vector<CUtensorMap> tm_in, tm_out;
+};
+
+namespace flux3 {
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+constexpr size_t kWInElems = (size_t)kInRows * kHidden;
+constexpr size_t kWOutElems = (size_t)kHidden * kCatCols;
+constexpr int kMaxTokensLimit = 65536;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool config_ok(const flux3_config *c) {
+  return c && c->hidden == kHidden && c->heads == kHeads && c->head_dim == kHeadDim && c->mlp_hidden == kMlp &&
+         c->n_blocks >= 1 && c->max_tokens >= 1 && c->max_tokens <= kMaxTokensLimit && c->wfmt == FLUX3_W_BF16 &&
+         c->rope_theta > 0.f && c->eps_ln > 0.f && c->eps_rms > 0.f;
+}
+
+struct Workspace {
+  uint8_t *sid;
+  float *cos_tab, *sin_tab;
+  __nv_bfloat16 *h, *qkv, *cat;
+};
+
+size_t workspace_layout(int T, uint8_t *base, Workspace *ws) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes);
+    return base ? base + o : nullptr;
+  };
+  uint8_t *sid = take((size_t)T);
+  uint8_t *cs = take((size_t)T * kRopePairs * 4);
+  uint8_t *sn = take((size_t)T * kRopePairs * 4);
+  uint8_t *h = take((size_t)T * kHidden * 2);
+  uint8_t *qkv = take((size_t)T * kQkvCols * 2);
+  uint8_t *cat = take((size_t)T * kCatCols * 2);
+  if (ws) {
+    ws->sid = sid;
+    ws->cos_tab = reinterpret_cast<float *>(cs);
+    ws->sin_tab = reinterpret_cast<float *>(sn);
+    ws->h = reinterpret_cast<__nv_bfloat16 *>(h);
+    ws->qkv = reinterpret_cast<__nv_bfloat16 *>(qkv);
+    ws->cat = reinterpret_cast<__nv_bfloat16 *>(cat);
+  }
+  return off;
+}
+
+flux3_status segments_ok(const flux3_segment *segs, int n_segs, int T) {
+  if (!segs || n_segs < 1 || n_segs > FLUX3_MAX_SEGMENTS || T < 1) return FLUX3_ERR_INVALID_ARG;
+  int expect = 0;
+  for (int i = 0; i < n_segs; ++i) {
+    if (segs[i].start != expect || segs[i].len < 1 || segs[i].stream < 0 || segs[i].stream > 2)
+      return FLUX3_ERR_INVALID_ARG;
+    expect += segs[i].len;
+    if (expect > T) return FLUX3_ERR_INVALID_ARG;
+  }
+  return expect == T ? FLUX3_OK : FLUX3_ERR_INVALID_ARG;
+}
+
+flux3_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FLUX3_OK : FLUX3_ERR_CUDA; }
+
+#define F3_TRY(expr)                         \
+  do {                                       \
+    flux3_status _st = (expr);               \
+    if (_st != FLUX3_OK) return _st;         \
+  } while (0)
+#define F3_CUDA(expr) F3_TRY(cuda_status(expr))
+
+const float *block_norms(const flux3_handle *h, int b) { return h->norms + (size_t)b * 2 * kHeadDim; }
+
+flux3_status run_in_projection(const flux3_handle *h, int b, const __nv_bfloat16 *hmod, int T, const float *cos_tab,
+                               const float *sin_tab, __nv_bfloat16 *qkv, __nv_bfloat16 *cat, cudaStream_t s) {
+  CUtensorMap tmA;
+  if (!make_tmap_bf16(&tmA, hmod, (uint64_t)T, kHidden, kBM)) return FLUX3_ERR_CUDA;
+  EpiParams ep{};
+  ep.qkv = qkv;
+  ep.cat = cat;
+  ep.cos_tab = cos_tab;
+  ep.sin_tab = sin_tab;
+  ep.qnorm = block_norms(h, b);
+  ep.knorm = block_norms(h, b) + kHeadDim;
+  ep.eps_rms = h->cfg.eps_rms;
+  return cuda_status(launch_gemm(EPI_IN_PROJ, tmA, h->tm_in[b], T, kInRows, kHidden, ep, s));
+}
+
+flux3_status run_out_projection(const flux3_handle *h, int b, const __nv_bfloat16 *cat, int T, const uint8_t *sid,
+                                const float *mod, float *x, cudaStream_t s) {
+  CUtensorMap tmA;
+  if (!make_tmap_bf16(&tmA, cat, (uint64_t)T, kCatCols, kBM)) return FLUX3_ERR_CUDA;
+  EpiParams ep{};
+  ep.x = x;
+  ep.sid = sid;
+  ep.mod = mod;
+  return cuda_status(launch_gemm(EPI_OUT_RESIDUAL, tmA, h->tm_out[b], T, kHidden, kCatCols, ep, s));
+}
+
+flux3_status forward_common(const flux3_handle *h, int first, int count, float *x, int T, const flux3_segment *segs,
+                            int n_segs, const float *pos, const float *mod, void *workspace, size_t ws_bytes,
+                            cudaStream_t s) {
+  if (!h || !x || !pos || !mod || !workspace) return FLUX3_ERR_INVALID_ARG;
+  if (first < 0 || count < 1 || first + count > h->n_blocks) return FLUX3_ERR_INVALID_ARG;
+  if (T < 1 || T > h->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
+  F3_TRY(segments_ok(segs, n_segs, T));
+  if (!aligned16(x) || !aligned16(pos) || !aligned16(mod) || !aligned16(workspace)) return FLUX3_ERR_ALIGNMENT;
+  Workspace ws;
+  if (ws_bytes < workspace_layout(T, nullptr, nullptr)) return FLUX3_ERR_WORKSPACE;
+  workspace_layout(T, static_cast<uint8_t *>(workspace), &ws);
+
+  F3_CUDA(launch_stream_ids(segs, n_segs, T, ws.sid, s));
+  F3_CUDA(launch_rope_tables(pos, T, h->cfg.rope_theta, ws.cos_tab, ws.sin_tab, s));
+  CUtensorMap tmH, tmCat;
+  if (!make_tmap_bf16(&tmH, ws.h, (uint64_t)T, kHidden, kBM)) return FLUX3_ERR_CUDA;
+  if (!make_tmap_bf16(&tmCat, ws.cat, (uint64_t)T, kCatCols, kBM)) return FLUX3_ERR_CUDA;
+  for (int b = first; b < first + count; ++b) {
+    F3_CUDA(launch_ln_modulate(x, T, ws.sid, mod, h->cfg.eps_ln, ws.h, s));
+    EpiParams ep{};
+    ep.qkv = ws.qkv;
+    ep.cat = ws.cat;
+    ep.cos_tab = ws.cos_tab;
+    ep.sin_tab = ws.sin_tab;
+    ep.qnorm = block_norms(h, b);
+    ep.knorm = block_norms(h, b) + kHeadDim;
+    ep.eps_rms = h->cfg.eps_rms;
+    F3_CUDA(launch_gemm(EPI_IN_PROJ, tmH, h->tm_in[b], T, kInRows, kHidden, ep, s));
+    F3_CUDA(launch_attention(ws.qkv, T, ws.cat, s));
+    EpiParams eo{};
+    eo.x = x;
+    eo.sid = ws.sid;
+    eo.mod = mod;
+    F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, h->tm_out[b], T, kHidden, kCatCols, eo, s));
+  }
+  return FLUX3_OK;
+}
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !aligned16(base) || (cols * 2) % 16 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (n[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 1;
+  }
+  return n[dev];
+}
+
+}  // namespace flux3
+
+using namespace flux3;
+
+extern "C" {
+
+void flux3_default_config(flux3_config *cfg) {
+  if (!cfg) return;
+  cfg->hidden = kHidden;
+  cfg->heads = kHeads;
+  cfg->head_dim = kHeadDim;
+  cfg->mlp_hidden = kMlp;
+  cfg->n_blocks = 28;
+  cfg->max_tokens = 16384;
+  cfg->wfmt = FLUX3_W_BF16;
+  cfg->rope_theta = 10000.0f;
+  cfg->eps_ln = 1e-6f;
+  cfg->eps_rms = 1e-6f;
+}
+
+size_t flux3_packed_weight_bytes(const flux3_config *cfg) {
+  if (!config_ok(cfg)) return 0;
+  return (size_t)cfg->n_blocks * (align_up(kWInElems * 2) + align_up(kWOutElems * 2) + align_up(2 * kHeadDim * 4));
+}
+
+size_t flux3_workspace_bytes(const flux3_config *cfg, int T) {
+  if (!config_ok(cfg) || T < 1 || T > cfg->max_tokens) return 0;
+  return workspace_layout(T, nullptr, nullptr);
+}
+
+flux3_status flux3_block_init(flux3_handle **out, const flux3_config *cfg, const flux3_block_weights *w, int n_blocks,
+                              void *packed, size_t packed_bytes, void *stream) {
+  if (!out) return FLUX3_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !w || !packed) return FLUX3_ERR_INVALID_ARG;
+  if (cfg->wfmt != FLUX3_W_BF16 && cfg->wfmt != FLUX3_W_NVFP4) return FLUX3_ERR_INVALID_ARG;
+  if (!config_ok(cfg)) return FLUX3_ERR_UNSUPPORTED;
+  if (n_blocks != cfg->n_blocks) return FLUX3_ERR_INVALID_ARG;
+  if (packed_bytes < flux3_packed_weight_bytes(cfg)) return FLUX3_ERR_WORKSPACE;
+  if (!aligned16(packed)) return FLUX3_ERR_ALIGNMENT;
+  for (int b = 0; b < n_blocks; ++b) {
+    const flux3_block_weights &bw = w[b];
+    const void *ps[8] = {bw.q_proj, bw.k_proj, bw.v_proj, bw.attn_out, bw.mlp_in, bw.mlp_out, bw.query_norm, bw.key_norm};
+    for (const void *p : ps) {
+      if (!p) return FLUX3_ERR_INVALID_ARG;
+      if (!aligned16(p)) return FLUX3_ERR_ALIGNMENT;
+    }
+  }
+  if (!encode_fn()) return FLUX3_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  flux3_handle *h = new (std::nothrow) flux3_handle();
+  if (!h) return FLUX3_ERR_CUDA;
+  h->cfg = *cfg;
+  h->n_blocks = n_blocks;
+  uint8_t *base = static_cast<uint8_t *>(packed);
+  const size_t in_bytes = align_up(kWInElems * 2), out_bytes = align_up(kWOutElems * 2);
+  auto *w_in = reinterpret_cast<__nv_bfloat16 *>(base);
+  auto *w_out = reinterpret_cast<__nv_bfloat16 *>(base + n_blocks * in_bytes);
+  auto *norms = reinterpret_cast<float *>(base + n_blocks * (in_bytes + out_bytes));
+  h->w_in = w_in;
+  h->w_out = w_out;
+  h->norms = norms;
+  h->tm_in.resize(n_blocks);
+  h->tm_out.resize(n_blocks);
+
+  const size_t row = (size_t)kHidden * 2;  // bytes of one [*, 3072] row
+  cudaError_t e = cudaSuccess;
+  for (int b = 0; b < n_blocks && e == cudaSuccess; ++b) {
+    const flux3_block_weights &bw = w[b];
+    uint8_t *win = reinterpret_cast<uint8_t *>(w_in) + b * in_bytes;
+    uint8_t *wout = reinterpret_cast<uint8_t *>(w_out) + b * out_bytes;
+    // in-projection rows: q | k | v | mlp_in with a and b interleaved in groups of 128
+    e = cudaMemcpyAsync(win, bw.q_proj, kHidden * row, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(win + kHidden * row, bw.k_proj, kHidden * row, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(win + 2 * kHidden * row, bw.v_proj, kHidden * row, cudaMemcpyDeviceToDevice, s);
+    const uint8_t *mi = static_cast<const uint8_t *>(bw.mlp_in);
+    uint8_t *wm = win + 3 * kHidden * row;
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(wm, 256 * row, mi, 128 * row, 128 * row, kMlp / 128, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(wm + 128 * row, 256 * row, mi + kMlp * row, 128 * row, 128 * row, kMlp / 128,
+                            cudaMemcpyDeviceToDevice, s);
+    // out-projection: [attn_out | mlp_out] concatenated along the input dimension
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(wout, kCatCols * 2, bw.attn_out, kHidden * 2, kHidden * 2, kHidden,
+                            cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(wout + kHidden * 2, kCatCols * 2, bw.mlp_out, kMlp * 2, kMlp * 2, kHidden,
+                            cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(norms + (size_t)b * 2 * kHeadDim, bw.query_norm, kHeadDim * 4, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(norms + (size_t)b * 2 * kHeadDim + kHeadDim, bw.key_norm, kHeadDim * 4,
+                          cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && (!make_tmap_bf16(&h->tm_in[b], win, kInRows, kHidden, kBN) ||
+                             !make_tmap_bf16(&h->tm_out[b], wout, kHidden, kCatCols, kBN)))
+      e = cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) {
+    delete h;
+    return FLUX3_ERR_CUDA;
+  }
+  *out = h;
+  return FLUX3_OK;
+}
+
+flux3_status flux3_block_forward(const flux3_handle *h, int block_idx, float *x, int T, const flux3_segment *segs,
+                                 int n_segs, const float *pos_ids, const float *mod, void *workspace, size_t ws_bytes,
+                                 void *stream) {
+  return forward_common(h, block_idx, 1, x, T, segs, n_segs, pos_ids, mod, workspace, ws_bytes,
+                        static_cast<cudaStream_t>(stream));
+}
+
+flux3_status flux3_stack_forward(const flux3_handle *h, int first_block, int n_blocks, float *x, int T,
+                                 const flux3_segment *segs, int n_segs, const float *pos_ids, const float *mod,
+                                 void *workspace, size_t ws_bytes, void *stream) {
+  return forward_common(h, first_block, n_blocks, x, T, segs, n_segs, pos_ids, mod, workspace, ws_bytes,
+                        static_cast<cudaStream_t>(stream));
+}
+
+flux3_status flux3_check_error(void *stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return FLUX3_ERR_CUDA;
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int));
+  if (e != cudaSuccess) return FLUX3_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return FLUX3_ERR_CUDA;
+  }
+  if (v == DEVERR_TIMEOUT) return FLUX3_ERR_TIMEOUT;
+  if (v != 0) return FLUX3_ERR_DEVICE;
+  return FLUX3_OK;
+}
+
+const char *flux3_status_string(flux3_status s) {
+  switch (s) {
+    case FLUX3_OK: return "ok";
+    case FLUX3_ERR_INVALID_ARG: return "invalid argument";
+    case FLUX3_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FLUX3_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case FLUX3_ERR_WORKSPACE: return "buffer too small";
+    case FLUX3_ERR_CUDA: return "CUDA runtime error";
+    case FLUX3_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    case FLUX3_ERR_DEVICE: return "kernel bounds check failed";
+  }
+  return "unknown status";
+}
+
+void flux3_destroy(flux3_handle *h) { delete h; }
+
+flux3_status flux3_stream_ids(const flux3_segment *segs, int n_segs, int T, uint8_t *stream_id, void *stream) {
+  if (!stream_id) return FLUX3_ERR_INVALID_ARG;
+  F3_TRY(segments_ok(segs, n_segs, T));
+  return cuda_status(launch_stream_ids(segs, n_segs, T, stream_id, static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_rope_tables(const float *pos_ids, int T, float theta, float *cos_tab, float *sin_tab,
+                               void *stream) {
+  if (!pos_ids || !cos_tab || !sin_tab || T < 1 || T > kMaxTokensLimit || !(theta > 0.f)) return FLUX3_ERR_INVALID_ARG;
+  return cuda_status(launch_rope_tables(pos_ids, T, theta, cos_tab, sin_tab, static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_ln_modulate(const float *x, int T, const uint8_t *stream_id, const float *mod, float eps, void *hout,
+                               void *stream) {
+  if (!x || !stream_id || !mod || !hout || T < 1 || T > kMaxTokensLimit || !(eps > 0.f)) return FLUX3_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(mod) || !aligned16(hout)) return FLUX3_ERR_ALIGNMENT;
+  return cuda_status(launch_ln_modulate(x, T, stream_id, mod, eps, static_cast<__nv_bfloat16 *>(hout),
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_in_projection(const flux3_handle *h, int block_idx, const void *hmod, int T, const float *cos_tab,
+                                 const float *sin_tab, void *qkv, void *cat, void *stream) {
+  if (!h || !hmod || !cos_tab || !sin_tab || !qkv || !cat) return FLUX3_ERR_INVALID_ARG;
+  if (block_idx < 0 || block_idx >= h->n_blocks || T < 1 || T > h->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
+  if (!aligned16(hmod) || !aligned16(qkv) || !aligned16(cat) || !aligned16(cos_tab) || !aligned16(sin_tab))
+    return FLUX3_ERR_ALIGNMENT;
+  return run_in_projection(h, block_idx, static_cast<const __nv_bfloat16 *>(hmod), T, cos_tab, sin_tab,
+                           static_cast<__nv_bfloat16 *>(qkv), static_cast<__nv_bfloat16 *>(cat),
+                           static_cast<cudaStream_t>(stream));
+}
+
+flux3_status flux3_attention(const void *qkv, int T, void *cat, void *stream) {
+  if (!qkv || !cat || T < 1 || T > kMaxTokensLimit) return FLUX3_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(cat)) return FLUX3_ERR_ALIGNMENT;
+  return cuda_status(launch_attention(static_cast<const __nv_bfloat16 *>(qkv), T, static_cast<__nv_bfloat16 *>(cat),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_out_projection(const flux3_handle *h, int block_idx, const void *cat, int T,
+                                  const uint8_t *stream_id, const float *mod, float *x, void *stream) {
+  if (!h || !cat || !stream_id || !mod || !x) return FLUX3_ERR_INVALID_ARG;
+  if (block_idx < 0 || block_idx >= h->n_blocks || T < 1 || T > h->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
+  if (!aligned16(cat) || !aligned16(mod) || !aligned16(x)) return FLUX3_ERR_ALIGNMENT;
+  return run_out_projection(h, block_idx, static_cast<const __nv_bfloat16 *>(cat), T, stream_id, mod, x,
+                            static_cast<cudaStream_t>(stream));
+}
+
+flux3_status flux3_gemm_bf16(const void *A, const void *B, void *C, int M, int N, int K, void *stream) {
+  if (!A || !B || !C || M < 1 || N < kBN || K < kBK || N % kBN != 0 || K % kBK != 0) return FLUX3_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return FLUX3_ERR_ALIGNMENT;
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, kBM) || !make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, kBN))
+    return FLUX3_ERR_CUDA;
+  EpiParams ep{};
+  ep.C = static_cast<__nv_bfloat16 *>(C);
+  ep.ldc = N;
+  return cuda_status(launch_gemm(EPI_STORE, ta, tb, M, N, K, ep, static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_selftest_wait_timeout(int timeout_us, void *stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return FLUX3_ERR_INVALID_ARG;
+  return cuda_status(launch_selftest_wait(1000ull * (unsigned long long)timeout_us, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// Internal launchers shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "flux3.h"
+
+namespace flux3 {
+
+// Model constants the kernels are built for (issue #2142 tensor list).
+constexpr int kHidden = 3072;
+constexpr int kHeads = 24;
+constexpr int kHeadDim = 128;
+constexpr int kMlp = 9216;
+constexpr int kModLen = 3 * kHidden;           // shift | scale | gate
+constexpr int kQkvCols = 3 * kHidden;          // q^ | k^ | v
+constexpr int kCatCols = kHidden + kMlp;       // attention | SwiGLU  (K of the out-projection)
+constexpr int kInRows = 3 * kHidden + 2 * kMlp; // rows of the packed in-projection weight
+constexpr int kRopePairs = kHeadDim / 2;       // 64 = 4 axes x 16 pairs
+
+// GEMM tile shape (tcgen05, one CTA per tile row-block of 128 x 256).
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+
+enum EpiMode : int { EPI_STORE = 0, EPI_IN_PROJ = 1, EPI_OUT_RESIDUAL = 2 };
+
+struct EpiParams {
+  // EPI_STORE
+  __nv_bfloat16 *C;
+  int ldc;
+  // EPI_IN_PROJ
+  __nv_bfloat16 *qkv;  // [M, 9216]
+  __nv_bfloat16 *cat;  // [M, 12288]
+  const float *cos_tab, *sin_tab;  // [M, 64]
+  const float *qnorm, *knorm;      // [128]
+  float eps_rms;
+  // EPI_OUT_RESIDUAL
+  float *x;             // [M, 3072]
+  const uint8_t *sid;   // [M]
+  const float *mod;     // [3, 9216]
+};
+
+// Encodes a 2-D bf16 tensor map over a row-major [rows, cols] matrix with a
+// {64 cols, box_rows} box and 128-byte swizzle.  Returns false on failure.
+bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+int num_sms();
+
+cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K,
+                        const EpiParams &ep, cudaStream_t s);
+
+cudaError_t launch_stream_ids(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, cudaStream_t s);
+cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_tab, float *sin_tab,
+                               cudaStream_t s);
+cudaError_t launch_ln_modulate(const float *x, int T, const uint8_t *sid, const float *mod, float eps,
+                               __nv_bfloat16 *h, cudaStream_t s);
+cudaError_t launch_selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
+cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s);
+
+}  // namespace flux3

@@ -1,0 +1,339 @@
+// Persistent, warp-specialised tcgen05 GEMM  C[M, N] = A[M, K] * B[N, K]^T
+// (bf16 operands, fp32 accumulation in tensor memory) with the block's fused
+// epilogues:
+//   EPI_STORE         bf16 store of C
+//   EPI_IN_PROJ       over the packed [Wq; Wk; Wv; Wmlp_in(a/b interleaved)]:
+//                     per-head RMSNorm + 4-axis RoPE of q and k, plain v, and
+//                     silu(a) * b of the MLP half
+//   EPI_OUT_RESIDUAL  x += gate[stream] * C  (fp32 residual, in place)
+//
+// Roles (192 threads): warp 0 issues TMA loads of 128x64 A and 256x64 B tiles
+// (128-byte swizzle) into a 4-stage ring; warp 1 owns the 512-column TMEM
+// allocation and issues 128x256x16 MMAs from one thread into one of two
+// accumulators; warps 2-5 drain the other accumulator through tcgen05.ld
+// (each warp reads its own 32-lane quarter, one output row per thread) and
+// run the epilogue, so the epilogue of tile i overlaps the MMAs of tile i+1.
+// Every wait is bounded (see mbar_wait); on a timeout the CTA drains its
+// in-flight copies and MMAs, frees TMEM and returns.
+
+#pragma once
+
+#include "flux3_internal.h"
+#include "ptx.cuh"
+
+namespace flux3 {
+
+namespace gemm_detail {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;   // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 512;           // two 128 x 256 fp32 accumulators
+
+struct SharedCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + sizeof(SharedCtl);
+
+__device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
+
+// Waits for `bar` to pass `parity`, with a time limit only (used while
+// draining after an abort, when the abort flag is already set).
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      record_error(DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
+  uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    d[q] = make_uint4(pack_bf16x2(f32(r[8 * q + 0]), f32(r[8 * q + 1])), pack_bf16x2(f32(r[8 * q + 2]), f32(r[8 * q + 3])),
+                      pack_bf16x2(f32(r[8 * q + 4]), f32(r[8 * q + 5])), pack_bf16x2(f32(r[8 * q + 6]), f32(r[8 * q + 7])));
+}
+
+// Epilogue of one 128 x 256 accumulator tile for the thread's row.
+// taddr: TMEM address of (this warp's lane quarter, column 0 of the tile).
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, int M, int n_blk, const EpiParams &ep) {
+  const bool live = row < M;
+  const int n0 = n_blk * kBN;
+  uint32_t r[32];
+  if constexpr (EPI == EPI_STORE) {
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      tmem_ld32(taddr + c * 32, r);
+      if (live) store_row_bf16(ep.C + (size_t)row * ep.ldc + n0 + c * 32, r);
+    }
+  } else if constexpr (EPI == EPI_OUT_RESIDUAL) {
+    const int s = live ? ep.sid[row] : 0;
+    const float4 *gate = reinterpret_cast<const float4 *>(ep.mod + (size_t)s * kModLen + 2 * kHidden + n0);
+    float4 *xr = reinterpret_cast<float4 *>(ep.x + (size_t)(live ? row : 0) * kHidden + n0);
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      tmem_ld32(taddr + c * 32, r);
+      if (live) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 g = __ldg(gate + c * 8 + q);
+          float4 xv = xr[c * 8 + q];
+          xv.x = fmaf(g.x, f32(r[4 * q + 0]), xv.x);
+          xv.y = fmaf(g.y, f32(r[4 * q + 1]), xv.y);
+          xv.z = fmaf(g.z, f32(r[4 * q + 2]), xv.z);
+          xv.w = fmaf(g.w, f32(r[4 * q + 3]), xv.w);
+          xr[c * 8 + q] = xv;
+        }
+      }
+    }
+  } else {  // EPI_IN_PROJ
+    constexpr int kQTiles = kHidden / kBN;          // 12
+    constexpr int kVEnd = 3 * kHidden / kBN;        // 36
+    if (n_blk < 2 * kQTiles) {
+      // q or k: two heads per tile; RMSNorm over the 128 dims of each head in
+      // fp32 straight from the accumulator, then RoPE on adjacent pairs; the
+      // 32 columns of chunk c are exactly RoPE axis c (t, h, w, l).
+      const float *nscale = n_blk < kQTiles ? ep.qnorm : ep.knorm;
+      const int rrow = live ? row : 0;
+      const float *cs_row = ep.cos_tab + (size_t)rrow * kRopePairs;
+      const float *sn_row = ep.sin_tab + (size_t)rrow * kRopePairs;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float ss = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(taddr + hh * 128 + c * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ss = fmaf(f32(r[i]), f32(r[i]), ss);
+        }
+        const float inv = rsqrtf(ss * (1.0f / kHeadDim) + ep.eps_rms);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(taddr + hh * 128 + c * 32, r);
+          uint32_t o[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float x0 = f32(r[2 * j]) * inv * __ldg(nscale + c * 32 + 2 * j);
+            const float x1 = f32(r[2 * j + 1]) * inv * __ldg(nscale + c * 32 + 2 * j + 1);
+            const float cs = __ldg(cs_row + c * 16 + j);
+            const float sn = __ldg(sn_row + c * 16 + j);
+            o[j] = pack_bf16x2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
+          }
+          if (live) {
+            uint4 *d = reinterpret_cast<uint4 *>(ep.qkv + (size_t)row * kQkvCols + n0 + hh * 128 + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          }
+        }
+      }
+    } else if (n_blk < kVEnd) {
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        tmem_ld32(taddr + c * 32, r);
+        if (live) store_row_bf16(ep.qkv + (size_t)row * kQkvCols + n0 + c * 32, r);
+      }
+    } else {
+      // MLP tile m holds a[128m .. 128m+127] in columns 0..127 and the matching
+      // b rows in columns 128..255 (interleaved when the weights were packed).
+      const int m = n_blk - kVEnd;
+      uint32_t b[32];
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32x2(taddr + c * 32, taddr + 128 + c * 32, r, b);
+        uint32_t o[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float a0 = f32(r[2 * j]), a1 = f32(r[2 * j + 1]);
+          const float g0 = a0 / (1.0f + __expf(-a0)) * f32(b[2 * j]);
+          const float g1 = a1 / (1.0f + __expf(-a1)) * f32(b[2 * j + 1]);
+          o[j] = pack_bf16x2(g0, g1);
+        }
+        if (live) {
+          uint4 *d = reinterpret_cast<uint4 *>(ep.cat + (size_t)row * kCatCols + kHidden + m * 128 + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
+    }
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+                int K, EpiParams ep) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *smA = smem;
+  uint8_t *smB = smem + kStages * kABytes;
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(smem + kStages * kStageBytes);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int num_m = (M + kBM - 1) / kBM;
+  const int num_n = N / kBN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&ctl->tmem_full[a], 1);
+      mbar_init(&ctl->tmem_empty[a], 128);
+    }
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+  volatile int *abort = &ctl->abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int last_phase[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m_blk = tile % num_m, n_blk = tile / num_m;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
+          tma_load_2d(smA + stage * kABytes, &tmA, &ctl->full[stage], kb * kBK, m_blk * kBM);
+          tma_load_2d(smB + stage * kBBytes, &tmB, &ctl->full[stage], kb * kBK, n_blk * kBN);
+          last_phase[stage] = (int)phase;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {  // let every copy still in flight land before the CTA exits
+        for (int s = 0; s < kStages; ++s)
+          if (last_phase[s] >= 0) drain_wait(&ctl->full[s], (uint32_t)last_phase[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16(kBM, kBN, false);
+      uint32_t stage = 0, phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1, abort)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&ctl->full[stage], phase, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(smA + stage * kABytes);
+          const uint32_t b0 = smem_addr(smB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t adesc = smem_desc(a0 + k * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bdesc = smem_desc(b0 + k * 32, 16, 1024, kSwizzle128B);
+            mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+          }
+          mma_commit(&ctl->empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) mma_commit(&ctl->tmem_full[acc]);
+      }
+      // all MMAs issued by this thread are complete once `drain` arrives
+      mma_commit(&ctl->drain);
+      drain_wait(&ctl->drain, 0);
+    }
+  } else {
+    // ---------------- epilogue warps 2..5
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int m_blk = tile % num_m, n_blk = tile / num_m;
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait(&ctl->tmem_full[acc], acc_phase, abort)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kBN;
+      epilogue_tile<EPI>(taddr, m_blk * kBM + row_in_tile, M, n_blk, ep);
+      tc_fence_before();
+      mbar_arrive(&ctl->tmem_empty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int EPI>
+cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K, const EpiParams &ep,
+                        cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = ((M + kBM - 1) / kBM) * (N / kBN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, M, N, K, ep);
+  return cudaGetLastError();
+}
+
+}  // namespace gemm_detail
+
+cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K,
+                        const EpiParams &ep, cudaStream_t s) {
+  using namespace gemm_detail;
+  switch (mode) {
+    case EPI_STORE: return launch_mode<EPI_STORE>(tmA, tmB, M, N, K, ep, s);
+    case EPI_IN_PROJ: return launch_mode<EPI_IN_PROJ>(tmA, tmB, M, N, K, ep, s);
+    case EPI_OUT_RESIDUAL: return launch_mode<EPI_OUT_RESIDUAL>(tmA, tmB, M, N, K, ep, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace flux3

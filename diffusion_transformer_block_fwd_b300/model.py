@@ -1,0 +1,87 @@
+"""Flux3Blocks: a handle plus the torch-allocated device buffers it needs
+(packed weights, workspace).  Argument marshalling only; the forward pass is
+flux3_stack_forward / flux3_block_forward of the C library."""
+
+import torch
+
+from . import (FLUX3_W_BF16, flux3_block_forward, flux3_block_init, flux3_default_config, flux3_destroy,
+               flux3_packed_weight_bytes, flux3_stack_forward, flux3_workspace_bytes)
+
+WEIGHT_KEYS = ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out", "query_norm", "key_norm")
+
+
+def _stream_ptr(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class Flux3Blocks:
+    """Joint single_blocks on one CUDA device.
+
+    weights: list (one per block) of dicts of device tensors: bf16 [out, in]
+    matrices q_proj, k_proj, v_proj, attn_out, mlp_in, mlp_out and float32
+    [128] query_norm, key_norm.  They are copied into the packed buffer at
+    construction and not referenced afterwards."""
+
+    def __init__(self, weights, max_tokens=16384, stream=None):
+        dev = weights[0]["q_proj"].device
+        self.device = dev
+        self.cfg = flux3_default_config()
+        self.cfg.n_blocks = len(weights)
+        self.cfg.max_tokens = int(max_tokens)
+        self.cfg.wfmt = FLUX3_W_BF16
+        nbytes = flux3_packed_weight_bytes(self.cfg)
+        if nbytes == 0:
+            raise ValueError("unsupported configuration")
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        ptrs = []
+        for w in weights:
+            for k in WEIGHT_KEYS[:6]:
+                assert w[k].dtype == torch.bfloat16 and w[k].is_contiguous() and w[k].device == dev, k
+            for k in WEIGHT_KEYS[6:]:
+                assert w[k].dtype == torch.float32 and w[k].is_contiguous(), k
+            ptrs.append({k: w[k].data_ptr() for k in WEIGHT_KEYS})
+        sp = _stream_ptr(stream)
+        self.handle = flux3_block_init(self.cfg, ptrs, self.packed.data_ptr(), nbytes, sp)
+        (stream or torch.cuda.current_stream()).synchronize()   # source weights may be freed after this
+        self._ws = torch.empty(0, dtype=torch.uint8, device=dev)
+
+    @property
+    def n_blocks(self):
+        return self.cfg.n_blocks
+
+    def workspace(self, T):
+        need = flux3_workspace_bytes(self.cfg, T)
+        if need == 0:
+            raise ValueError(f"T={T} out of range (max_tokens={self.cfg.max_tokens})")
+        if self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, x, segments, pos_ids, mod, first_block=0, n_blocks=None, stream=None):
+        """Applies blocks first_block .. first_block + n_blocks - 1 to x in place.
+        x: float32 [T, 3072]; pos_ids: float32 [T, 4]; mod: float32 [3, 9216]."""
+        T = x.shape[0]
+        n = self.n_blocks - first_block if n_blocks is None else n_blocks
+        for t, dt in ((x, torch.float32), (pos_ids, torch.float32), (mod, torch.float32)):
+            assert t.dtype == dt and t.is_contiguous() and t.device == self.device
+        ws = self.workspace(T)
+        sp = _stream_ptr(stream)
+        if n == 1:
+            flux3_block_forward(self.handle, first_block, x.data_ptr(), T, segments, pos_ids.data_ptr(),
+                                mod.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+        else:
+            flux3_stack_forward(self.handle, first_block, n, x.data_ptr(), T, segments, pos_ids.data_ptr(),
+                                mod.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+        return x
+
+    def close(self):
+        if getattr(self, "handle", None):
+            flux3_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

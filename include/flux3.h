@@ -1,0 +1,240 @@
+/*
+ * flux3.h -- C ABI of the B300 (sm_103a) library for the FLUX.3 Image Klein
+ * joint single_block forward pass.
+ *
+ * What the library computes (per block, for every token t of one sample):
+ *   h    = (1 + scale[s]) * LayerNorm(x) + shift[s]        LayerNorm without affine, eps 1e-6
+ *   q,k,v = h Wq^T, h Wk^T, h Wv^T                           24 heads x 128, no bias
+ *   q^, k^ = RoPE4(RMSNorm(q) * query_norm), RoPE4(RMSNorm(k) * key_norm)   per head, eps 1e-6
+ *   o    = softmax(q^ k^T / sqrt(128)) v                     all tokens attend to all tokens
+ *   a|b  = h Wmlp_in^T,  g = silu(a) * b                     a = first 9216 outputs
+ *   x'   = x + gate[s] * (o Wattn_out^T + g Wmlp_out^T)
+ * s = the token's stream (image, image_cond, txt); each stream has its own
+ * [shift | scale | gate] vector of 3 x 3072 floats.  Sources: "FLUX.3 Image
+ * Klein support" (stable-diffusion.cpp issue #2142), comment "Structure (from
+ * dit.py)" and its tensor list; "Welcome FLUX.3 Image Klein in Diffusers",
+ * sections "Inside one block", "Two stages" and "Positions in four dimensions".
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device addresses on the current device; host
+ *     pointers are ordinary process memory.  Each argument says which.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous on it; nothing synchronises except
+ *     flux3_check_error().
+ *   - All device memory (weights, packed weights, activations, workspace) is
+ *     owned by the caller.  Weights are borrowed by flux3_block_init only for
+ *     the packing copy it enqueues; the packed buffer must outlive the handle.
+ *   - Layouts are row-major, token-major: a [T, C] tensor has element (t, c) at
+ *     offset t*C + c.  bf16 is IEEE bfloat16 stored in 16 bits.
+ *   - Errors are returned as flux3_status codes, never by aborting.  Argument
+ *     errors are detected on the host before anything is enqueued.  Device-side
+ *     failures (a pipeline wait that timed out, an index out of range) set a
+ *     device error word that flux3_check_error() reads and clears.
+ */
+#ifndef FLUX3_H
+#define FLUX3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FLUX3_API __attribute__((visibility("default")))
+
+typedef enum flux3_status {
+  FLUX3_OK = 0,
+  FLUX3_ERR_INVALID_ARG = -1,   /* null pointer, bad size, bad segment table      */
+  FLUX3_ERR_UNSUPPORTED = -2,   /* configuration the kernels are not built for    */
+  FLUX3_ERR_ALIGNMENT = -3,     /* pointer not 16-byte aligned                    */
+  FLUX3_ERR_WORKSPACE = -4,     /* workspace / packed buffer smaller than needed  */
+  FLUX3_ERR_CUDA = -5,          /* a CUDA runtime call failed                     */
+  FLUX3_ERR_TIMEOUT = -6,       /* a kernel pipeline wait ran out (device word)   */
+  FLUX3_ERR_DEVICE = -7         /* a kernel's own bounds check fired (device word) */
+} flux3_status;
+
+/* Weight formats.  NVFP4 = e2m1 values with one e4m3 scale per 16 inputs and a
+ * float32 per-tensor scale ("Welcome FLUX.3 Image Klein in Diffusers", section
+ * "Single-file format checkpoints", names nvfp4 and fp8r variants). */
+typedef enum flux3_wfmt { FLUX3_W_BF16 = 0, FLUX3_W_NVFP4 = 1 } flux3_wfmt;
+
+/* Token streams ("modes"): each selects its own modulation vector. */
+typedef enum flux3_stream {
+  FLUX3_STREAM_IMAGE = 0,
+  FLUX3_STREAM_IMAGE_COND = 1,
+  FLUX3_STREAM_TXT = 2
+} flux3_stream;
+
+/* Model configuration.  The kernels are built for hidden 3072, 24 heads of
+ * 128, SwiGLU width 9216 (the shapes of the issue's tensor list); other values
+ * return FLUX3_ERR_UNSUPPORTED.  max_tokens bounds T for workspace sizing. */
+typedef struct flux3_config {
+  int hidden;       /* 3072 */
+  int heads;        /* 24   */
+  int head_dim;     /* 128  */
+  int mlp_hidden;   /* 9216 (mlp_in has 2 * mlp_hidden rows) */
+  int n_blocks;     /* blocks held by a handle, 28 for the joint stack */
+  int max_tokens;   /* largest T a forward call may use (<= 65536) */
+  int wfmt;         /* flux3_wfmt */
+  float rope_theta; /* 10000 */
+  float eps_ln;     /* 1e-6 */
+  float eps_rms;    /* 1e-6 */
+} flux3_config;
+
+/* One block's weights as the checkpoint stores them: device bf16 matrices of
+ * shape [out, in] (row-major, no bias) and device float32 [128] norm scales.
+ * Pointers must be 16-byte aligned. */
+typedef struct flux3_block_weights {
+  const void *q_proj;     /* [3072, 3072]  */
+  const void *k_proj;     /* [3072, 3072]  */
+  const void *v_proj;     /* [3072, 3072]  */
+  const void *attn_out;   /* [3072, 3072]  */
+  const void *mlp_in;     /* [18432, 3072] */
+  const void *mlp_out;    /* [3072, 9216]  */
+  const float *query_norm;/* [128] */
+  const float *key_norm;  /* [128] */
+} flux3_block_weights;
+
+/* A contiguous run of tokens of one stream.  A forward call's segments must be
+ * in increasing order, non-overlapping, non-empty, and cover [0, T) exactly;
+ * at most FLUX3_MAX_SEGMENTS of them.  Any stream order is accepted. */
+typedef struct flux3_segment {
+  int start;
+  int len;
+  int stream;   /* flux3_stream */
+} flux3_segment;
+
+#define FLUX3_MAX_SEGMENTS 32
+
+typedef struct flux3_handle flux3_handle;
+
+/* Fills *cfg with the FLUX.3 Image Klein joint-block configuration
+ * (3072 / 24 / 128 / 9216, 28 blocks, max_tokens 16384, bf16, theta 1e4,
+ * eps 1e-6). */
+FLUX3_API void flux3_default_config(flux3_config *cfg);
+
+/* Bytes of the caller-owned buffer flux3_block_init packs the weights into
+ * (per block: the q/k/v/mlp_in rows concatenated, the attn_out/mlp_out
+ * columns concatenated, and the two norm scales).  0 if cfg is invalid. */
+FLUX3_API size_t flux3_packed_weight_bytes(const flux3_config *cfg);
+
+/* Bytes of workspace a forward call with T tokens needs (stream ids, RoPE
+ * tables, modulated input, q/k/v, attention + SwiGLU output).  0 if cfg is
+ * invalid or T is out of range. */
+FLUX3_API size_t flux3_workspace_bytes(const flux3_config *cfg, int T);
+
+/* Creates a handle for n_blocks blocks (n_blocks == cfg->n_blocks).
+ *   w        host array of n_blocks weight sets (device pointers inside)
+ *   packed   device buffer of flux3_packed_weight_bytes(cfg) bytes (caller-owned)
+ * Enqueues the packing copies on `stream`; the handle may be used for forward
+ * calls on that stream right away (other streams: synchronise first).
+ * Returns FLUX3_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT / _WORKSPACE / _CUDA. */
+FLUX3_API flux3_status flux3_block_init(flux3_handle **out, const flux3_config *cfg,
+                                        const flux3_block_weights *w, int n_blocks,
+                                        void *packed, size_t packed_bytes, void *stream);
+
+/* One joint block (block_idx of the handle) applied in place.
+ *   x        device float32 [T, 3072]: the residual stream, updated in place
+ *   segs     host array of n_segs segments covering [0, T)
+ *   pos_ids  device float32 [T, 4]: RoPE ids (t, h, w, l) per token
+ *   mod      device float32 [3, 9216]: per stream (image, image_cond, txt) the
+ *            shift | scale | gate vectors, each 3072 long
+ *   workspace device buffer of at least flux3_workspace_bytes(cfg, T) bytes
+ * 1 <= T <= cfg->max_tokens. */
+FLUX3_API flux3_status flux3_block_forward(const flux3_handle *h, int block_idx, float *x, int T,
+                                           const flux3_segment *segs, int n_segs,
+                                           const float *pos_ids, const float *mod,
+                                           void *workspace, size_t ws_bytes, void *stream);
+
+/* Blocks first_block .. first_block + n_blocks - 1 applied in sequence to the
+ * residual stream x (same arguments as flux3_block_forward).  All blocks use
+ * the same `mod` (the joint blocks share one set of stream modulations: the
+ * modulation tensors of the issue's list carry no block index).  The stream
+ * ids and RoPE tables are built once per call. */
+FLUX3_API flux3_status flux3_stack_forward(const flux3_handle *h, int first_block, int n_blocks,
+                                           float *x, int T, const flux3_segment *segs, int n_segs,
+                                           const float *pos_ids, const float *mod,
+                                           void *workspace, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device error word.
+ * Returns FLUX3_OK, FLUX3_ERR_TIMEOUT, FLUX3_ERR_DEVICE or FLUX3_ERR_CUDA. */
+FLUX3_API flux3_status flux3_check_error(void *stream);
+
+FLUX3_API const char *flux3_status_string(flux3_status s);
+
+/* Frees the handle's host state.  Does not touch caller-owned device memory. */
+FLUX3_API void flux3_destroy(flux3_handle *h);
+
+/* ------------------------------------------------------------------------
+ * Step entry points: the stages of one block, exposed so each can be checked
+ * on its own.  flux3_block_forward is exactly these in sequence.
+ * ------------------------------------------------------------------------ */
+
+/* Per-token stream id from the segment table (validated as above).
+ *   stream_id  device uint8 [T] (output) */
+FLUX3_API flux3_status flux3_stream_ids(const flux3_segment *segs, int n_segs, int T,
+                                        uint8_t *stream_id, void *stream);
+
+/* RoPE tables: for token t, pair p = 16 a + j (axis a in t, h, w, l; j < 16):
+ *   angle = pos_ids[t, a] * theta^(-2j/32);  cos_tab[t, p], sin_tab[t, p].
+ * The 4 axes of 32 dims and theta are from the issue's "Structure" comment;
+ * the frequency ladder within an axis is the standard RoPE one.
+ *   pos_ids device float32 [T, 4]; cos_tab, sin_tab device float32 [T, 64] (outputs) */
+FLUX3_API flux3_status flux3_rope_tables(const float *pos_ids, int T, float theta,
+                                         float *cos_tab, float *sin_tab, void *stream);
+
+/* LayerNorm (no affine) + per-stream modulation:
+ *   h[t] = (1 + scale[s(t)]) * (x[t] - mean) / sqrt(var + eps) + shift[s(t)]
+ *   x device float32 [T, 3072]; stream_id device uint8 [T];
+ *   mod device float32 [3, 9216]; h device bf16 [T, 3072] (output). */
+FLUX3_API flux3_status flux3_ln_modulate(const float *x, int T, const uint8_t *stream_id,
+                                         const float *mod, float eps, void *h, void *stream);
+
+/* The block's input projections with their fused epilogues (one tensor-core
+ * GEMM over the concatenated [Wq; Wk; Wv; Wmlp_in] rows):
+ *   qkv[t, 0:3072]      = RoPE4(RMSNorm(h Wq^T) * query_norm)   per head (bf16)
+ *   qkv[t, 3072:6144]   = RoPE4(RMSNorm(h Wk^T) * key_norm)     per head (bf16)
+ *   qkv[t, 6144:9216]   = h Wv^T                                 (bf16)
+ *   cat[t, 3072:12288]  = silu(a) * b,  [a | b] = h Wmlp_in^T    (bf16)
+ *   h device bf16 [T, 3072]; cos_tab/sin_tab from flux3_rope_tables;
+ *   qkv device bf16 [T, 9216]; cat device bf16 [T, 12288] (columns 0..3071
+ *   are left untouched: the attention writes them). */
+FLUX3_API flux3_status flux3_in_projection(const flux3_handle *h, int block_idx, const void *hmod,
+                                           int T, const float *cos_tab, const float *sin_tab,
+                                           void *qkv, void *cat, void *stream);
+
+/* Bidirectional attention over all T tokens, per head (24 x 128), scale
+ * 1/sqrt(128), no mask:
+ *   cat[t, 128 h : 128 h + 128] = softmax(q^_h k^_h^T / sqrt(128)) v_h
+ *   qkv device bf16 [T, 9216] laid out as above; cat device bf16 [T, 12288]
+ *   (only columns 0..3071 are written). */
+FLUX3_API flux3_status flux3_attention(const void *qkv, int T, void *cat, void *stream);
+
+/* Output projection and gated residual (one GEMM with K = 3072 + 9216 over
+ * cat = [attention | SwiGLU] against [Wattn_out | Wmlp_out]):
+ *   x[t] += gate[s(t)] * (cat[t] [Wattn_out | Wmlp_out]^T)
+ *   cat device bf16 [T, 12288]; stream_id device uint8 [T];
+ *   mod device float32 [3, 9216]; x device float32 [T, 3072] (in place). */
+FLUX3_API flux3_status flux3_out_projection(const flux3_handle *h, int block_idx, const void *cat,
+                                            int T, const uint8_t *stream_id, const float *mod,
+                                            float *x, void *stream);
+
+/* Plain tensor-core GEMM C = A B^T (fp32 accumulation, bf16 result), the core
+ * the projections are built on.  A device bf16 [M, K], B device bf16 [N, K],
+ * C device bf16 [M, N]; M >= 1, N % 256 == 0, K % 64 == 0, 16-byte aligned. */
+FLUX3_API flux3_status flux3_gemm_bf16(const void *A, const void *B, void *C, int M, int N, int K,
+                                       void *stream);
+
+/* Diagnostics for the failure path: launches one CTA that waits on a pipeline
+ * barrier nothing ever arrives at.  The wait gives up after timeout_us
+ * (1 .. 1e6) and records a timeout in the device error word, exactly as a
+ * stalled pipeline in a forward kernel would; flux3_check_error() then
+ * returns FLUX3_ERR_TIMEOUT and the CUDA context stays usable. */
+FLUX3_API flux3_status flux3_selftest_wait_timeout(int timeout_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLUX3_H */

@@ -1,0 +1,82 @@
+"""Shared helpers of the GPU parity tests: device buffers from the seeded
+generators, and the comparison criteria.
+
+Tolerances:
+* Block / stack outputs x' (the stated criterion): max|err| <= 2e-2 * RMS(x')
+  and cosine >= 0.9995.  Because x' = x + gate * y is dominated by the input,
+  the update delta = x' - x is also held to max|err| <= 5e-2 * RMS(delta) and
+  cosine >= 0.9995 (derivation: about eight bf16 roundings of ~2^-9 relative
+  each on the path give ~3e-3 RMS relative error; the maximum over ~1e7
+  Gaussian-tailed elements is ~6 sigma, i.e. ~2e-2, so 5e-2 leaves margin
+  while a dropped term or a wrong index costs far more).
+* Single steps whose only rounding is the final bf16 store:
+  |err| <= 2^-8 |ref| + slack, elementwise.
+"""
+
+import numpy as np
+import torch
+
+import synth
+
+DEV = "cuda"
+
+
+def stats(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(got - ref)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    denom = float(np.linalg.norm(got) * np.linalg.norm(ref))
+    cos = float(np.sum(got * ref) / denom) if denom > 0 else 1.0
+    return float(err.max()) if err.size else 0.0, rms, cos
+
+
+def assert_close(got, ref, max_rel=2e-2, cos_min=0.9995, what=""):
+    mx, rms, cos = stats(got, ref)
+    assert mx <= max_rel * rms, f"{what}: max|err| {mx:.3e} > {max_rel} * RMS {rms:.3e} (cos {cos:.7f})"
+    assert cos >= cos_min, f"{what}: cosine {cos:.7f} < {cos_min}"
+
+
+def assert_bf16_elementwise(got, ref, slack, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    bound = 2.0 ** -8 * np.abs(ref) + slack
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside 2^-8|ref| + {slack:.2e}; "
+                           f"worst {np.abs(got - ref)[bad].max():.3e}")
+
+
+def assert_block_output(got, ref, x_in, what=""):
+    """The stated criterion on x' and the derived one on the update."""
+    assert_close(got, ref, 2e-2, 0.9995, what + " x'")
+    x_in = np.asarray(x_in, np.float64)
+    assert_close(np.asarray(got, np.float64) - x_in, np.asarray(ref, np.float64) - x_in, 5e-2, 0.9995,
+                 what + " update")
+
+
+def f64(t):
+    return synth.to_f64(t)
+
+
+def weights_f64(w):
+    return {k: f64(v) for k, v in w.items()}
+
+
+def layout_tensors(lay):
+    pos = torch.from_numpy(lay.pos).to(DEV)
+    sid = torch.from_numpy(lay.stream_id).to(DEV)
+    return pos, sid
+
+
+def sample_rows(T, segments, n_random=24, seed=0):
+    """Rows to check at full size: both ends of every segment, the ragged
+    tail tile, and random rows."""
+    rows = set()
+    for s, n, _ in segments:
+        rows.update({s, s + 1, s + n - 2, s + n - 1})
+    tail0 = (T // 128) * 128 if T % 128 else T - 128
+    rows.update(range(max(0, tail0), min(T, tail0 + 4)))
+    rows.update(range(max(0, T - 3), T))
+    rng = np.random.default_rng(seed)
+    rows.update(rng.integers(0, T, n_random).tolist())
+    return np.array(sorted(r for r in rows if 0 <= r < T))

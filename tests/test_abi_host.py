@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, every
+entry point the header declares is exported, configuration and sizing
+helpers, and argument validation that returns before anything is enqueued."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import diffusion_transformer_block_fwd_b300 as F3
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from diffusion_transformer_block_fwd_b300 import build
+    build.build()
+
+
+def header_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"FLUX3_API\s+[\w\s\*]+?\b(flux3_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for must in ("flux3_block_init", "flux3_block_forward", "flux3_stack_forward", "flux3_check_error",
+                 "flux3_workspace_bytes", "flux3_packed_weight_bytes"):
+        assert must in names
+    assert sorted(F3.EXPORTED) == names
+
+
+def test_library_exports_every_declared_symbol():
+    L = F3.lib()
+    for n in header_functions():
+        assert hasattr(L, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", F3.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (flux3_\w+)", out))
+    assert exported == set(header_functions())
+
+
+def test_default_config_and_sizes():
+    cfg = F3.flux3_default_config()
+    assert (cfg.hidden, cfg.heads, cfg.head_dim, cfg.mlp_hidden, cfg.n_blocks) == (3072, 24, 128, 9216, 28)
+    assert abs(cfg.rope_theta - 1e4) < 1e-3 and abs(cfg.eps_ln - 1e-6) < 1e-12 and abs(cfg.eps_rms - 1e-6) < 1e-12
+    per_block = (27648 * 3072 + 3072 * 12288) * 2 + 256 * 4
+    assert F3.flux3_packed_weight_bytes(cfg) >= 28 * per_block
+    assert F3.flux3_packed_weight_bytes(cfg) < 28 * (per_block + 3 * 256)
+    ws = F3.flux3_workspace_bytes(cfg, 4608)
+    assert ws >= 4608 * (1 + 2 * 64 * 4 + (3072 + 9216 + 12288) * 2)
+    assert F3.flux3_workspace_bytes(cfg, 0) == 0
+    assert F3.flux3_workspace_bytes(cfg, cfg.max_tokens + 1) == 0
+    bad = F3.flux3_default_config()
+    bad.hidden = 2048
+    assert F3.flux3_packed_weight_bytes(bad) == 0
+
+
+def test_status_strings():
+    for s in range(-7, 1):
+        assert F3.status_string(s)
+    assert F3.status_string(0) == "ok"
+
+
+def _segs(lst):
+    return F3.segments_array(lst), len(lst)
+
+
+@pytest.mark.parametrize("segments,T", [
+    ([], 10),                                   # no segments
+    ([(0, 5, 0), (6, 4, 2)], 10),                # gap
+    ([(0, 5, 0), (4, 6, 2)], 10),                # overlap
+    ([(0, 5, 0), (5, 4, 2)], 10),                # short of T
+    ([(0, 5, 0), (5, 6, 2)], 10),                # past T
+    ([(0, 10, 3)], 10),                          # bad stream
+    ([(0, 0, 0), (0, 10, 1)], 10),               # empty segment
+    ([(i, 1, 0) for i in range(33)], 33),        # too many
+])
+def test_segment_validation_rejects_bad_tables(segments, T):
+    arr, n = _segs(segments)
+    st = F3.lib().flux3_stream_ids(arr, n, T, ctypes.c_void_p(16), None)
+    assert st == F3.FLUX3_ERR_INVALID_ARG
+
+
+def test_forward_argument_validation_before_any_launch():
+    L = F3.lib()
+    arr, n = _segs([(0, 8, 0)])
+    # null handle
+    assert L.flux3_block_forward(None, 0, 16, 8, arr, n, 16, 16, 16, 1 << 20, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_stack_forward(None, 0, 28, 16, 8, arr, n, 16, 16, 16, 1 << 20, None) == F3.FLUX3_ERR_INVALID_ARG
+    # init: null output, null weights, wrong block count, small packed buffer, misaligned pointers
+    cfg = F3.flux3_default_config()
+    cfg.n_blocks = 1
+    h = ctypes.c_void_p()
+    w = (F3.flux3_block_weights * 1)()
+    assert L.flux3_block_init(None, ctypes.byref(cfg), w, 1, 256, 1 << 40, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_block_init(ctypes.byref(h), ctypes.byref(cfg), w, 1, 256, 1 << 40, None) == F3.FLUX3_ERR_INVALID_ARG
+    for k, _ in F3.flux3_block_weights._fields_:
+        setattr(w[0], k, 4096)
+    assert L.flux3_block_init(ctypes.byref(h), ctypes.byref(cfg), w, 2, 256, 1 << 40, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_block_init(ctypes.byref(h), ctypes.byref(cfg), w, 1, 256, 1024, None) == F3.FLUX3_ERR_WORKSPACE
+    assert L.flux3_block_init(ctypes.byref(h), ctypes.byref(cfg), w, 1, 264, 1 << 40, None) == F3.FLUX3_ERR_ALIGNMENT
+    w[0].mlp_in = 4100
+    assert L.flux3_block_init(ctypes.byref(h), ctypes.byref(cfg), w, 1, 256, 1 << 40, None) == F3.FLUX3_ERR_ALIGNMENT
+    bad = F3.flux3_default_config()
+    bad.heads = 16
+    assert L.flux3_block_init(ctypes.byref(h), ctypes.byref(bad), w, 28, 256, 1 << 40, None) == F3.FLUX3_ERR_UNSUPPORTED
+    assert h.value is None
+    # step entry points
+    assert L.flux3_gemm_bf16(16, 16, 16, 128, 200, 64, None) == F3.FLUX3_ERR_INVALID_ARG     # N % 256
+    assert L.flux3_gemm_bf16(16, 16, 16, 128, 256, 96, None) == F3.FLUX3_ERR_INVALID_ARG     # K % 64
+    assert L.flux3_gemm_bf16(18, 16, 16, 128, 256, 64, None) == F3.FLUX3_ERR_ALIGNMENT
+    assert L.flux3_attention(16, 0, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_ln_modulate(16, 4, 16, 16, ctypes.c_float(0.0), 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_rope_tables(16, 4, ctypes.c_float(-1.0), 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_selftest_wait_timeout(0, None) == F3.FLUX3_ERR_INVALID_ARG

@@ -1,0 +1,71 @@
+"""The 28-block stack: parity with the oracle run from the same inputs (no
+GPU value ever feeds the oracle) at a size the oracle finishes in seconds,
+and properties at the full 6656-token size."""
+
+import numpy as np
+import pytest
+import torch
+
+import diffusion_transformer_block_fwd_b300 as F3
+import oracle as O
+import synth
+from _f3 import DEV, assert_block_output, f64, layout_tensors, weights_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def stack28():
+    ws = [synth.block_weights(4321, b, device=DEV) for b in range(28)]
+    blocks = F3.Flux3Blocks(ws, max_tokens=16384)
+    return ws, blocks
+
+
+def _sync_ok():
+    assert F3.flux3_check_error(torch.cuda.current_stream().cuda_stream) == 0
+
+
+def test_stack28_small_against_oracle_every_block(stack28):
+    """Two consecutive calls (fresh modulation each, like two sampler steps) of
+    the 28 blocks on 96 tokens; GPU and oracle each run the whole chain, and
+    the residual stream is compared after every block."""
+    ws, blocks = stack28
+    lay = synth.build_layout(synth.WORKLOADS["block_t96"]["spec"])
+    pos, _ = layout_tensors(lay)
+    x = synth.activations(77, lay.T, device=DEV)
+    xo = f64(x)
+    xg = x.clone()
+    for call in range(2):
+        mods = synth.modulation(77, call=call, device=DEV)
+        m64 = f64(mods)
+        for b in range(28):
+            x_in = xo
+            blocks.forward(xg, lay.segments, pos, mods, first_block=b, n_blocks=1)
+            xo = O.single_block(xo, weights_f64(ws[b]), m64, lay.stream_id, lay.pos.astype(np.float64))
+            _sync_ok()
+            assert_block_output(f64(xg), xo, x_in, f"call {call} block {b}")
+
+
+def test_stack28_full_size_properties(stack28):
+    _, blocks = stack28
+    lay = synth.build_layout(synth.WORKLOADS["stack28_1024sq_2ref512_t6656"]["spec"])
+    pos, _ = layout_tensors(lay)
+    x = synth.activations(78, lay.T, device=DEV)
+    mods = synth.modulation(78, device=DEV)
+    a = x.clone()
+    blocks.forward(a, lay.segments, pos, mods)
+    _sync_ok()
+    assert torch.isfinite(a).all()
+    # the stack is the 28 blocks in sequence, bit for bit
+    b = x.clone()
+    for i in range(28):
+        blocks.forward(b, lay.segments, pos, mods, first_block=i, n_blocks=1)
+    _sync_ok()
+    assert torch.equal(a, b)
+    # gates zero -> every block is the identity
+    m0 = mods.clone()
+    m0[:, 6144:] = 0.0
+    c = x.clone()
+    blocks.forward(c, lay.segments, pos, m0)
+    _sync_ok()
+    assert torch.equal(c, x)

@@ -1,0 +1,189 @@
+"""Parity of each step of the block (through the C ABI) against the CPU
+oracle, on seeded inputs that span several tiles and a ragged tail."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import diffusion_transformer_block_fwd_b300 as F3
+import oracle as O
+import synth
+from _f3 import (DEV, assert_bf16_elementwise, assert_close, f64, layout_tensors, sample_rows, weights_f64)
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [("txt", 37), ("image", (9, 11)), ("image_cond", (5, 7))]          # T = 171, three streams
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+@pytest.fixture(scope="module")
+def block1():
+    w = synth.block_weights(7, 0, device=DEV)
+    blocks = F3.Flux3Blocks([w], max_tokens=16384)
+    return w, blocks
+
+
+def test_stream_ids_bit_exact():
+    for spec in (RAGGED, synth.WORKLOADS["stack28_nvfp4_1024sq_10ref512_t14848"]["spec"], [("image", (1, 1))]):
+        lay = synth.build_layout(spec)
+        out = torch.full((lay.T,), 255, dtype=torch.uint8, device=DEV)
+        F3.flux3_stream_ids(lay.segments, lay.T, out.data_ptr(), _stream())
+        assert F3.flux3_check_error(_stream()) == 0
+        assert np.array_equal(out.cpu().numpy(), lay.stream_id)
+
+
+def test_rope_tables_match_oracle_angles():
+    lay = synth.build_layout(synth.WORKLOADS["stack28_nvfp4_1024sq_10ref512_t14848"]["spec"])
+    rng = np.random.default_rng(3)
+    extra = np.stack([rng.integers(0, 5, 500), rng.integers(0, 128, 500) * 0.5, rng.integers(0, 128, 500) * 0.5,
+                      rng.integers(-4096, 4096, 500)], 1).astype(np.float32)
+    pos = np.concatenate([lay.pos, extra])
+    T = pos.shape[0]
+    pd = torch.from_numpy(pos).to(DEV)
+    cs = torch.empty((T, 64), device=DEV)
+    sn = torch.empty((T, 64), device=DEV)
+    F3.flux3_rope_tables(pd.data_ptr(), T, 1e4, cs.data_ptr(), sn.data_ptr(), _stream())
+    ang = O.rope_angles(pos.astype(np.float64))
+    assert np.abs(cs.cpu().numpy() - np.cos(ang)).max() < 1e-6
+    assert np.abs(sn.cpu().numpy() - np.sin(ang)).max() < 1e-6
+
+
+@pytest.mark.parametrize("T", [1, 37, 171, 4608])
+def test_ln_modulate(T):
+    lay = synth.build_layout(RAGGED) if T == 171 else None
+    x = synth.activations(11, T, device=DEV) * 1.7 + 0.3
+    mods = synth.modulation(11, device=DEV)
+    sid_np = lay.stream_id if lay else (np.arange(T) % 3).astype(np.uint8)
+    sid = torch.from_numpy(sid_np).to(DEV)
+    h = torch.empty((T, 3072), dtype=torch.bfloat16, device=DEV)
+    F3.flux3_ln_modulate(x.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), 1e-6, h.data_ptr(), _stream())
+    assert F3.flux3_check_error(_stream()) == 0
+    ref = O.modulate(f64(x), f64(mods), sid_np)
+    assert_bf16_elementwise(f64(h), ref, 1e-4, "ln_modulate")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (100, 512, 192), (128, 256, 3072), (129, 768, 3072),
+                                   (300, 1024, 640), (1000, 256, 12288), (4608, 3072, 3072)])
+def test_gemm_bf16(M, N, K):
+    A = synth.bf16_matrix(1, M, K, device=DEV)
+    B = synth.bf16_matrix(2, N, K, device=DEV, std=0.05)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    F3.flux3_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _stream())
+    assert F3.flux3_check_error(_stream()) == 0
+    a, b = f64(A), f64(B)
+    rows = np.arange(M) if M <= 1000 else sample_rows(M, [(0, M, 0)], 64)
+    ref = a[rows] @ b.T
+    absprod = np.abs(a[rows]) @ np.abs(b).T
+    assert_bf16_elementwise(f64(C)[rows], ref, 2e-5 * absprod, f"gemm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("T", [96, 171, 4608])
+def test_in_projection(block1, T):
+    w, blocks = block1
+    if T == 171:
+        lay = synth.build_layout(RAGGED)
+    elif T == 96:
+        lay = synth.build_layout(synth.WORKLOADS["block_t96"]["spec"])
+    else:
+        lay = synth.build_layout(synth.WORKLOADS["block_1024sq_t4608"]["spec"])
+    pos, _ = layout_tensors(lay)
+    hmod = synth.bf16_matrix(5, T, 3072, device=DEV)
+    cs = torch.empty((T, 64), device=DEV)
+    sn = torch.empty((T, 64), device=DEV)
+    F3.flux3_rope_tables(pos.data_ptr(), T, 1e4, cs.data_ptr(), sn.data_ptr(), _stream())
+    qkv = torch.full((T, 9216), float("nan"), dtype=torch.bfloat16, device=DEV)
+    cat = torch.full((T, 12288), float("nan"), dtype=torch.bfloat16, device=DEV)
+    F3.flux3_in_projection(blocks.handle, 0, hmod.data_ptr(), T, cs.data_ptr(), sn.data_ptr(), qkv.data_ptr(),
+                           cat.data_ptr(), _stream())
+    assert F3.flux3_check_error(_stream()) == 0
+    wf = weights_f64(w)
+    rows = np.arange(T) if T <= 200 else sample_rows(T, lay.segments)
+    h64 = f64(hmod)
+    hr = h64[rows]
+    pr = lay.pos[rows].astype(np.float64)
+    d = 128
+    q = O.apply_rope(O.rms_norm((hr @ wf["q_proj"].T).reshape(-1, 24, d), wf["query_norm"]), pr).reshape(-1, 3072)
+    k = O.apply_rope(O.rms_norm((hr @ wf["k_proj"].T).reshape(-1, 24, d), wf["key_norm"]), pr).reshape(-1, 3072)
+    v = hr @ wf["v_proj"].T
+    g = O.swiglu(hr @ wf["mlp_in"].T)
+    got = f64(qkv)[rows]
+    gcat = f64(cat)[rows]
+    for name, gv, rv in (("q^", got[:, :3072], q), ("k^", got[:, 3072:6144], k), ("v", got[:, 6144:], v),
+                         ("g", gcat[:, 3072:], g)):
+        rms = float(np.sqrt(np.mean(rv * rv)))
+        assert_bf16_elementwise(gv, rv, 2e-3 * rms, f"in_projection {name} T={T}")
+        assert_close(gv, rv, 1e-2, 0.99995, f"in_projection {name} T={T}")
+    assert torch.isnan(cat[:, :3072].float()).all(), "attention columns must be left untouched"
+
+
+def _qkv_inputs(T, seed, q_scale=1.0):
+    qkv = synth.bf16_matrix(seed, T, 9216, device=DEV)
+    if q_scale != 1.0:
+        qkv[:, :3072] = (qkv[:, :3072].float() * q_scale).to(torch.bfloat16)
+    return qkv
+
+
+@pytest.mark.parametrize("T,q_scale", [(1, 1.0), (5, 1.0), (64, 1.0), (65, 1.0), (127, 1.0), (128, 1.0),
+                                       (129, 1.0), (300, 1.0), (1000, 1.0), (300, 6.0), (1000, 12.0)])
+def test_attention(T, q_scale):
+    qkv = _qkv_inputs(T, 21 + T, q_scale)
+    cat = torch.full((T, 12288), float("nan"), dtype=torch.bfloat16, device=DEV)
+    F3.flux3_attention(qkv.data_ptr(), T, cat.data_ptr(), _stream())
+    assert F3.flux3_check_error(_stream()) == 0
+    a = f64(qkv).reshape(T, 3, 24, 128)
+    ref = O.attention(a[:, 0], a[:, 1], a[:, 2]).reshape(T, 3072)
+    got = f64(cat)[:, :3072]
+    assert_close(got, ref, 1e-2, 0.9999, f"attention T={T} qscale={q_scale}")
+    assert torch.isnan(cat[:, 3072:].float()).all(), "SwiGLU columns must be left untouched"
+
+
+@pytest.mark.parametrize("T", [4608, 8704])
+def test_attention_full_size_sampled_rows(T):
+    qkv = _qkv_inputs(T, 31, 3.0)
+    cat = torch.empty((T, 12288), dtype=torch.bfloat16, device=DEV)
+    F3.flux3_attention(qkv.data_ptr(), T, cat.data_ptr(), _stream())
+    assert F3.flux3_check_error(_stream()) == 0
+    rows = sample_rows(T, [(0, T, 0)], 40)
+    a = f64(qkv).reshape(T, 3, 24, 128)
+    ref = O.attention(a[rows, 0], a[:, 1], a[:, 2]).reshape(len(rows), 3072)
+    assert_close(f64(cat)[rows, :3072], ref, 1e-2, 0.9999, f"attention T={T}")
+
+
+@pytest.mark.parametrize("T", [96, 171, 4608])
+def test_out_projection(block1, T):
+    w, blocks = block1
+    lay = synth.build_layout(RAGGED if T == 171 else synth.WORKLOADS[
+        "block_t96" if T == 96 else "block_1024sq_t4608"]["spec"])
+    _, sid = layout_tensors(lay)
+    cat = synth.bf16_matrix(9, T, 12288, device=DEV)
+    x = synth.activations(9, T, device=DEV)
+    x0 = x.clone()
+    mods = synth.modulation(9, device=DEV)
+    F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), x.data_ptr(),
+                            _stream())
+    assert F3.flux3_check_error(_stream()) == 0
+    wf = weights_f64(w)
+    rows = np.arange(T) if T <= 200 else sample_rows(T, lay.segments)
+    c = f64(cat)[rows]
+    y = c[:, :3072] @ wf["attn_out"].T + c[:, 3072:] @ wf["mlp_out"].T
+    gate = f64(mods)[lay.stream_id[rows], 6144:]
+    ref_delta = gate * y
+    got_delta = f64(x)[rows] - f64(x0)[rows]
+    assert_close(got_delta, ref_delta, 1e-3, 0.999999, f"out_projection T={T}")
+
+
+def test_timeout_path_reports_and_context_survives():
+    F3.flux3_selftest_wait_timeout(20000, _stream())
+    assert F3.flux3_check_error(_stream()) == F3.FLUX3_ERR_TIMEOUT
+    assert F3.flux3_check_error(_stream()) == F3.FLUX3_OK          # the word was cleared
+    A = synth.bf16_matrix(1, 128, 64, device=DEV)
+    C = torch.empty((128, 256), dtype=torch.bfloat16, device=DEV)
+    B = synth.bf16_matrix(2, 256, 64, device=DEV)
+    F3.flux3_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), 128, 256, 64, _stream())
+    assert F3.flux3_check_error(_stream()) == F3.FLUX3_OK
+    np.testing.assert_allclose(f64(C), f64(A) @ f64(B).T, rtol=2 ** -8, atol=1e-3)
