@@ -3,14 +3,19 @@ generators, and the comparison criteria.
 
 Tolerances:
 * Block / stack outputs x' (the stated criterion): max|err| <= 2e-2 * RMS(x')
-  and cosine >= 0.9995.  Because x' = x + gate * y is dominated by the input,
-  the update delta = x' - x is also held to max|err| <= 5e-2 * RMS(delta) and
-  cosine >= 0.9995 (derivation: about eight bf16 roundings of ~2^-9 relative
-  each on the path give ~3e-3 RMS relative error; the maximum over ~1e7
-  Gaussian-tailed elements is ~6 sigma, i.e. ~2e-2, so 5e-2 leaves margin
-  while a dropped term or a wrong index costs far more).
+  and cosine >= 0.9995.
+* Because x' = x + gate * y is dominated by the input, the update
+  delta = gate * y is held to more: cosine >= 0.9999, and elementwise
+  |err| <= |gate| * 5e-2 * RMS(y) + 1e-5 * RMS(delta).  Derivation: the GPU
+  rounds h, q/k/v, P, the attention output and g to bf16 (relative error
+  <= 2^-8 each, ~2.3e-3 RMS); carried through the projections that is ~4e-3
+  RMS relative error in y, whose Gaussian-tailed maximum over ~1e7 elements
+  (~6 sigma) is ~2.4e-2 of RMS(y).  The gate multiplies error and value alike,
+  so it is factored out elementwise rather than folded into one max/RMS ratio
+  (a product of two Gaussians has exponential tails).
 * Single steps whose only rounding is the final bf16 store:
-  |err| <= 2^-8 |ref| + slack, elementwise.
+  |err| <= 2^-8 |ref| + slack, elementwise (2^-8 = the largest relative
+  rounding error of a bf16 store).
 """
 
 import numpy as np
@@ -46,12 +51,23 @@ def assert_bf16_elementwise(got, ref, slack, what=""):
                            f"worst {np.abs(got - ref)[bad].max():.3e}")
 
 
-def assert_block_output(got, ref, x_in, what=""):
-    """The stated criterion on x' and the derived one on the update."""
+def assert_block_output(got, ref, x_in, gate, y_ref, what="", x_in_ref=None):
+    """The stated criterion on x' and the derived one on the update.
+    x_in: the GPU block's input; x_in_ref: the oracle's (defaults to x_in);
+    gate: per-element gate of each row; y_ref: the oracle's un-gated update."""
     assert_close(got, ref, 2e-2, 0.9995, what + " x'")
     x_in = np.asarray(x_in, np.float64)
-    assert_close(np.asarray(got, np.float64) - x_in, np.asarray(ref, np.float64) - x_in, 5e-2, 0.9995,
-                 what + " update")
+    x_in_ref = x_in if x_in_ref is None else np.asarray(x_in_ref, np.float64)
+    d_got = np.asarray(got, np.float64) - x_in
+    d_ref = np.asarray(ref, np.float64) - x_in_ref
+    _, _, cos = stats(d_got, d_ref)
+    assert cos >= 0.9999, f"{what} update: cosine {cos:.7f} < 0.9999"
+    y_rms = float(np.sqrt(np.mean(np.asarray(y_ref, np.float64) ** 2)))
+    d_rms = float(np.sqrt(np.mean(d_ref ** 2)))
+    bound = np.abs(gate) * 5e-2 * y_rms + 1e-5 * d_rms
+    bad = np.abs(d_got - d_ref) > bound
+    assert not bad.any(), (f"{what} update: {int(bad.sum())} elements outside |gate|*5e-2*RMS(y); worst ratio "
+                           f"{(np.abs(d_got - d_ref) / bound).max():.2f}")
 
 
 def f64(t):

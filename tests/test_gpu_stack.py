@@ -9,7 +9,7 @@ import torch
 import diffusion_transformer_block_fwd_b300 as F3
 import oracle as O
 import synth
-from _f3 import DEV, assert_block_output, f64, layout_tensors, weights_f64
+from _f3 import DEV, assert_block_output, f64, layout_tensors, stats, weights_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -27,23 +27,34 @@ def _sync_ok():
 
 def test_stack28_small_against_oracle_every_block(stack28):
     """Two consecutive calls (fresh modulation each, like two sampler steps) of
-    the 28 blocks on 96 tokens; GPU and oracle each run the whole chain, and
-    the residual stream is compared after every block."""
+    the 28 blocks on 96 tokens.  Per block: the GPU block runs on the oracle's
+    own input of that block (fp32-rounded; values flow oracle -> GPU only) and
+    its output meets the per-block criterion.  End to end: the GPU chain run on
+    its own outputs stays within cosine 0.9995 of the oracle chain (drift is
+    reported, not held to the per-block max bound)."""
     ws, blocks = stack28
     lay = synth.build_layout(synth.WORKLOADS["block_t96"]["spec"])
     pos, _ = layout_tensors(lay)
     x = synth.activations(77, lay.T, device=DEV)
     xo = f64(x)
-    xg = x.clone()
+    xg_free = x.clone()
     for call in range(2):
         mods = synth.modulation(77, call=call, device=DEV)
         m64 = f64(mods)
+        gate = m64[lay.stream_id, 6144:]
         for b in range(28):
-            x_in = xo
+            x_in = torch.from_numpy(xo.astype(np.float32)).to(DEV)
+            xg = x_in.clone()
             blocks.forward(xg, lay.segments, pos, mods, first_block=b, n_blocks=1)
-            xo = O.single_block(xo, weights_f64(ws[b]), m64, lay.stream_id, lay.pos.astype(np.float64))
+            blocks.forward(xg_free, lay.segments, pos, mods, first_block=b, n_blocks=1)
+            parts = O.single_block_parts(f64(x_in), weights_f64(ws[b]), m64, lay.stream_id,
+                                         lay.pos.astype(np.float64))
             _sync_ok()
-            assert_block_output(f64(xg), xo, x_in, f"call {call} block {b}")
+            assert_block_output(f64(xg), parts["out"], f64(x_in), gate, parts["y"], f"call {call} block {b}")
+            xo = parts["out"]
+    mx, rms, cos = stats(f64(xg_free), xo)
+    print(f"free-running 56-block drift: max|err|/RMS = {mx / rms:.3e}, cosine = {cos:.7f}")
+    assert cos >= 0.9995
 
 
 def test_stack28_full_size_properties(stack28):

@@ -117,8 +117,18 @@ def test_in_projection(block1, T):
                          ("g", gcat[:, 3072:], g)):
         rms = float(np.sqrt(np.mean(rv * rv)))
         assert_bf16_elementwise(gv, rv, 2e-3 * rms, f"in_projection {name} T={T}")
-        assert_close(gv, rv, 1e-2, 0.99995, f"in_projection {name} T={T}")
+        assert_close(gv, rv, 1.0, 0.99999, f"in_projection {name} T={T}")     # cosine; the bound above is the max
     assert torch.isnan(cat[:, :3072].float()).all(), "attention columns must be left untouched"
+
+
+def check_attention(got, ref, ref_abs, what):
+    """P and the output are rounded to bf16 (relative error <= 2^-8 each), so
+    |err| <= 2^-8 * sum_j p_j |v_j| + 2^-8 |o| (+ a 1e-5 slack for the fp32
+    logits and exp2); plus cosine >= 0.9999."""
+    bound = 2.0 ** -8 * (ref_abs + np.abs(ref)) * 1.01 + 1e-5 * ref_abs + 1e-6
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements outside the bf16 bound"
+    assert_close(got, ref, 1.0, 0.9999, what)
 
 
 def _qkv_inputs(T, seed, q_scale=1.0):
@@ -137,8 +147,9 @@ def test_attention(T, q_scale):
     assert F3.flux3_check_error(_stream()) == 0
     a = f64(qkv).reshape(T, 3, 24, 128)
     ref = O.attention(a[:, 0], a[:, 1], a[:, 2]).reshape(T, 3072)
+    ref_abs = O.attention(a[:, 0], a[:, 1], np.abs(a[:, 2])).reshape(T, 3072)
     got = f64(cat)[:, :3072]
-    assert_close(got, ref, 1e-2, 0.9999, f"attention T={T} qscale={q_scale}")
+    check_attention(got, ref, ref_abs, f"attention T={T} qscale={q_scale}")
     assert torch.isnan(cat[:, 3072:].float()).all(), "SwiGLU columns must be left untouched"
 
 
@@ -151,7 +162,8 @@ def test_attention_full_size_sampled_rows(T):
     rows = sample_rows(T, [(0, T, 0)], 40)
     a = f64(qkv).reshape(T, 3, 24, 128)
     ref = O.attention(a[rows, 0], a[:, 1], a[:, 2]).reshape(len(rows), 3072)
-    assert_close(f64(cat)[rows, :3072], ref, 1e-2, 0.9999, f"attention T={T}")
+    ref_abs = O.attention(a[rows, 0], a[:, 1], np.abs(a[:, 2])).reshape(len(rows), 3072)
+    check_attention(f64(cat)[rows, :3072], ref, ref_abs, f"attention T={T}")
 
 
 @pytest.mark.parametrize("T", [96, 171, 4608])
