@@ -29,12 +29,13 @@ FLUX3_STREAM_IMAGE = 0
 FLUX3_STREAM_IMAGE_COND = 1
 FLUX3_STREAM_TXT = 2
 FLUX3_MAX_SEGMENTS = 32
+FLUX3_NOALLOC_MAX_TOKENS = 512
 
 EXPORTED = (
     "flux3_default_config", "flux3_packed_weight_bytes", "flux3_workspace_bytes", "flux3_block_init",
     "flux3_block_forward", "flux3_stack_forward", "flux3_check_error", "flux3_status_string", "flux3_destroy",
     "flux3_stream_ids", "flux3_rope_tables", "flux3_ln_modulate", "flux3_in_projection", "flux3_attention",
-    "flux3_out_projection", "flux3_gemm_bf16", "flux3_selftest_wait_timeout",
+    "flux3_out_projection", "flux3_gemm_bf16", "flux3_selftest_wait_timeout", "flux3_block_forward_noalloc",
 )
 
 
@@ -92,6 +93,7 @@ def lib():
             "flux3_out_projection": (i, [vp, i, vp, i, vp, vp, vp, vp]),
             "flux3_gemm_bf16": (i, [vp, vp, vp, i, i, i, vp]),
             "flux3_selftest_wait_timeout": (i, [i, vp]),
+            "flux3_block_forward_noalloc": (i, [vp, i, vp, i, segp, i, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -195,6 +197,13 @@ def flux3_out_projection(h, block_idx, cat, T, stream_id, mod, x, stream=0):
 
 def flux3_gemm_bf16(A, B, C, M, N, K, stream=0):
     _check(lib().flux3_gemm_bf16(A, B, C, M, N, K, stream), "flux3_gemm_bf16")
+
+
+def flux3_block_forward_noalloc(h, block_idx, x, T, segments, pos_ids, mod, stream=0):
+    """flux3_block_forward with the library's built-in scratch (T <= 512)."""
+    segs = segments_array(segments)
+    _check(lib().flux3_block_forward_noalloc(h, block_idx, x, T, segs, len(segments), pos_ids, mod, stream),
+           "flux3_block_forward_noalloc")
 
 
 def flux3_selftest_wait_timeout(timeout_us, stream=0):

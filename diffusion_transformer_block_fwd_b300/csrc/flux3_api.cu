@@ -61,6 +61,14 @@ bool config_ok(const flux3_config *c) {
          c->rope_theta > 0.f && c->eps_ln > 0.f && c->eps_rms > 0.f;
 }
 
+// Bytes of the workspace for T tokens (each sub-buffer rounded up to 256 B);
+// the order and sizes match workspace_layout below.
+constexpr size_t ws_round(size_t v) { return (v + 255) / 256 * 256; }
+constexpr size_t workspace_total(size_t T) {
+  return ws_round(T) + 2 * ws_round(T * kRopePairs * 4) + ws_round(T * kHidden * 2) + ws_round(T * kQkvCols * 2) +
+         ws_round(T * kCatCols * 2);
+}
+
 struct Workspace {
   uint8_t *sid;
   float *cos_tab, *sin_tab;
@@ -176,6 +184,32 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, h->tm_out[b], T, kHidden, kCatCols, eo, s));
   }
   return FLUX3_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Scratch for flux3_block_forward_noalloc: a file-scope device array sized for
+// FLUX3_NOALLOC_MAX_TOKENS tokens.  Every device that loads the library holds
+// it until the process exits.  Host code only ever sees a host-side stand-in
+// for the symbol, so the device address is looked up once per device with
+// cudaGetSymbolAddress (with that device current) and cached.
+constexpr size_t kNoAllocScratchBytes = workspace_total(FLUX3_NOALLOC_MAX_TOKENS);
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device, or nullptr.
+void *noalloc_scratch() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
 }
 
 }  // namespace
@@ -416,6 +450,17 @@ flux3_status flux3_gemm_bf16(const void *A, const void *B, void *C, int M, int N
   ep.C = static_cast<__nv_bfloat16 *>(C);
   ep.ldc = N;
   return cuda_status(launch_gemm(EPI_STORE, ta, tb, M, N, K, ep, static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_block_forward_noalloc(const flux3_handle *h, int block_idx, float *x, int T,
+                                         const flux3_segment *segs, int n_segs, const float *pos_ids,
+                                         const float *mod, void *stream) {
+  if (T > FLUX3_NOALLOC_MAX_TOKENS) return FLUX3_ERR_WORKSPACE;
+  if (!h || T < 1) return FLUX3_ERR_INVALID_ARG;
+  void *scratch = noalloc_scratch();
+  if (!scratch) return FLUX3_ERR_CUDA;
+  return forward_common(h, block_idx, 1, x, T, segs, n_segs, pos_ids, mod, scratch, kNoAllocScratchBytes,
+                        static_cast<cudaStream_t>(stream));
 }
 
 flux3_status flux3_selftest_wait_timeout(int timeout_us, void *stream) {

@@ -157,6 +157,35 @@ FLUX3_API flux3_status flux3_stack_forward(const flux3_handle *h, int first_bloc
                                            const float *pos_ids, const float *mod,
                                            void *workspace, size_t ws_bytes, void *stream);
 
+/* Largest T flux3_block_forward_noalloc accepts (its scratch is ~25 MB). */
+#define FLUX3_NOALLOC_MAX_TOKENS 512
+
+/* flux3_block_forward for callers that must not allocate device memory.
+ * The paper has no counterpart: this is a deployment variant.
+ *
+ * Some callers cannot call cudaMalloc (or any allocating routine) at the point
+ * where they run a block: plug-in hosts whose device memory is owned by another
+ * allocator, runtimes that reserve all memory up front and forbid allocation
+ * afterwards, and real-time loops where an allocation's latency or failure is
+ * not acceptable.  This entry point takes the same arguments as
+ * flux3_block_forward minus the workspace: its scratch (stream ids, RoPE tables,
+ * modulated input, q/k/v, attention + SwiGLU output) lives in a fixed device
+ * array inside the library, sized for FLUX3_NOALLOC_MAX_TOKENS tokens, which
+ * every GPU that loads the library holds until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   - T > FLUX3_NOALLOC_MAX_TOKENS returns FLUX3_ERR_WORKSPACE; other errors as
+ *     flux3_block_forward.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero: every call writes each scratch
+ *     value before reading it.  Calls whose kernels overlap on the GPU (other
+ *     streams, or other host threads) race on the array: serialise them. */
+FLUX3_API flux3_status flux3_block_forward_noalloc(const flux3_handle *h, int block_idx, float *x, int T,
+                                                   const flux3_segment *segs, int n_segs,
+                                                   const float *pos_ids, const float *mod, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device error word.
  * Returns FLUX3_OK, FLUX3_ERR_TIMEOUT, FLUX3_ERR_DEVICE or FLUX3_ERR_CUDA. */
 FLUX3_API flux3_status flux3_check_error(void *stream);
