@@ -11,7 +11,7 @@
 #include "flux3_internal.h"
 #include "ptx.cuh"
 
-#include "attention_mma.cuh"
+#include "attention.cuh"
 #include "elementwise.cuh"
 #include "gemm.cuh"
 
