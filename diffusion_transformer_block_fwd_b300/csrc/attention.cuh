@@ -1,21 +1,24 @@
 // Bidirectional attention over all tokens of one sample (24 heads x 128, no
-// mask), tcgen05 / TMEM flash attention.
+// mask), tcgen05 / TMEM flash attention with two query tiles per CTA.
 //
-// CTA = (128 query rows, one head), 192 threads:
-//   warp 0      TMA producer: the Q tile once, then K and V tiles of 128 keys
-//               into a 2-stage ring (128-byte swizzle, two 64-dim boxes each)
-//   warp 1      owns the TMEM allocation (512 columns) and issues the MMAs
-//               from one thread: S_j = Q K_j^T into one of two S buffers
-//               (columns 0..127 / 128..255), then O += P_{j-1} V_{j-1}
-//               (columns 256..383) with P read from tensor memory
-//   warps 2..5  softmax, one query row per thread (TMEM lane = row): read the
-//               S row, online max / exp2 / sum in fp32, write P as packed bf16
-//               over the first 64 columns of the same S buffer; rescale the O
-//               row in TMEM when the running max grows by more than 2^8
-//               (otherwise the stale max is kept: P <= 2^8 is exact enough
-//               for bf16 and the fp32 accumulator); finally O / l -> bf16.
-// Keys past T (zero rows of the last tile) are masked to -inf.  Every wait is
-// bounded; on a timeout the CTA drains, frees TMEM and returns.
+// CTA = (256 query rows as two 128-row tiles A and B, one head), 320 threads:
+//   warps 0..3  softmax of tile A, one query row per thread (TMEM lane = row)
+//   warps 4..7  softmax of tile B
+//   warp 8      TMA producer: Q_A, Q_B once; K and V tiles of 128 keys in two
+//               independent 2-stage rings (128-byte swizzle, two 64-dim boxes
+//               per tile); K runs one tile ahead of V
+//   warp 9      owns the TMEM allocation and issues every MMA from one thread
+// TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256..383, O_B 384..511.
+// P overwrites the first 64 columns of its S buffer as packed bf16 and is the
+// A operand of O += P V.  MMA order per key tile j:
+//   S_A(j), PV_B(j-1), S_B(j), PV_A(j)
+// so while softmax A works on S_A(j) the tensor core runs PV_B(j-1) and
+// S_B(j), and while softmax B works on S_B(j) it runs PV_A(j) and S_A(j+1).
+// Softmax: online max in the log2 domain with lazy rescale (O is rescaled in
+// TMEM only when a row's max grows by more than 2^8), exp2 on the MUFU for 3
+// of every 4 columns and on the FMA pipe (2^floor * cubic) for the fourth,
+// row sums in fp32, P rounded to bf16.  Keys past T are masked to -inf.
+// Every wait is bounded; on a timeout the CTA drains, frees TMEM and returns.
 
 #pragma once
 
@@ -25,27 +28,27 @@
 namespace flux3 {
 namespace attn_tc {
 
-constexpr int kRows = 128;                       // query rows per CTA and keys per tile
-constexpr int kThreads = 192;
+constexpr int kRows = 128;                       // rows per query tile and keys per key tile
+constexpr int kThreads = 320;
+constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr uint32_t kHalfBytes = kRows * 128;     // 128 rows x 64 bf16 (one 128-byte swizzle box)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 dims = 32 KB
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+__host__ __device__ constexpr uint32_t col_s(int x) { return 128u * (uint32_t)x; }         // S_x / P_x
+__host__ __device__ constexpr uint32_t col_o(int x) { return 256u + 128u * (uint32_t)x; }  // O_x
 
 struct Ctl {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_done;
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr size_t kSmem = 1024 + kTileBytes /*Q*/ + kStages * 2 * kTileBytes /*K, V*/ + sizeof(Ctl);
+constexpr size_t kSmem = 1024 + 2 * kTileBytes /*Q_A, Q_B*/ + 2 * kStages * kTileBytes /*K, V*/ + sizeof(Ctl);
 
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   const unsigned long long t0 = global_timer_ns();
@@ -57,37 +60,58 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
+// 2^x on the FMA pipe for x <= 2^7: 2^floor(x) (exponent-field add) times a
+// cubic in f = x - floor(x) fitted to 2^f on [0, 1) for least maximum relative
+// error (7.5e-5, far below the 2^-9 of the bf16 P it feeds).  Inputs below
+// -126 are clamped there (2^-126 is negligible against a row sum >= 1).
+__device__ __forceinline__ float exp2_fma(float x) {
+  x = fmaxf(x, -126.0f);
+  const float xi = floorf(x);
+  const float f = x - xi;
+  float p = fmaf(0.07802422344684601f, f, 0.22606723010540009f);
+  p = fmaf(p, f, 0.695833683013916f);
+  p = fmaf(p, f, 0.9999251961708069f);
+  return __int_as_float(__float_as_int(p) + (static_cast<int>(xi) << 23));
+}
+
+template <int N>
+__device__ __forceinline__ uint32_t (&chunk(uint32_t (&a)[N], int c))[32] {
+  return *reinterpret_cast<uint32_t(*)[32]>(a + 32 * c);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_qkv, int T, __nv_bfloat16 *__restrict__ out) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sQ = smem;
-  uint8_t *sK = smem + kTileBytes;                          // [stage][2 halves]
+  uint8_t *sQ = smem;                                       // [tile A, B][2 halves]
+  uint8_t *sK = smem + 2 * kTileBytes;                      // [stage][2 halves]
   uint8_t *sV = sK + kStages * kTileBytes;                  // [stage][2 halves]
   Ctl *ctl = reinterpret_cast<Ctl *>(sV + kStages * kTileBytes);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int head = blockIdx.y;
-  const int q0 = blockIdx.x * kRows;
+  const int q0 = blockIdx.x * 2 * kRows;
   const int nt = (T + kRows - 1) / kRows;
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctl->kv_full[s], 1);
-      mbar_init(&ctl->kv_empty[s], 1);
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&ctl->s_full[b], 1);
-      mbar_init(&ctl->p_full[b], 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&ctl->s_full[x], 1);
+      mbar_init(&ctl->p_full[x], 128);
+      mbar_init(&ctl->o_done[x], 1);
     }
-    mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_qkv);
-  if (warp == 1) {
+  if (warp == kWarpTma && lane == 0) tma_prefetch_desc(&tm_qkv);
+  if (warp == kWarpMma) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -97,106 +121,122 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
 
-  if (warp == 0) {
+  if (warp == kWarpTma) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer: K_0, then per tile j: K_{j+1}, V_j
       const int xq = head * kHeadDim, xk = kHidden + head * kHeadDim, xv = 2 * kHidden + head * kHeadDim;
-      mbar_arrive_expect_tx(&ctl->q_full, kTileBytes);
-      tma_load_2d(sQ, &tm_qkv, &ctl->q_full, xq, q0);
-      tma_load_2d(sQ + kHalfBytes, &tm_qkv, &ctl->q_full, xq + 64, q0);
-      int last_phase[kStages] = {-1, -1};
+      mbar_arrive_expect_tx(&ctl->q_full, 2 * kTileBytes);
+      for (int x = 0; x < 2; ++x) {
+        tma_load_2d(sQ + x * kTileBytes, &tm_qkv, &ctl->q_full, xq, q0 + x * kRows);
+        tma_load_2d(sQ + x * kTileBytes + kHalfBytes, &tm_qkv, &ctl->q_full, xq + 64, q0 + x * kRows);
+      }
+      int k_last[kStages] = {-1, -1}, v_last[kStages] = {-1, -1};
       bool ok = true;
-      for (int j = 0; j < nt; ++j) {
+      auto load = [&](bool is_k, int j) -> bool {
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
-        if (!mbar_wait(&ctl->kv_empty[s], ph ^ 1, abort)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&ctl->kv_full[s], 2 * kTileBytes);
-        uint8_t *k = sK + s * kTileBytes, *v = sV + s * kTileBytes;
-        tma_load_2d(k, &tm_qkv, &ctl->kv_full[s], xk, j * kRows);
-        tma_load_2d(k + kHalfBytes, &tm_qkv, &ctl->kv_full[s], xk + 64, j * kRows);
-        tma_load_2d(v, &tm_qkv, &ctl->kv_full[s], xv, j * kRows);
-        tma_load_2d(v + kHalfBytes, &tm_qkv, &ctl->kv_full[s], xv + 64, j * kRows);
-        last_phase[s] = (int)ph;
+        uint64_t *empty = is_k ? &ctl->k_empty[s] : &ctl->v_empty[s];
+        uint64_t *full = is_k ? &ctl->k_full[s] : &ctl->v_full[s];
+        if (!mbar_wait(empty, ph ^ 1, abort)) return false;
+        mbar_arrive_expect_tx(full, kTileBytes);
+        uint8_t *dst = (is_k ? sK : sV) + s * kTileBytes;
+        const int x = is_k ? xk : xv;
+        tma_load_2d(dst, &tm_qkv, full, x, j * kRows);
+        tma_load_2d(dst + kHalfBytes, &tm_qkv, full, x + 64, j * kRows);
+        (is_k ? k_last : v_last)[s] = (int)ph;
+        return true;
+      };
+      ok = load(true, 0);
+      for (int j = 0; ok && j < nt; ++j) {
+        if (j + 1 < nt && !(ok = load(true, j + 1))) break;
+        ok = load(false, j);
       }
       drain_wait(&ctl->q_full, 0);
       if (!ok)
-        for (int s = 0; s < kStages; ++s)
-          if (last_phase[s] >= 0) drain_wait(&ctl->kv_full[s], (uint32_t)last_phase[s]);
+        for (int s = 0; s < kStages; ++s) {
+          if (k_last[s] >= 0) drain_wait(&ctl->k_full[s], (uint32_t)k_last[s]);
+          if (v_last[s] >= 0) drain_wait(&ctl->v_full[s], (uint32_t)v_last[s]);
+        }
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     if (lane == 0) {
       // ---------------- MMA issuer
       constexpr uint32_t idesc_s = idesc_bf16(kRows, kRows, false);   // B = K tile, K-major
       constexpr uint32_t idesc_o = idesc_bf16(kRows, kHeadDim, true); // B = V tile, MN-major
       const uint32_t q_addr = smem_addr(sQ);
+      auto issue_s = [&](int x, int s) {
+        const uint32_t qa = q_addr + x * kTileBytes, ka = smem_addr(sK + s * kTileBytes);
+#pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k) {
+          const uint32_t off = (uint32_t)(k / 4) * kHalfBytes + (uint32_t)(k % 4) * 32;
+          mma_bf16_ss(tmem + col_s(x), smem_desc(qa + off, 16, 1024, kSwizzle128B),
+                      smem_desc(ka + off, 16, 1024, kSwizzle128B), idesc_s, k > 0);
+        }
+        mma_commit(&ctl->s_full[x]);
+      };
+      // O_x += P_x V: 16 keys per MMA (P columns 8k.., V rows 16k..); V is
+      // MN-major: 64-dim halves 16 KB apart, 8-row groups 1 KB apart.
+      auto issue_pv = [&](int x, int s, bool first) {
+        const uint32_t va = smem_addr(sV + s * kTileBytes);
+#pragma unroll
+        for (int k = 0; k < kRows / 16; ++k)
+          mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + k * 8,
+                      smem_desc(va + k * 2048, kHalfBytes, 1024, kSwizzle128B), idesc_o, !(first && k == 0));
+        mma_commit(&ctl->o_done[x]);
+      };
       bool ok = mbar_wait(&ctl->q_full, 0, abort);
-      for (int j = 0; ok && j <= nt; ++j) {
-        if (j < nt) {
-          const int s = j % kStages;
-          if (!mbar_wait(&ctl->kv_full[s], (j / kStages) & 1, abort)) break;
-          tc_fence_after();
-          const uint32_t k_addr = smem_addr(sK + s * kTileBytes);
-          const uint32_t d = tmem + (uint32_t)(j & 1) * kRows;
-#pragma unroll
-          for (int k = 0; k < kHeadDim / 16; ++k) {
-            const uint32_t off = (uint32_t)(k / 4) * kHalfBytes + (uint32_t)(k % 4) * 32;
-            mma_bf16_ss(d, smem_desc(q_addr + off, 16, 1024, kSwizzle128B),
-                        smem_desc(k_addr + off, 16, 1024, kSwizzle128B), idesc_s, k > 0);
-          }
-          mma_commit(&ctl->s_full[j & 1]);
-        }
+      for (int j = 0; ok && j < nt; ++j) {
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        if (!(ok = mbar_wait(&ctl->k_full[s], ph, abort))) break;
+        tc_fence_after();
+        issue_s(0, s);
         if (j >= 1) {
-          const int jj = j - 1;
-          const int s = jj % kStages;
-          if (!mbar_wait(&ctl->p_full[jj & 1], (jj >> 1) & 1, abort)) break;
+          if (!(ok = mbar_wait(&ctl->p_full[1], (j - 1) & 1, abort))) break;
           tc_fence_after();
-          const uint32_t v_addr = smem_addr(sV + s * kTileBytes);
-          const uint32_t p = tmem + (uint32_t)(jj & 1) * kRows;
-          // 16 keys per MMA: P columns 8k .. 8k+7 (packed bf16 pairs), V rows 16k .. 16k+15;
-          // V is MN-major: 64-dim halves 16 KB apart (leading offset), 8-row groups 1 KB apart.
-#pragma unroll
-          for (int k = 0; k < kRows / 16; ++k)
-            mma_bf16_ts(tmem + kColO, p + k * 8, smem_desc(v_addr + k * 2048, kHalfBytes, 1024, kSwizzle128B),
-                        idesc_o, (jj | k) != 0);
-          mma_commit(&ctl->kv_empty[s]);
-          mma_commit(&ctl->o_done);
+          issue_pv(1, (j - 1) % kStages, j - 1 == 0);
+          mma_commit(&ctl->v_empty[(j - 1) % kStages]);
         }
+        issue_s(1, s);
+        mma_commit(&ctl->k_empty[s]);
+        if (!(ok = mbar_wait(&ctl->v_full[s], ph, abort))) break;
+        if (!(ok = mbar_wait(&ctl->p_full[0], j & 1, abort))) break;
+        tc_fence_after();
+        issue_pv(0, s, j == 0);
+      }
+      if (ok && mbar_wait(&ctl->p_full[1], (nt - 1) & 1, abort)) {
+        tc_fence_after();
+        issue_pv(1, (nt - 1) % kStages, nt - 1 == 0);
+        mma_commit(&ctl->v_empty[(nt - 1) % kStages]);
       }
       mma_commit(&ctl->drain);
       drain_wait(&ctl->drain, 0);
     }
   } else {
-    // ---------------- softmax / correction / epilogue, one row per thread
+    // ---------------- softmax / correction / epilogue of tile x, one row per thread
+    const int x = warp / 4;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + col_s(x), t_o = tmem + lane_off + col_o(x);
     const float scale_log2 = 1.4426950408889634f * rsqrtf((float)kHeadDim);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&ctl->s_full[sb], (j >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
+      if (!(ok = mbar_wait(&ctl->s_full[x], j & 1, abort))) break;
       tc_fence_after();
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + sb * kRows + c * 32, sv[c]);
+      uint32_t sv[128];
+      tmem_ld32x2(t_s, t_s + 32, chunk(sv, 0), chunk(sv, 1));
+      tmem_ld32x2(t_s + 64, t_s + 96, chunk(sv, 2), chunk(sv, 3));
       const int valid = T - j * kRows;   // keys of this tile that exist
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = __uint_as_float(sv[c][i]) * scale_log2;
-          if (c * 32 + i >= valid) v = -INFINITY;
-          sv[c][i] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
+      for (int i = 0; i < 128; ++i) {
+        float v = __uint_as_float(sv[i]) * scale_log2;
+        if (i >= valid) v = -INFINITY;
+        sv[i] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
       const float m_new = fmaxf(m, mx);
       const bool need = (j > 0) && (m_new > m + 8.0f);
       bool waited = false;
@@ -204,10 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
       } else if (__any_sync(0xffffffffu, need)) {
         // O must hold every PV up to j-1 before it is rescaled
-        if (!mbar_wait(&ctl->o_done, (j - 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
+        if (!(ok = mbar_wait(&ctl->o_done[x], (j - 1) & 1, abort))) break;
         waited = true;
         tc_fence_after();
         const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
@@ -216,46 +253,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kColO + c * 32, o);
+          tmem_ld32(t_o + c * 32, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tmem + lane_off + kColO + c * 32, o);
+          tmem_st32(t_o + c * 32, o);
         }
       }
+      // p = 2^(s - m), packed in place: pair k (columns 2k, 2k+1) -> sv[k]
       float sum = 0.f;
-      uint32_t pk[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(__uint_as_float(sv[c][2 * i]) - m);
-          const float p1 = ex2_approx(__uint_as_float(sv[c][2 * i + 1]) - m);
-          sum += p0 + p1;
-          pk[c >> 1][(c & 1) * 16 + i] = pack_bf16x2(p0, p1);
+      for (int k = 0; k < 64; ++k) {
+        const float a = __uint_as_float(sv[2 * k]) - m;
+        const float b = __uint_as_float(sv[2 * k + 1]) - m;
+        float p0, p1;
+        if ((k & 3) == 3) {
+          p0 = exp2_fma(a);
+          p1 = exp2_fma(b);
+        } else {
+          p0 = ex2_approx(a);
+          p1 = ex2_approx(b);
         }
+        sum += p0 + p1;
+        sv[k] = pack_bf16x2(p0, p1);
+      }
       l += sum;
       // keep o_done's phases in step: every PV completion is observed in order
-      if (j > 0 && !waited) {
-        if (!mbar_wait(&ctl->o_done, (j - 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
-      }
-      tmem_st32(tmem + lane_off + sb * kRows, pk[0]);
-      tmem_st32(tmem + lane_off + sb * kRows + 32, pk[1]);
+      if (j > 0 && !waited && !(ok = mbar_wait(&ctl->o_done[x], (j - 1) & 1, abort))) break;
+      tmem_st32(t_s, chunk(sv, 0));
+      tmem_st32(t_s + 32, chunk(sv, 1));
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&ctl->p_full[sb]);
+      mbar_arrive(&ctl->p_full[x]);
     }
-    if (ok && mbar_wait(&ctl->o_done, (nt - 1) & 1, abort)) {
+    if (ok && mbar_wait(&ctl->o_done[x], (nt - 1) & 1, abort)) {
       tc_fence_after();
       const float inv = 1.0f / l;
-      const int t = q0 + row;
+      const int t = q0 + x * kRows + row;
       uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)(t < T ? t : 0) * kCatCols + head * kHeadDim);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + kColO + c * 32, o);
+        tmem_ld32(t_o + c * 32, o);
         if (t < T) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -272,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace attn_tc
@@ -287,7 +325,7 @@ cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat
   }
   CUtensorMap tm;
   if (!make_tmap_bf16(&tm, qkv, (uint64_t)T, kQkvCols, kRows)) return cudaErrorInvalidValue;
-  dim3 grid((T + kRows - 1) / kRows, kHeads);
+  dim3 grid((T + 2 * kRows - 1) / (2 * kRows), kHeads);
   attention_kernel<<<grid, kThreads, kSmem, s>>>(tm, T, cat);
   return cudaGetLastError();
 }

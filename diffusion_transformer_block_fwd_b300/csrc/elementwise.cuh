@@ -38,23 +38,31 @@ __global__ void stream_ids_kernel(SegTable tab, int T, uint8_t *sid) {
 }
 
 // Angles are formed in double precision (positions reach a few thousand, so a
-// float product would lose ~1e-4 rad); the tables are float32.
-__global__ void rope_tables_kernel(const float *pos, int T, double log2_theta, float *cos_tab, float *sin_tab) {
+// float product would lose ~1e-4 rad) and reduced modulo 2*pi in double; the
+// reduced angle, within [-pi, pi], goes through the float sincos.  The 16
+// frequencies theta^(-2j/32) come from the host in double.
+struct RopeFreqs {
+  double f[16];
+};
+
+__global__ void rope_tables_kernel(const float *pos, int T, RopeFreqs fr, float *cos_tab, float *sin_tab) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= T * kRopePairs) return;
   const int t = i / kRopePairs, p = i % kRopePairs;
   const int axis = p / 16, j = p % 16;
-  const double freq = exp2(-(2.0 * j / 32.0) * log2_theta);
-  const double ang = (double)pos[(size_t)t * 4 + axis] * freq;
-  double sn, cs;
-  sincos(ang, &sn, &cs);
-  cos_tab[i] = (float)cs;
-  sin_tab[i] = (float)sn;
+  const double two_pi = 6.283185307179586;
+  const double ang = (double)pos[(size_t)t * 4 + axis] * fr.f[j];
+  const double turns = rint(ang * (1.0 / two_pi));
+  const float r = (float)fma(-turns, two_pi, ang);
+  float sn, cs;
+  sincosf(r, &sn, &cs);
+  cos_tab[i] = cs;
+  sin_tab[i] = sn;
 }
 
 constexpr int kLnWarps = 8;
 
-__global__ void __launch_bounds__(kLnWarps * 32)
+__global__ void __launch_bounds__(kLnWarps * 32, 2)
     ln_modulate_kernel(const float *__restrict__ x, int T, const uint8_t *__restrict__ sid,
                        const float *__restrict__ mod, float eps, __nv_bfloat16 *__restrict__ h) {
   constexpr int kVec = kHidden / (32 * 4);  // 24 float4 per lane
@@ -131,7 +139,9 @@ cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_
                                cudaStream_t s) {
   using namespace ew_detail;
   const int n = T * kRopePairs;
-  rope_tables_kernel<<<(n + 255) / 256, 256, 0, s>>>(pos, T, log2((double)theta), cos_tab, sin_tab);
+  RopeFreqs fr;
+  for (int j = 0; j < 16; ++j) fr.f[j] = pow((double)theta, -2.0 * j / 32.0);
+  rope_tables_kernel<<<(n + 255) / 256, 256, 0, s>>>(pos, T, fr, cos_tab, sin_tab);
   return cudaGetLastError();
 }
 
