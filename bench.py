@@ -12,6 +12,13 @@ events.  For N > 1 (torchrun) every rank runs an independent replica (the
 path needs no exchange): the value is the tokens of all ranks over the
 slowest rank's time.
 
+Each timed step is one replay of a CUDA graph of that launch sequence, so
+the per-kernel events (event-record nodes in the graph) measure device time
+without host launch gaps.  `--workload` selects another configuration: the
+other single-block layouts, or a 28-block stack (bf16 or NVFP4 weights), where
+a step is one call of the stack per sampler step of the workload (16 for the
+two-reference stack, each with fresh modulation vectors).
+
 One JSON line is printed by rank 0.  `--impl reference` times the CPU oracle
 on the host cores instead (rank 0 only).
 """
@@ -89,7 +96,7 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -206,13 +213,9 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- GPU arm
-def run_ours(args):
+def dist_setup():
     import torch
     import torch.distributed as dist
-
-    import diffusion_transformer_block_fwd_b300 as F3
-    import synth
-
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -220,9 +223,48 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
+    return rank, world, local, dev
 
+
+def max_over_ranks(v, world, dev):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_graphs(step_fn, n_events, steps, stream):
+    """Captures `steps` CUDA graphs of step_fn(events), each with its own
+    event-record nodes; returns (graphs, events)."""
+    import torch
+    graphs, evs = [], []
+    for _ in range(steps):
+        e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_events)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step_fn(e)
+        graphs.append(g)
+        evs.append(e)
+    torch.cuda.synchronize()
+    return graphs, evs
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import diffusion_transformer_block_fwd_b300 as F3
+    import synth
+
+    rank, world, local, dev = dist_setup()
     F3.lib()   # fail loudly if the library is missing
-    spec = synth.WORKLOADS[args.workload]["spec"]
+    wl = synth.WORKLOADS[args.workload]
+    if wl["blocks"] > 1:
+        return run_stack(args, rank, world, local, dev)
+    spec = wl["spec"]
     lay = synth.build_layout(spec)
     T = lay.T
     w = synth.block_weights(1, 0, device=dev)
@@ -237,7 +279,7 @@ def run_ours(args):
     qkv = torch.empty((T, 9216), dtype=torch.bfloat16, device=dev)
     cat = torch.empty((T, 12288), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MiB > L2
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)
     sp = stream.cuda_stream
     cfg = blocks.cfg
 
@@ -267,24 +309,28 @@ def run_ours(args):
             evs[5].record(stream)
 
     launches_per_step = 6
-    for _ in range(args.warmup):
-        step()
-    st = F3.flux3_check_error(sp)
-    assert st == 0, F3.status_string(st)
-
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    sampler = ClockSampler(local)
-    sampler.start()
-    t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        step(events[i])
-    torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter() - t_wall0
-    clocks = sampler.stop()
+    torch.cuda.synchronize(dev)          # inputs were made on the default stream
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        st = F3.flux3_check_error(sp)
+        assert st == 0, F3.status_string(st)
+        graphs, events = timed_graphs(step, 6, args.steps, stream)
+        for g in graphs[:2]:                      # the graphs themselves warm up once
+            g.replay()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(local)
+        sampler.start()
+        t_wall0 = time.perf_counter()
+        for g in graphs:
+            flush.zero_()
+            g.replay()
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+        clocks = sampler.stop()
     if world > 1:
         dist.barrier()
     st = F3.flux3_check_error(sp)
@@ -293,10 +339,7 @@ def run_ours(args):
     per_kernel = {n: statistics.mean(events[i][k].elapsed_time(events[i][k + 1]) for i in range(args.steps))
                   for k, n in enumerate(names)}
     step_ms = statistics.mean(events[i][0].elapsed_time(events[i][5]) for i in range(args.steps))
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, world, dev)
     value = world * T / (step_ms * 1e-3)
     tflops = world * block_flops(T) / (step_ms * 1e-3) / 1e12
 
@@ -313,25 +356,22 @@ def run_ours(args):
         xd.copy_(x_host, non_blocking=True)
         posd.copy_(pos_host, non_blocking=True)
         modd.copy_(mod_host, non_blocking=True)
-        blocks.forward(xd, lay.segments, posd, modd)
+        blocks.forward(xd, lay.segments, posd, modd, stream=stream)
         out_host.copy_(xd, non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     h2d = x_host.numel() * 4 + pos_host.numel() * 4 + mod_host.numel() * 4
     d2h = out_host.numel() * 4
     st = F3.flux3_check_error(sp)
@@ -354,8 +394,10 @@ def run_ours(args):
         d = {"ms": per_kernel[n]}
         if n in kf:
             d["tflops"] = kf[n] / (per_kernel[n] * 1e-3) / 1e12
+            d["frac_of_bf16_peak"] = d["tflops"] / bf16_burst
         if n == "ln_modulate":
             d["gbs"] = kernel_bytes(T)["ln_modulate"] / (per_kernel[n] * 1e-3) / 1e9
+            d["frac_of_hbm"] = d["gbs"] / hbm
         kernels[n] = d
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -363,6 +405,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init N(0,0.02) bf16 weights)",
             "config": {"workload": args.workload, "T": T, "segments": lay.segments,
                        "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+                       "launch": "one CUDA graph replay per step (event-record nodes around each kernel)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
             "frac_of_bf16_spec_2250": tflops / world / 2250.0,
@@ -383,10 +426,104 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_stack(args, rank, world, local, dev):
+    """A 28-block stack workload: a step is `calls` stack calls (one per
+    sampler step, each with its own modulation vectors) over the whole token
+    sequence, bf16 or NVFP4 weights (quantised on the device)."""
+    import torch
+    import torch.distributed as dist
+
+    import diffusion_transformer_block_fwd_b300 as F3
+    import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    lay = synth.build_layout(wl["spec"])
+    T, nb, calls, fp4 = lay.T, wl["blocks"], wl["calls"], wl["wfmt"] == "nvfp4"
+    ws = []
+    for b in range(nb):
+        w = synth.block_weights(1, b, device=dev)
+        if fp4:
+            q = {k: F3.quantize_nvfp4(w[k]) for k in F3.NVFP4_MATRICES}
+            q.update({k: w[k] for k in ("query_norm", "key_norm")})
+            w = q
+        ws.append(w)
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+    torch.cuda.synchronize(dev)          # weights were made (and quantised) on the default stream
+    with torch.cuda.stream(stream):
+        blocks = F3.Flux3Blocks(ws, max_tokens=T, wfmt=wl["wfmt"], stream=stream)
+    del ws
+    torch.cuda.synchronize(dev)
+    x0 = synth.activations(1, T, device=dev)
+    x = x0.clone()
+    mods = [synth.modulation(1, call=c, device=dev) for c in range(calls)]
+    pos = torch.from_numpy(lay.pos).to(dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        for c in range(calls):
+            blocks.forward(x, lay.segments, pos, mods[c], stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+
+    per_call_launches = 2 + nb * (4 + (1 if fp4 else 0))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            x.copy_(x0)
+            step()
+        st = F3.flux3_check_error(sp)
+        assert st == 0, F3.status_string(st)
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(local)
+        sampler.start()
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            x.copy_(x0)
+            flush.zero_()
+            step(events[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+        clocks = sampler.stop()
+    st = F3.flux3_check_error(sp)
+    assert st == 0, F3.status_string(st)
+    step_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in events), world, dev)
+    flops = calls * nb * block_flops(T)
+    hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
+    tflops = world * flops / (step_ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": world * T * calls / (step_ms * 1e-3), "unit": "tokens/s (per stack call)",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" + (" (NVFP4 weights dequantised per block)" if fp4 else ""),
+            "data": "synthetic (random-init N(0,0.02) weights" + (", NVFP4-quantised on the device)" if fp4 else ")"),
+            "config": {"workload": args.workload, "T": T, "blocks": nb, "calls_per_step": calls,
+                       "segments": lay.segments, "l2": "flushed between timed steps",
+                       "launch": "stream launches through flux3_stack_forward"},
+            "ms_per_stack_call": step_ms / calls, "ms_per_block": step_ms / calls / nb,
+            "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
+            "frac_of_bf16_sustained": (tflops / world / bf16_sust) if bf16_sust else None,
+            "frac_of_bf16_spec_2250": tflops / world / 2250.0,
+            "roofline": {"kernel": "whole stack", "bound": "tensor", "achieved": tflops / world,
+                         "peak": bf16_sust or bf16_burst, "unit": "TFLOP/s",
+                         "frac": tflops / world / (bf16_sust or bf16_burst), "traffic": None,
+                         "peak_source": "measured bf16 sustained (MEASURED_PEAKS.json)"},
+            "gpu_launches": per_call_launches * calls * args.steps, "clocks": clocks, "wall_s_timed_region": t_wall}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    blocks.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="block_1024sq_t4608")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

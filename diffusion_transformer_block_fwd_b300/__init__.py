@@ -36,6 +36,7 @@ EXPORTED = (
     "flux3_block_forward", "flux3_stack_forward", "flux3_check_error", "flux3_status_string", "flux3_destroy",
     "flux3_stream_ids", "flux3_rope_tables", "flux3_ln_modulate", "flux3_in_projection", "flux3_attention",
     "flux3_out_projection", "flux3_gemm_bf16", "flux3_selftest_wait_timeout", "flux3_block_forward_noalloc",
+    "flux3_block_init_nvfp4", "flux3_quantize_nvfp4", "flux3_dequantize_block",
 )
 
 
@@ -55,6 +56,18 @@ class flux3_config(ctypes.Structure):
 class flux3_block_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out",
                                                 "query_norm", "key_norm")]
+
+
+class flux3_nvfp4_tensor(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("global_scale", ctypes.c_void_p)]
+
+
+NVFP4_MATRICES = ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out")
+
+
+class flux3_block_weights_nvfp4(ctypes.Structure):
+    _fields_ = [(n, flux3_nvfp4_tensor) for n in NVFP4_MATRICES] + [("query_norm", ctypes.c_void_p),
+                                                                    ("key_norm", ctypes.c_void_p)]
 
 
 class flux3_segment(ctypes.Structure):
@@ -94,6 +107,10 @@ def lib():
             "flux3_gemm_bf16": (i, [vp, vp, vp, i, i, i, vp]),
             "flux3_selftest_wait_timeout": (i, [i, vp]),
             "flux3_block_forward_noalloc": (i, [vp, i, vp, i, segp, i, vp, vp, vp]),
+            "flux3_block_init_nvfp4": (i, [ctypes.POINTER(vp), cfgp, ctypes.POINTER(flux3_block_weights_nvfp4), i,
+                                           vp, sz, vp]),
+            "flux3_quantize_nvfp4": (i, [vp, i, i, vp, vp, vp, vp]),
+            "flux3_dequantize_block": (i, [vp, i, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -147,6 +164,31 @@ def flux3_block_init(cfg, weights, packed_ptr, packed_bytes, stream=0):
     _check(lib().flux3_block_init(ctypes.byref(h), ctypes.byref(cfg), arr, n, packed_ptr, packed_bytes, stream),
            "flux3_block_init")
     return h.value
+
+
+def flux3_block_init_nvfp4(cfg, weights, packed_ptr, packed_bytes, stream=0):
+    """weights: list of dicts: for each matrix name a (codes, scales, global)
+    triple of device pointers, and query_norm / key_norm device pointers."""
+    n = len(weights)
+    arr = (flux3_block_weights_nvfp4 * n)()
+    for b, w in enumerate(weights):
+        for k in NVFP4_MATRICES:
+            c, sc, g = w[k]
+            t = getattr(arr[b], k)
+            t.codes, t.scales, t.global_scale = int(c), int(sc), int(g)
+        arr[b].query_norm, arr[b].key_norm = int(w["query_norm"]), int(w["key_norm"])
+    h = ctypes.c_void_p()
+    _check(lib().flux3_block_init_nvfp4(ctypes.byref(h), ctypes.byref(cfg), arr, n, packed_ptr, packed_bytes, stream),
+           "flux3_block_init_nvfp4")
+    return h.value
+
+
+def flux3_quantize_nvfp4(w, rows, cols, codes, scales, global_scale, stream=0):
+    _check(lib().flux3_quantize_nvfp4(w, rows, cols, codes, scales, global_scale, stream), "flux3_quantize_nvfp4")
+
+
+def flux3_dequantize_block(h, block_idx, w_in, w_out, stream=0):
+    _check(lib().flux3_dequantize_block(h, block_idx, w_in, w_out, stream), "flux3_dequantize_block")
 
 
 def flux3_block_forward(h, block_idx, x, T, segments, pos_ids, mod, workspace, ws_bytes, stream=0):
@@ -210,4 +252,4 @@ def flux3_selftest_wait_timeout(timeout_us, stream=0):
     _check(lib().flux3_selftest_wait_timeout(timeout_us, stream), "flux3_selftest_wait_timeout")
 
 
-from .model import Flux3Blocks  # noqa: E402,F401  (torch-owned buffers around the handle)
+from .model import Flux3Blocks, quantize_nvfp4  # noqa: E402,F401  (torch-owned buffers around the handle)

@@ -14,10 +14,13 @@
 //   S_A(j), PV_B(j-1), S_B(j), PV_A(j)
 // so while softmax A works on S_A(j) the tensor core runs PV_B(j-1) and
 // S_B(j), and while softmax B works on S_B(j) it runs PV_A(j) and S_A(j+1).
-// Softmax: online max in the log2 domain with lazy rescale (O is rescaled in
-// TMEM only when a row's max grows by more than 2^8), exp2 on the MUFU for 3
-// of every 4 columns and on the FMA pipe (2^floor * cubic) for the fourth,
-// row sums in fp32, P rounded to bf16.  Keys past T are masked to -inf.
+// Softmax, one row per thread, two passes over the S columns in TMEM (32 at
+// a time, so the scores never all sit in registers): the row max (3-input
+// max, 4 chains), then p = exp2(s * log2(e)/sqrt(128) - m) on the MUFU with
+// packed float-pair FMAs and adds, P rounded to bf16 and stored over the
+// columns already consumed.  Online max in the log2 domain with lazy rescale
+// (O is rescaled in TMEM only when a row's max grows by more than 2^8); row
+// sums in fp32.  Keys past T are masked to -inf (last key tile only).
 // Every wait is bounded; on a timeout the CTA drains, frees TMEM and returns.
 
 #pragma once
@@ -60,23 +63,33 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
-// 2^x on the FMA pipe for x <= 2^7: 2^floor(x) (exponent-field add) times a
-// cubic in f = x - floor(x) fitted to 2^f on [0, 1) for least maximum relative
-// error (7.5e-5, far below the 2^-9 of the bf16 P it feeds).  Inputs below
-// -126 are clamped there (2^-126 is negligible against a row sum >= 1).
-__device__ __forceinline__ float exp2_fma(float x) {
-  x = fmaxf(x, -126.0f);
-  const float xi = floorf(x);
-  const float f = x - xi;
-  float p = fmaf(0.07802422344684601f, f, 0.22606723010540009f);
-  p = fmaf(p, f, 0.695833683013916f);
-  p = fmaf(p, f, 0.9999251961708069f);
-  return __int_as_float(__float_as_int(p) + (static_cast<int>(xi) << 23));
+// Keys at or past `valid` (counted from the chunk's first column) get -inf.
+__device__ __forceinline__ void mask_keys(uint32_t (&r)[32], int valid) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i >= valid) r[i] = __float_as_uint(-INFINITY);
 }
 
-template <int N>
-__device__ __forceinline__ uint32_t (&chunk(uint32_t (&a)[N], int c))[32] {
-  return *reinterpret_cast<uint32_t(*)[32]>(a + 32 * c);
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (a, b) = (x0, x1) * s + (t, t) as one packed float-pair FMA.
+__device__ __forceinline__ void fma2(float x0, float x1, float s, float t, float &a, float &b) {
+  asm("{\n .reg .b64 x, m, c, d;\n mov.b64 x, {%2, %3};\n mov.b64 m, {%4, %4};\n mov.b64 c, {%5, %5};\n"
+      " fma.rn.f32x2 d, x, m, c;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(a), "=f"(b)
+      : "f"(x0), "f"(x1), "f"(s), "f"(t));
+}
+
+// (s0, s1) += (p0, p1) as one packed float-pair add.
+__device__ __forceinline__ void add2(float &s0, float &s1, float p0, float p1) {
+  asm("{\n .reg .b64 x, y, d;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n add.f32x2 d, x, y;\n"
+      " mov.b64 {%0, %1}, d;\n}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(p0), "f"(p1));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -224,29 +237,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       if (!(ok = mbar_wait(&ctl->s_full[x], j & 1, abort))) break;
+      // S_x(j) complete implies PV_x(j-1) complete (MMAs finish in issue
+      // order); observing o_done here keeps its phases in step.
+      if (j > 0 && !(ok = mbar_wait(&ctl->o_done[x], (j - 1) & 1, abort))) break;
       tc_fence_after();
-      uint32_t sv[128];
-      tmem_ld32x2(t_s, t_s + 32, chunk(sv, 0), chunk(sv, 1));
-      tmem_ld32x2(t_s + 64, t_s + 96, chunk(sv, 2), chunk(sv, 3));
-      const int valid = T - j * kRows;   // keys of this tile that exist
-      float mx = -INFINITY;
+      const int valid = T - j * kRows;   // keys of this tile that exist (< 128 only in the last tile)
+      // pass 1: row max of the raw scores, 4 chains of 3-input max (scale > 0 commutes with max)
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        float v = __uint_as_float(sv[i]) * scale_log2;
-        if (i >= valid) v = -INFINITY;
-        sv[i] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(t_s + c * 32, r);
+        if (valid < kRows) mask_keys(r, valid - c * 32);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          m4[i & 3] = max3(m4[i & 3], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
       }
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
       const float m_new = fmaxf(m, mx);
       const bool need = (j > 0) && (m_new > m + 8.0f);
-      bool waited = false;
       if (j == 0) {
         m = m_new;
       } else if (__any_sync(0xffffffffu, need)) {
-        // O must hold every PV up to j-1 before it is rescaled
-        if (!(ok = mbar_wait(&ctl->o_done[x], (j - 1) & 1, abort))) break;
-        waited = true;
-        tc_fence_after();
         const float alpha = need ? ex2_approx(m - m_new) : 1.0f;
         if (need) m = m_new;
         l *= alpha;
@@ -259,28 +271,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(t_o + c * 32, o);
         }
       }
-      // p = 2^(s - m), packed in place: pair k (columns 2k, 2k+1) -> sv[k]
-      float sum = 0.f;
+      // pass 2: p = 2^(s * scale_log2 - m) in float pairs, rounded to bf16 and
+      // stored over the consumed S columns (chunk c -> columns 16c .. 16c+15);
+      // the row sum in 4 independent pair accumulators
+      const float neg_m = -m;
+      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        const float a = __uint_as_float(sv[2 * k]) - m;
-        const float b = __uint_as_float(sv[2 * k + 1]) - m;
-        float p0, p1;
-        if ((k & 3) == 3) {
-          p0 = exp2_fma(a);
-          p1 = exp2_fma(b);
-        } else {
-          p0 = ex2_approx(a);
-          p1 = ex2_approx(b);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32], pk[16];
+        tmem_ld32(t_s + c * 32, r);
+        if (valid < kRows) mask_keys(r, valid - c * 32);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float a, b;
+          fma2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]), scale_log2, neg_m, a, b);
+          const float p0 = ex2_approx(a), p1 = ex2_approx(b);
+          add2(sum[2 * (k & 3)], sum[2 * (k & 3) + 1], p0, p1);
+          pk[k] = pack_bf16x2(p0, p1);
         }
-        sum += p0 + p1;
-        sv[k] = pack_bf16x2(p0, p1);
+        tmem_st16(t_s + c * 16, pk);
       }
-      l += sum;
-      // keep o_done's phases in step: every PV completion is observed in order
-      if (j > 0 && !waited && !(ok = mbar_wait(&ctl->o_done[x], (j - 1) & 1, abort))) break;
-      tmem_st32(t_s, chunk(sv, 0));
-      tmem_st32(t_s + 32, chunk(sv, 1));
+      l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctl->p_full[x]);

@@ -37,12 +37,15 @@ __global__ void stream_ids_kernel(SegTable tab, int T, uint8_t *sid) {
   sid[t] = (uint8_t)s;
 }
 
-// Angles are formed in double precision (positions reach a few thousand, so a
-// float product would lose ~1e-4 rad) and reduced modulo 2*pi in double; the
-// reduced angle, within [-pi, pi], goes through the float sincos.  The 16
-// frequencies theta^(-2j/32) come from the host in double.
+// Angles are carried in turns (angle / 2 pi) as an unevaluated float pair
+// hi + lo: hi = pos * fh (rounded), lo = its exact rounding error (fma) plus
+// pos * fl, where fh + fl is theta^(-2j/32) / (2 pi) split on the host from a
+// double.  The pair holds the angle to ~2^-47 relative, so dropping the whole
+// turns (hi - rint(hi) is exact) leaves the fraction of a turn accurate to
+// ~3e-8 turns for |pos| < 2^20; sincospif of twice the fraction gives the
+// table entries.  No float64 arithmetic runs on the device.
 struct RopeFreqs {
-  double f[16];
+  float hi[16], lo[16];
 };
 
 __global__ void rope_tables_kernel(const float *pos, int T, RopeFreqs fr, float *cos_tab, float *sin_tab) {
@@ -50,12 +53,12 @@ __global__ void rope_tables_kernel(const float *pos, int T, RopeFreqs fr, float 
   if (i >= T * kRopePairs) return;
   const int t = i / kRopePairs, p = i % kRopePairs;
   const int axis = p / 16, j = p % 16;
-  const double two_pi = 6.283185307179586;
-  const double ang = (double)pos[(size_t)t * 4 + axis] * fr.f[j];
-  const double turns = rint(ang * (1.0 / two_pi));
-  const float r = (float)fma(-turns, two_pi, ang);
+  const float x = __ldg(pos + (size_t)t * 4 + axis);
+  const float th = x * fr.hi[j];
+  const float tl = fmaf(x, fr.hi[j], -th) + x * fr.lo[j];
+  const float frac = (th - rintf(th)) + tl;
   float sn, cs;
-  sincosf(r, &sn, &cs);
+  sincospif(2.0f * frac, &sn, &cs);
   cos_tab[i] = cs;
   sin_tab[i] = sn;
 }
@@ -140,7 +143,12 @@ cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_
   using namespace ew_detail;
   const int n = T * kRopePairs;
   RopeFreqs fr;
-  for (int j = 0; j < 16; ++j) fr.f[j] = pow((double)theta, -2.0 * j / 32.0);
+  const double inv_two_pi = 0.15915494309189535;
+  for (int j = 0; j < 16; ++j) {
+    const double turns = pow((double)theta, -2.0 * j / 32.0) * inv_two_pi;
+    fr.hi[j] = (float)turns;
+    fr.lo[j] = (float)(turns - (double)fr.hi[j]);
+  }
   rope_tables_kernel<<<(n + 255) / 256, 256, 0, s>>>(pos, T, fr, cos_tab, sin_tab);
   return cudaGetLastError();
 }

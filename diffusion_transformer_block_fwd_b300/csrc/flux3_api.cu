@@ -14,14 +14,16 @@
 #include "attention.cuh"
 #include "elementwise.cuh"
 #include "gemm.cuh"
+#include "nvfp4.cuh"
 
 struct flux3_handle {
   flux3_config cfg;
   int n_blocks;
-  const __nv_bfloat16 *w_in;   // [n_blocks][kInRows, kHidden]
-  const __nv_bfloat16 *w_out;  // [n_blocks][kHidden, kCatCols]
+  const __nv_bfloat16 *w_in;   // bf16: [n_blocks][kInRows, kHidden]
+  const __nv_bfloat16 *w_out;  // bf16: [n_blocks][kHidden, kCatCols]
   const float *norms;          // [n_blocks][2][kHeadDim]
-  std::vector<CUtensorMap> tm_in, tm_out;
+  std::vector<CUtensorMap> tm_in, tm_out;               // bf16 only
+  std::vector<flux3::fp4_detail::Fp4BlockView> fp4;    // NVFP4 only
 };
 
 namespace flux3 {
@@ -57,7 +59,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool config_ok(const flux3_config *c) {
   return c && c->hidden == kHidden && c->heads == kHeads && c->head_dim == kHeadDim && c->mlp_hidden == kMlp &&
-         c->n_blocks >= 1 && c->max_tokens >= 1 && c->max_tokens <= kMaxTokensLimit && c->wfmt == FLUX3_W_BF16 &&
+         c->n_blocks >= 1 && c->max_tokens >= 1 && c->max_tokens <= kMaxTokensLimit &&
+         (c->wfmt == FLUX3_W_BF16 || c->wfmt == FLUX3_W_NVFP4) &&
          c->rope_theta > 0.f && c->eps_ln > 0.f && c->eps_rms > 0.f;
 }
 
@@ -69,13 +72,23 @@ constexpr size_t workspace_total(size_t T) {
          ws_round(T * kCatCols * 2);
 }
 
+// NVFP4 packed block: in-projection codes and scales, out-projection codes and
+// scales, the six global scales.
+constexpr size_t kFp4InCodes = (size_t)kInRows * kHidden / 2;
+constexpr size_t kFp4InScales = (size_t)kInRows * kHidden / 16;
+constexpr size_t kFp4OutCodes = (size_t)kHidden * kCatCols / 2;
+constexpr size_t kFp4OutScales = (size_t)kHidden * kCatCols / 16;
+constexpr size_t kFp4BlockBytes =
+    ws_round(kFp4InCodes) + ws_round(kFp4InScales) + ws_round(kFp4OutCodes) + ws_round(kFp4OutScales) + 256;
+
 struct Workspace {
   uint8_t *sid;
   float *cos_tab, *sin_tab;
   __nv_bfloat16 *h, *qkv, *cat;
+  __nv_bfloat16 *w_in, *w_out;   // NVFP4 handles: the running block's weights in bf16
 };
 
-size_t workspace_layout(int T, uint8_t *base, Workspace *ws) {
+size_t workspace_layout(int T, uint8_t *base, Workspace *ws, bool fp4_weights = false) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -88,6 +101,8 @@ size_t workspace_layout(int T, uint8_t *base, Workspace *ws) {
   uint8_t *h = take((size_t)T * kHidden * 2);
   uint8_t *qkv = take((size_t)T * kQkvCols * 2);
   uint8_t *cat = take((size_t)T * kCatCols * 2);
+  uint8_t *w_in = fp4_weights ? take(kWInElems * 2) : nullptr;
+  uint8_t *w_out = fp4_weights ? take(kWOutElems * 2) : nullptr;
   if (ws) {
     ws->sid = sid;
     ws->cos_tab = reinterpret_cast<float *>(cs);
@@ -95,6 +110,8 @@ size_t workspace_layout(int T, uint8_t *base, Workspace *ws) {
     ws->h = reinterpret_cast<__nv_bfloat16 *>(h);
     ws->qkv = reinterpret_cast<__nv_bfloat16 *>(qkv);
     ws->cat = reinterpret_cast<__nv_bfloat16 *>(cat);
+    ws->w_in = reinterpret_cast<__nv_bfloat16 *>(w_in);
+    ws->w_out = reinterpret_cast<__nv_bfloat16 *>(w_out);
   }
   return off;
 }
@@ -156,16 +173,21 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
   if (T < 1 || T > h->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
   F3_TRY(segments_ok(segs, n_segs, T));
   if (!aligned16(x) || !aligned16(pos) || !aligned16(mod) || !aligned16(workspace)) return FLUX3_ERR_ALIGNMENT;
+  const bool fp4 = h->cfg.wfmt == FLUX3_W_NVFP4;
   Workspace ws;
-  if (ws_bytes < workspace_layout(T, nullptr, nullptr)) return FLUX3_ERR_WORKSPACE;
-  workspace_layout(T, static_cast<uint8_t *>(workspace), &ws);
+  if (ws_bytes < workspace_layout(T, nullptr, nullptr, fp4)) return FLUX3_ERR_WORKSPACE;
+  workspace_layout(T, static_cast<uint8_t *>(workspace), &ws, fp4);
 
   F3_CUDA(launch_stream_ids(segs, n_segs, T, ws.sid, s));
   F3_CUDA(launch_rope_tables(pos, T, h->cfg.rope_theta, ws.cos_tab, ws.sin_tab, s));
-  CUtensorMap tmH, tmCat;
+  CUtensorMap tmH, tmCat, tmWin, tmWout;
   if (!make_tmap_bf16(&tmH, ws.h, (uint64_t)T, kHidden, kBM)) return FLUX3_ERR_CUDA;
   if (!make_tmap_bf16(&tmCat, ws.cat, (uint64_t)T, kCatCols, kBM)) return FLUX3_ERR_CUDA;
+  if (fp4 && (!make_tmap_bf16(&tmWin, ws.w_in, kInRows, kHidden, kBN) ||
+              !make_tmap_bf16(&tmWout, ws.w_out, kHidden, kCatCols, kBN)))
+    return FLUX3_ERR_CUDA;
   for (int b = first; b < first + count; ++b) {
+    if (fp4) F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s));
     F3_CUDA(launch_ln_modulate(x, T, ws.sid, mod, h->cfg.eps_ln, ws.h, s));
     EpiParams ep{};
     ep.qkv = ws.qkv;
@@ -175,13 +197,13 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     ep.qnorm = block_norms(h, b);
     ep.knorm = block_norms(h, b) + kHeadDim;
     ep.eps_rms = h->cfg.eps_rms;
-    F3_CUDA(launch_gemm(EPI_IN_PROJ, tmH, h->tm_in[b], T, kInRows, kHidden, ep, s));
+    F3_CUDA(launch_gemm(EPI_IN_PROJ, tmH, fp4 ? tmWin : h->tm_in[b], T, kInRows, kHidden, ep, s));
     F3_CUDA(launch_attention(ws.qkv, T, ws.cat, s));
     EpiParams eo{};
     eo.x = x;
     eo.sid = ws.sid;
     eo.mod = mod;
-    F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, h->tm_out[b], T, kHidden, kCatCols, eo, s));
+    F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, fp4 ? tmWout : h->tm_out[b], T, kHidden, kCatCols, eo, s));
   }
   return FLUX3_OK;
 }
@@ -262,12 +284,13 @@ void flux3_default_config(flux3_config *cfg) {
 
 size_t flux3_packed_weight_bytes(const flux3_config *cfg) {
   if (!config_ok(cfg)) return 0;
-  return (size_t)cfg->n_blocks * (align_up(kWInElems * 2) + align_up(kWOutElems * 2) + align_up(2 * kHeadDim * 4));
+  const size_t per_block = cfg->wfmt == FLUX3_W_NVFP4 ? kFp4BlockBytes : align_up(kWInElems * 2) + align_up(kWOutElems * 2);
+  return (size_t)cfg->n_blocks * (per_block + align_up(2 * kHeadDim * 4));
 }
 
 size_t flux3_workspace_bytes(const flux3_config *cfg, int T) {
   if (!config_ok(cfg) || T < 1 || T > cfg->max_tokens) return 0;
-  return workspace_layout(T, nullptr, nullptr);
+  return workspace_layout(T, nullptr, nullptr, cfg->wfmt == FLUX3_W_NVFP4);
 }
 
 flux3_status flux3_block_init(flux3_handle **out, const flux3_config *cfg, const flux3_block_weights *w, int n_blocks,
@@ -275,7 +298,7 @@ flux3_status flux3_block_init(flux3_handle **out, const flux3_config *cfg, const
   if (!out) return FLUX3_ERR_INVALID_ARG;
   *out = nullptr;
   if (!cfg || !w || !packed) return FLUX3_ERR_INVALID_ARG;
-  if (cfg->wfmt != FLUX3_W_BF16 && cfg->wfmt != FLUX3_W_NVFP4) return FLUX3_ERR_INVALID_ARG;
+  if (cfg->wfmt != FLUX3_W_BF16) return FLUX3_ERR_INVALID_ARG;   // NVFP4: flux3_block_init_nvfp4
   if (!config_ok(cfg)) return FLUX3_ERR_UNSUPPORTED;
   if (n_blocks != cfg->n_blocks) return FLUX3_ERR_INVALID_ARG;
   if (packed_bytes < flux3_packed_weight_bytes(cfg)) return FLUX3_ERR_WORKSPACE;
@@ -348,6 +371,109 @@ flux3_status flux3_block_init(flux3_handle **out, const flux3_config *cfg, const
   return FLUX3_OK;
 }
 
+flux3_status flux3_block_init_nvfp4(flux3_handle **out, const flux3_config *cfg, const flux3_block_weights_nvfp4 *w,
+                                    int n_blocks, void *packed, size_t packed_bytes, void *stream) {
+  if (!out) return FLUX3_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !w || !packed) return FLUX3_ERR_INVALID_ARG;
+  if (cfg->wfmt != FLUX3_W_NVFP4) return FLUX3_ERR_INVALID_ARG;
+  if (!config_ok(cfg)) return FLUX3_ERR_UNSUPPORTED;
+  if (n_blocks != cfg->n_blocks) return FLUX3_ERR_INVALID_ARG;
+  if (packed_bytes < flux3_packed_weight_bytes(cfg)) return FLUX3_ERR_WORKSPACE;
+  if (!aligned16(packed)) return FLUX3_ERR_ALIGNMENT;
+  for (int b = 0; b < n_blocks; ++b) {
+    const flux3_block_weights_nvfp4 &bw = w[b];
+    const flux3_nvfp4_tensor *ts[6] = {&bw.q_proj, &bw.k_proj, &bw.v_proj, &bw.attn_out, &bw.mlp_in, &bw.mlp_out};
+    for (const flux3_nvfp4_tensor *t : ts) {
+      if (!t->codes || !t->scales || !t->global_scale) return FLUX3_ERR_INVALID_ARG;
+      if (!aligned16(t->codes) || !aligned16(t->scales) || (reinterpret_cast<uintptr_t>(t->global_scale) & 3u))
+        return FLUX3_ERR_ALIGNMENT;
+    }
+    if (!bw.query_norm || !bw.key_norm) return FLUX3_ERR_INVALID_ARG;
+    if (!aligned16(bw.query_norm) || !aligned16(bw.key_norm)) return FLUX3_ERR_ALIGNMENT;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  flux3_handle *h = new (std::nothrow) flux3_handle();
+  if (!h) return FLUX3_ERR_CUDA;
+  h->cfg = *cfg;
+  h->n_blocks = n_blocks;
+  h->w_in = h->w_out = nullptr;
+  uint8_t *base = static_cast<uint8_t *>(packed);
+  auto *norms = reinterpret_cast<float *>(base + n_blocks * kFp4BlockBytes);
+  h->norms = norms;
+  h->fp4.resize(n_blocks);
+
+  constexpr size_t in_row = kHidden / 2, in_srow = kHidden / 16;     // bytes per row: codes, scales
+  constexpr size_t out_row = kCatCols / 2, out_srow = kCatCols / 16;
+  constexpr size_t mlp_row = kMlp / 2, mlp_srow = kMlp / 16;          // mlp_out rows (9216 inputs)
+  cudaError_t e = cudaSuccess;
+  auto copy = [&](void *dst, const void *src, size_t bytes) {
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+  };
+  auto copy2d = [&](void *dst, size_t dpitch, const void *src, size_t spitch, size_t width, size_t height) {
+    if (e == cudaSuccess) e = cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, cudaMemcpyDeviceToDevice, s);
+  };
+  for (int b = 0; b < n_blocks && e == cudaSuccess; ++b) {
+    const flux3_block_weights_nvfp4 &bw = w[b];
+    uint8_t *blk = base + b * kFp4BlockBytes;
+    uint8_t *in_c = blk;
+    uint8_t *in_s = in_c + ws_round(kFp4InCodes);
+    uint8_t *out_c = in_s + ws_round(kFp4InScales);
+    uint8_t *out_s = out_c + ws_round(kFp4OutCodes);
+    float *globals = reinterpret_cast<float *>(out_s + ws_round(kFp4OutScales));
+    // in-projection rows q | k | v | mlp_in (a and b interleaved in groups of 128), codes and scales alike
+    const flux3_nvfp4_tensor *qkv[3] = {&bw.q_proj, &bw.k_proj, &bw.v_proj};
+    for (int i = 0; i < 3; ++i) {
+      copy(in_c + (size_t)i * kHidden * in_row, qkv[i]->codes, kHidden * in_row);
+      copy(in_s + (size_t)i * kHidden * in_srow, qkv[i]->scales, kHidden * in_srow);
+    }
+    const uint8_t *mc = static_cast<const uint8_t *>(bw.mlp_in.codes);
+    const uint8_t *ms = static_cast<const uint8_t *>(bw.mlp_in.scales);
+    uint8_t *wc = in_c + 3 * kHidden * in_row, *wsc = in_s + 3 * kHidden * in_srow;
+    copy2d(wc, 256 * in_row, mc, 128 * in_row, 128 * in_row, kMlp / 128);
+    copy2d(wc + 128 * in_row, 256 * in_row, mc + kMlp * in_row, 128 * in_row, 128 * in_row, kMlp / 128);
+    copy2d(wsc, 256 * in_srow, ms, 128 * in_srow, 128 * in_srow, kMlp / 128);
+    copy2d(wsc + 128 * in_srow, 256 * in_srow, ms + kMlp * in_srow, 128 * in_srow, 128 * in_srow, kMlp / 128);
+    // out-projection rows: attn_out's inputs then mlp_out's
+    copy2d(out_c, out_row, bw.attn_out.codes, in_row, in_row, kHidden);
+    copy2d(out_c + in_row, out_row, bw.mlp_out.codes, mlp_row, mlp_row, kHidden);
+    copy2d(out_s, out_srow, bw.attn_out.scales, in_srow, in_srow, kHidden);
+    copy2d(out_s + in_srow, out_srow, bw.mlp_out.scales, mlp_srow, mlp_srow, kHidden);
+    const float *gsrc[6] = {bw.q_proj.global_scale, bw.k_proj.global_scale, bw.v_proj.global_scale,
+                            bw.mlp_in.global_scale, bw.attn_out.global_scale, bw.mlp_out.global_scale};
+    for (int i = 0; i < 6; ++i) copy(globals + i, gsrc[i], sizeof(float));
+    copy(norms + (size_t)b * 2 * kHeadDim, bw.query_norm, kHeadDim * 4);
+    copy(norms + (size_t)b * 2 * kHeadDim + kHeadDim, bw.key_norm, kHeadDim * 4);
+    h->fp4[b] = fp4_detail::Fp4BlockView{in_c, in_s, out_c, out_s, globals};
+  }
+  if (e != cudaSuccess) {
+    delete h;
+    return FLUX3_ERR_CUDA;
+  }
+  *out = h;
+  return FLUX3_OK;
+}
+
+flux3_status flux3_quantize_nvfp4(const void *w, int rows, int cols, void *codes, void *scales, float *global_scale,
+                                  void *stream) {
+  if (!w || !codes || !scales || !global_scale || rows < 1 || cols < 16 || cols % 16 != 0)
+    return FLUX3_ERR_INVALID_ARG;
+  if ((size_t)rows * (size_t)cols > (size_t)1 << 34) return FLUX3_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(global_scale) & 3u))
+    return FLUX3_ERR_ALIGNMENT;
+  return cuda_status(launch_quantize_nvfp4(static_cast<const __nv_bfloat16 *>(w), rows, cols,
+                                           static_cast<uint8_t *>(codes), static_cast<uint8_t *>(scales),
+                                           global_scale, static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_dequantize_block(const flux3_handle *h, int block_idx, void *w_in, void *w_out, void *stream) {
+  if (!h || !w_in || !w_out || block_idx < 0 || block_idx >= h->n_blocks) return FLUX3_ERR_INVALID_ARG;
+  if (h->cfg.wfmt != FLUX3_W_NVFP4) return FLUX3_ERR_UNSUPPORTED;
+  if (!aligned16(w_in) || !aligned16(w_out)) return FLUX3_ERR_ALIGNMENT;
+  return cuda_status(launch_dequantize_block(h->fp4[block_idx], static_cast<__nv_bfloat16 *>(w_in),
+                                             static_cast<__nv_bfloat16 *>(w_out), static_cast<cudaStream_t>(stream)));
+}
+
 flux3_status flux3_block_forward(const flux3_handle *h, int block_idx, float *x, int T, const flux3_segment *segs,
                                  int n_segs, const float *pos_ids, const float *mod, void *workspace, size_t ws_bytes,
                                  void *stream) {
@@ -417,6 +543,7 @@ flux3_status flux3_in_projection(const flux3_handle *h, int block_idx, const voi
                                  const float *sin_tab, void *qkv, void *cat, void *stream) {
   if (!h || !hmod || !cos_tab || !sin_tab || !qkv || !cat) return FLUX3_ERR_INVALID_ARG;
   if (block_idx < 0 || block_idx >= h->n_blocks || T < 1 || T > h->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
+  if (h->cfg.wfmt != FLUX3_W_BF16) return FLUX3_ERR_UNSUPPORTED;
   if (!aligned16(hmod) || !aligned16(qkv) || !aligned16(cat) || !aligned16(cos_tab) || !aligned16(sin_tab))
     return FLUX3_ERR_ALIGNMENT;
   return run_in_projection(h, block_idx, static_cast<const __nv_bfloat16 *>(hmod), T, cos_tab, sin_tab,
@@ -435,6 +562,7 @@ flux3_status flux3_out_projection(const flux3_handle *h, int block_idx, const vo
                                   const uint8_t *stream_id, const float *mod, float *x, void *stream) {
   if (!h || !cat || !stream_id || !mod || !x) return FLUX3_ERR_INVALID_ARG;
   if (block_idx < 0 || block_idx >= h->n_blocks || T < 1 || T > h->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
+  if (h->cfg.wfmt != FLUX3_W_BF16) return FLUX3_ERR_UNSUPPORTED;
   if (!aligned16(cat) || !aligned16(mod) || !aligned16(x)) return FLUX3_ERR_ALIGNMENT;
   return run_out_projection(h, block_idx, static_cast<const __nv_bfloat16 *>(cat), T, stream_id, mod, x,
                             static_cast<cudaStream_t>(stream));
@@ -457,6 +585,7 @@ flux3_status flux3_block_forward_noalloc(const flux3_handle *h, int block_idx, f
                                          const float *mod, void *stream) {
   if (T > FLUX3_NOALLOC_MAX_TOKENS) return FLUX3_ERR_WORKSPACE;
   if (!h || T < 1) return FLUX3_ERR_INVALID_ARG;
+  if (h->cfg.wfmt != FLUX3_W_BF16) return FLUX3_ERR_UNSUPPORTED;
   void *scratch = noalloc_scratch();
   if (!scratch) return FLUX3_ERR_CUDA;
   return forward_common(h, block_idx, 1, x, T, segs, n_segs, pos_ids, mod, scratch, kNoAllocScratchBytes,

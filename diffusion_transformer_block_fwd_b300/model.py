@@ -4,8 +4,9 @@ flux3_stack_forward / flux3_block_forward of the C library."""
 
 import torch
 
-from . import (FLUX3_W_BF16, flux3_block_forward, flux3_block_init, flux3_default_config, flux3_destroy,
-               flux3_packed_weight_bytes, flux3_stack_forward, flux3_workspace_bytes)
+from . import (FLUX3_W_BF16, FLUX3_W_NVFP4, NVFP4_MATRICES, flux3_block_forward, flux3_block_init,
+               flux3_block_init_nvfp4, flux3_default_config, flux3_destroy, flux3_packed_weight_bytes,
+               flux3_quantize_nvfp4, flux3_stack_forward, flux3_workspace_bytes)
 
 WEIGHT_KEYS = ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out", "query_norm", "key_norm")
 
@@ -15,34 +16,62 @@ def _stream_ptr(stream):
     return s.cuda_stream
 
 
+def quantize_nvfp4(w, stream=None):
+    """NVFP4 of a bf16 [rows, cols] device matrix through flux3_quantize_nvfp4:
+    returns (codes uint8 [rows, cols/2], scales uint8 [rows, cols/16],
+    global float32 [1]) device tensors."""
+    assert w.dtype == torch.bfloat16 and w.is_contiguous() and w.dim() == 2
+    rows, cols = w.shape
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((rows, cols // 16), dtype=torch.uint8, device=w.device)
+    g = torch.empty(1, dtype=torch.float32, device=w.device)
+    flux3_quantize_nvfp4(w.data_ptr(), rows, cols, codes.data_ptr(), scales.data_ptr(), g.data_ptr(),
+                         _stream_ptr(stream))
+    return codes, scales, g
+
+
 class Flux3Blocks:
     """Joint single_blocks on one CUDA device.
 
-    weights: list (one per block) of dicts of device tensors: bf16 [out, in]
-    matrices q_proj, k_proj, v_proj, attn_out, mlp_in, mlp_out and float32
-    [128] query_norm, key_norm.  They are copied into the packed buffer at
-    construction and not referenced afterwards."""
+    weights: list (one per block) of dicts of device tensors.  bf16 format:
+    bf16 [out, in] matrices q_proj, k_proj, v_proj, attn_out, mlp_in, mlp_out.
+    nvfp4 format: each of those is a (codes, scales, global) triple as
+    quantize_nvfp4 returns.  Both: float32 [128] query_norm, key_norm.  The
+    weights are copied into the packed buffer at construction and not
+    referenced afterwards."""
 
-    def __init__(self, weights, max_tokens=16384, stream=None):
-        dev = weights[0]["q_proj"].device
+    def __init__(self, weights, max_tokens=16384, stream=None, wfmt="bf16"):
+        fp4 = wfmt == "nvfp4"
+        dev = (weights[0]["q_proj"][0] if fp4 else weights[0]["q_proj"]).device
         self.device = dev
+        self.wfmt = wfmt
         self.cfg = flux3_default_config()
         self.cfg.n_blocks = len(weights)
         self.cfg.max_tokens = int(max_tokens)
-        self.cfg.wfmt = FLUX3_W_BF16
+        self.cfg.wfmt = FLUX3_W_NVFP4 if fp4 else FLUX3_W_BF16
         nbytes = flux3_packed_weight_bytes(self.cfg)
         if nbytes == 0:
             raise ValueError("unsupported configuration")
         self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         ptrs = []
         for w in weights:
-            for k in WEIGHT_KEYS[:6]:
-                assert w[k].dtype == torch.bfloat16 and w[k].is_contiguous() and w[k].device == dev, k
             for k in WEIGHT_KEYS[6:]:
                 assert w[k].dtype == torch.float32 and w[k].is_contiguous(), k
-            ptrs.append({k: w[k].data_ptr() for k in WEIGHT_KEYS})
+            if fp4:
+                for k in NVFP4_MATRICES:
+                    c, sc, g = w[k]
+                    assert c.dtype == torch.uint8 and sc.dtype == torch.uint8 and g.dtype == torch.float32, k
+                    assert c.is_contiguous() and sc.is_contiguous() and c.device == dev, k
+                d = {k: tuple(t.data_ptr() for t in w[k]) for k in NVFP4_MATRICES}
+                d.update({k: w[k].data_ptr() for k in WEIGHT_KEYS[6:]})
+                ptrs.append(d)
+            else:
+                for k in WEIGHT_KEYS[:6]:
+                    assert w[k].dtype == torch.bfloat16 and w[k].is_contiguous() and w[k].device == dev, k
+                ptrs.append({k: w[k].data_ptr() for k in WEIGHT_KEYS})
         sp = _stream_ptr(stream)
-        self.handle = flux3_block_init(self.cfg, ptrs, self.packed.data_ptr(), nbytes, sp)
+        init = flux3_block_init_nvfp4 if fp4 else flux3_block_init
+        self.handle = init(self.cfg, ptrs, self.packed.data_ptr(), nbytes, sp)
         (stream or torch.cuda.current_stream()).synchronize()   # source weights may be freed after this
         self._ws = torch.empty(0, dtype=torch.uint8, device=dev)
 

@@ -96,6 +96,32 @@ typedef struct flux3_block_weights {
   const float *key_norm;  /* [128] */
 } flux3_block_weights;
 
+/* One weight matrix [rows, cols] in NVFP4 (cols a multiple of 16):
+ *   codes         device uint8 [rows, cols / 2]: e2m1 codes (sign bit 3,
+ *                 exponent bits 2..1 with bias 1, mantissa bit 0); element 2i
+ *                 of a row is the low nibble of byte i, element 2i+1 the high
+ *   scales        device uint8 [rows, cols / 16]: e4m3 bit patterns (sign 7,
+ *                 exponent 6..3 with bias 7, mantissa 2..0); scale b of a row
+ *                 covers its elements 16b .. 16b+15
+ *   global_scale  device float32 [1]
+ * weight[r, c] = e2m1(code[r, c]) * e4m3(scales[r, c / 16]) * global_scale.
+ * The pages name the nvfp4 checkpoint variant ("Welcome FLUX.3 Image Klein in
+ * Diffusers", section "Single-file format checkpoints") but not its layout;
+ * this is the layout flux3_quantize_nvfp4 writes. */
+typedef struct flux3_nvfp4_tensor {
+  const void *codes;
+  const void *scales;
+  const float *global_scale;
+} flux3_nvfp4_tensor;
+
+/* One block's weights in NVFP4 (shapes as flux3_block_weights); the norm
+ * scales stay float32.  Pointers must be 16-byte aligned (global_scale: 4). */
+typedef struct flux3_block_weights_nvfp4 {
+  flux3_nvfp4_tensor q_proj, k_proj, v_proj, attn_out, mlp_in, mlp_out;
+  const float *query_norm;
+  const float *key_norm;
+} flux3_block_weights_nvfp4;
+
 /* A contiguous run of tokens of one stream.  A forward call's segments must be
  * in increasing order, non-overlapping, non-empty, and cover [0, T) exactly;
  * at most FLUX3_MAX_SEGMENTS of them.  Any stream order is accepted. */
@@ -114,14 +140,18 @@ typedef struct flux3_handle flux3_handle;
  * eps 1e-6). */
 FLUX3_API void flux3_default_config(flux3_config *cfg);
 
-/* Bytes of the caller-owned buffer flux3_block_init packs the weights into
+/* Bytes of the caller-owned buffer flux3_block_init (bf16) or
+ * flux3_block_init_nvfp4 (cfg->wfmt == FLUX3_W_NVFP4) packs the weights into
  * (per block: the q/k/v/mlp_in rows concatenated, the attn_out/mlp_out
- * columns concatenated, and the two norm scales).  0 if cfg is invalid. */
+ * columns concatenated, and the two norm scales; NVFP4 keeps codes, block
+ * scales and the six global scales, 69.0 MB per block instead of 245.4 MB).
+ * 0 if cfg is invalid. */
 FLUX3_API size_t flux3_packed_weight_bytes(const flux3_config *cfg);
 
 /* Bytes of workspace a forward call with T tokens needs (stream ids, RoPE
- * tables, modulated input, q/k/v, attention + SwiGLU output).  0 if cfg is
- * invalid or T is out of range. */
+ * tables, modulated input, q/k/v, attention + SwiGLU output; with NVFP4
+ * weights also one block's weights dequantised to bf16, 245.4 MB).  0 if cfg
+ * is invalid or T is out of range. */
 FLUX3_API size_t flux3_workspace_bytes(const flux3_config *cfg, int T);
 
 /* Creates a handle for n_blocks blocks (n_blocks == cfg->n_blocks).
@@ -133,6 +163,40 @@ FLUX3_API size_t flux3_workspace_bytes(const flux3_config *cfg, int T);
 FLUX3_API flux3_status flux3_block_init(flux3_handle **out, const flux3_config *cfg,
                                         const flux3_block_weights *w, int n_blocks,
                                         void *packed, size_t packed_bytes, void *stream);
+
+/* flux3_block_init for NVFP4 weights (cfg->wfmt == FLUX3_W_NVFP4): packs the
+ * codes, block scales, global scales and norm scales into `packed`
+ * (flux3_packed_weight_bytes(cfg) bytes).  Every forward call then expands
+ * each block's weights to bf16 in the workspace (each weight rounded once, to
+ * nearest even, from the exact product of its code and scales) just before
+ * the block runs, and the projections run as bf16 tensor-core GEMMs with bf16
+ * activations.  Same errors as flux3_block_init. */
+FLUX3_API flux3_status flux3_block_init_nvfp4(flux3_handle **out, const flux3_config *cfg,
+                                              const flux3_block_weights_nvfp4 *w, int n_blocks,
+                                              void *packed, size_t packed_bytes, void *stream);
+
+/* Quantises a bf16 matrix to NVFP4 on the device:
+ *   global_scale = float32(amax / (6 * 448))   (1 if the matrix is all zero)
+ *   scale of block b = e4m3, nearest even, of amax_b / (6 * global_scale),
+ *                      saturating at 448 (amax_b = largest |w| of the block)
+ *   code = e2m1, nearest even, of w / (scale * global_scale), saturating at
+ *          +-6; zero never carries a sign; a block whose scale is 0 is all 0
+ * Every rounding decision is taken on the float64 quotient, so the result is
+ * reproducible bit for bit.
+ *   w             device bf16 [rows, cols], cols % 16 == 0, 16-byte aligned
+ *   codes, scales device outputs in the flux3_nvfp4_tensor layout
+ *   global_scale  device float32 [1] (output; it holds the amax bits while the
+ *                 call's kernels run) */
+FLUX3_API flux3_status flux3_quantize_nvfp4(const void *w, int rows, int cols, void *codes, void *scales,
+                                            float *global_scale, void *stream);
+
+/* The bf16 weights an NVFP4 handle's block_idx runs with, as the forward pass
+ * expands them: w_in device bf16 [27648, 3072] = rows of q | k | v | mlp_in
+ * (mlp_in's a and b halves interleaved in groups of 128 rows: a[128m..],
+ * b[128m..], ...), w_out device bf16 [3072, 12288] = [attn_out | mlp_out]
+ * along the input dimension.  FLUX3_ERR_UNSUPPORTED for a bf16 handle. */
+FLUX3_API flux3_status flux3_dequantize_block(const flux3_handle *h, int block_idx, void *w_in, void *w_out,
+                                              void *stream);
 
 /* One joint block (block_idx of the handle) applied in place.
  *   x        device float32 [T, 3072]: the residual stream, updated in place
@@ -173,8 +237,9 @@ FLUX3_API flux3_status flux3_stack_forward(const flux3_handle *h, int first_bloc
  * array inside the library, sized for FLUX3_NOALLOC_MAX_TOKENS tokens, which
  * every GPU that loads the library holds until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
- *   - T > FLUX3_NOALLOC_MAX_TOKENS returns FLUX3_ERR_WORKSPACE; other errors as
- *     flux3_block_forward.
+ *   - T > FLUX3_NOALLOC_MAX_TOKENS returns FLUX3_ERR_WORKSPACE; a handle with
+ *     NVFP4 weights returns FLUX3_ERR_UNSUPPORTED (its dequantised weights
+ *     would not fit); other errors as flux3_block_forward.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
  *     stream capture.
@@ -219,6 +284,10 @@ FLUX3_API flux3_status flux3_rope_tables(const float *pos_ids, int T, float thet
  *   mod device float32 [3, 9216]; h device bf16 [T, 3072] (output). */
 FLUX3_API flux3_status flux3_ln_modulate(const float *x, int T, const uint8_t *stream_id,
                                          const float *mod, float eps, void *h, void *stream);
+
+/* Step entry points flux3_in_projection and flux3_out_projection use the
+ * handle's packed bf16 weights: with an NVFP4 handle they return
+ * FLUX3_ERR_UNSUPPORTED (the forward calls expand NVFP4 weights themselves). */
 
 /* The block's input projections with their fused epilogues (one tensor-core
  * GEMM over the concatenated [Wq; Wk; Wv; Wmlp_in] rows):

@@ -55,10 +55,10 @@ E2M1_TABLE = np.array([e2m1_value(c) for c in range(16)], dtype=np.float64)
 E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
 
 
-def _round_to_grid(mag, grid_vals, grid_codes):
+def _round_to_grid_brute(mag, grid_vals, grid_codes):
     """Nearest grid value for non-negative ``mag`` (already clamped to the grid
     maximum); ties go to the code with an even mantissa LSB.  Brute force over
-    the grid: slow but evidently the definition."""
+    the grid: slow but evidently the definition (pins ``_round_to_grid``)."""
     mag = np.asarray(mag, np.float64)
     d = np.abs(mag[..., None] - grid_vals)                  # [..., G]
     best = d.min(axis=-1, keepdims=True)
@@ -70,6 +70,20 @@ def _round_to_grid(mag, grid_vals, grid_codes):
     choose = np.where(has_even, pick_even, tie_ok)
     idx = np.argmax(choose, axis=-1)
     return grid_codes[idx]
+
+
+def _round_to_grid(mag, grid_vals, grid_codes):
+    """Same result as ``_round_to_grid_brute`` in O(log G) per value: the
+    grid is increasing, so the nearest value is found by locating ``mag``
+    among the midpoints of neighbouring grid values (exact in float64); a
+    value equal to a midpoint is a tie and takes the even code of the two."""
+    mag = np.asarray(mag, np.float64)
+    mid = 0.5 * (grid_vals[:-1] + grid_vals[1:])
+    i = np.searchsorted(mid, mag, side="left")          # first midpoint >= mag
+    tie = (i < len(mid)) & (mid[np.minimum(i, len(mid) - 1)] == mag)
+    lo_code = grid_codes[i]
+    hi_code = grid_codes[np.minimum(i + 1, len(grid_codes) - 1)]
+    return np.where(tie & (lo_code % 2 != 0), hi_code, lo_code)
 
 
 _E2M1_POS_CODES = np.arange(8)

@@ -120,3 +120,43 @@ def test_forward_argument_validation_before_any_launch():
     assert L.flux3_ln_modulate(16, 4, 16, 16, ctypes.c_float(0.0), 16, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_rope_tables(16, 4, ctypes.c_float(-1.0), 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_selftest_wait_timeout(0, None) == F3.FLUX3_ERR_INVALID_ARG
+
+
+def test_nvfp4_sizes_and_validation():
+    L = F3.lib()
+    cfg = F3.flux3_default_config()
+    cfg.wfmt = F3.FLUX3_W_NVFP4
+    per_block = 27648 * 3072 // 2 + 27648 * 3072 // 16 + 3072 * 12288 // 2 + 3072 * 12288 // 16
+    assert per_block == 69_009_408                      # 4.5 bits per weight
+    assert 28 * per_block <= F3.flux3_packed_weight_bytes(cfg) < 28 * (per_block + 8 * 256)
+    bf = F3.flux3_default_config()
+    # the NVFP4 workspace adds one block's weights in bf16
+    assert F3.flux3_workspace_bytes(cfg, 4608) - F3.flux3_workspace_bytes(bf, 4608) >= (27648 + 12288) * 3072 * 2
+    cfg.n_blocks = 1
+    h = ctypes.c_void_p()
+    w = (F3.flux3_block_weights_nvfp4 * 1)()
+    # bf16 init refuses an NVFP4 config and vice versa
+    wb = (F3.flux3_block_weights * 1)()
+    for k, _ in F3.flux3_block_weights._fields_:
+        setattr(wb[0], k, 4096)
+    assert L.flux3_block_init(ctypes.byref(h), ctypes.byref(cfg), wb, 1, 256, 1 << 40, None) == F3.FLUX3_ERR_INVALID_ARG
+    bf.n_blocks = 1
+    assert L.flux3_block_init_nvfp4(ctypes.byref(h), ctypes.byref(bf), w, 1, 256, 1 << 40, None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_block_init_nvfp4(ctypes.byref(h), ctypes.byref(cfg), w, 1, 256, 1 << 40, None) == \
+        F3.FLUX3_ERR_INVALID_ARG                         # null tensors
+    for k in F3.NVFP4_MATRICES:
+        t = getattr(w[0], k)
+        t.codes, t.scales, t.global_scale = 4096, 8192, 12288
+    w[0].query_norm, w[0].key_norm = 256, 512
+    assert L.flux3_block_init_nvfp4(ctypes.byref(h), ctypes.byref(cfg), w, 1, 256, 1024, None) == \
+        F3.FLUX3_ERR_WORKSPACE
+    w[0].mlp_out.global_scale = 12290
+    assert L.flux3_block_init_nvfp4(ctypes.byref(h), ctypes.byref(cfg), w, 1, 256, 1 << 40, None) == \
+        F3.FLUX3_ERR_ALIGNMENT
+    assert h.value is None
+    # quantiser: cols must be a multiple of 16, pointers aligned
+    assert L.flux3_quantize_nvfp4(16, 4, 40, 16, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_quantize_nvfp4(16, 0, 32, 16, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_quantize_nvfp4(18, 4, 32, 16, 16, 16, None) == F3.FLUX3_ERR_ALIGNMENT
+    assert L.flux3_dequantize_block(None, 0, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG

@@ -63,3 +63,17 @@ def test_quantise_dequantise_error_bound_and_layout():
     # the block maximum maps to the top of the grid (6) up to the scale rounding
     blk = np.abs(w[0, :16]).max()
     assert abs(blk / (Q.E4M3_TABLE[scales[0, 0]] * float(g)) - 6.0) < 6.0 * 2 ** -3
+
+
+def test_fast_grid_rounding_equals_brute_force_definition():
+    """The searchsorted rounding used by quantize() picks exactly what the
+    brute-force nearest-value search (ties to the even code) picks: on random
+    values, on every grid value, on every midpoint (a tie) and one ulp either
+    side of it, for both the E2M1 and the E4M3 grids."""
+    rng = np.random.default_rng(5)
+    for vals, codes in ((Q._E2M1_POS_VALS, Q._E2M1_POS_CODES), (Q._E4M3_POS_VALS, Q._E4M3_POS_CODES)):
+        mid = 0.5 * (vals[:-1] + vals[1:])
+        x = np.concatenate([rng.uniform(0, vals[-1], 50000), vals, mid, np.nextafter(mid, 0),
+                            np.nextafter(mid, np.inf), vals[-1] * 2.0 ** rng.uniform(-16, 0, 5000)])
+        x = np.minimum(x, vals[-1])
+        assert np.array_equal(Q._round_to_grid(x, vals, codes), Q._round_to_grid_brute(x, vals, codes))
