@@ -183,8 +183,8 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
   CUtensorMap tmH, tmCat, tmWin, tmWout;
   if (!make_tmap_bf16(&tmH, ws.h, (uint64_t)T, kHidden, kBM)) return FLUX3_ERR_CUDA;
   if (!make_tmap_bf16(&tmCat, ws.cat, (uint64_t)T, kCatCols, kBM)) return FLUX3_ERR_CUDA;
-  if (fp4 && (!make_tmap_bf16(&tmWin, ws.w_in, kInRows, kHidden, kBN) ||
-              !make_tmap_bf16(&tmWout, ws.w_out, kHidden, kCatCols, kBN)))
+  if (fp4 && (!make_tmap_bf16(&tmWin, ws.w_in, kInRows, kHidden, kBoxB) ||
+              !make_tmap_bf16(&tmWout, ws.w_out, kHidden, kCatCols, kBoxB)))
     return FLUX3_ERR_CUDA;
   for (int b = first; b < first + count; ++b) {
     if (fp4) F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s));
@@ -359,8 +359,8 @@ flux3_status flux3_block_init(flux3_handle **out, const flux3_config *cfg, const
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(norms + (size_t)b * 2 * kHeadDim + kHeadDim, bw.key_norm, kHeadDim * 4,
                           cudaMemcpyDeviceToDevice, s);
-    if (e == cudaSuccess && (!make_tmap_bf16(&h->tm_in[b], win, kInRows, kHidden, kBN) ||
-                             !make_tmap_bf16(&h->tm_out[b], wout, kHidden, kCatCols, kBN)))
+    if (e == cudaSuccess && (!make_tmap_bf16(&h->tm_in[b], win, kInRows, kHidden, kBoxB) ||
+                             !make_tmap_bf16(&h->tm_out[b], wout, kHidden, kCatCols, kBoxB)))
       e = cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) {
@@ -572,7 +572,8 @@ flux3_status flux3_gemm_bf16(const void *A, const void *B, void *C, int M, int N
   if (!A || !B || !C || M < 1 || N < kBN || K < kBK || N % kBN != 0 || K % kBK != 0) return FLUX3_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return FLUX3_ERR_ALIGNMENT;
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, kBM) || !make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, kBN))
+  if (!make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, kBM) ||
+      !make_tmap_bf16(&tb, B, (uint64_t)N, (uint64_t)K, kBoxB))
     return FLUX3_ERR_CUDA;
   EpiParams ep{};
   ep.C = static_cast<__nv_bfloat16 *>(C);

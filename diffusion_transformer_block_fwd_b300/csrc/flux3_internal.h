@@ -21,9 +21,11 @@ constexpr int kCatCols = kHidden + kMlp;       // attention | SwiGLU  (K of the 
 constexpr int kInRows = 3 * kHidden + 2 * kMlp; // rows of the packed in-projection weight
 constexpr int kRopePairs = kHeadDim / 2;       // 64 = 4 axes x 16 pairs
 
-// GEMM tile shape (tcgen05, one CTA per tile row-block of 128 x 256).
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+// GEMM tile shape (tcgen05, a CTA pair per 256 x 256 output tile; each CTA
+// loads boxes of 128 rows x 64 columns of A and of B).
+constexpr int kBM = 128;      // rows of one A box (one CTA's share of the 256-row tile)
+constexpr int kBN = 256;      // output columns of a tile
+constexpr int kBoxB = 128;    // rows of one B box (one CTA's share of the tile's 256 B rows)
 constexpr int kBK = 64;
 
 enum EpiMode : int { EPI_STORE = 0, EPI_IN_PROJ = 1, EPI_OUT_RESIDUAL = 2 };

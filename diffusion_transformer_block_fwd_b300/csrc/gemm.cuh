@@ -7,12 +7,20 @@
 //                     silu(a) * b of the MLP half
 //   EPI_OUT_RESIDUAL  x += gate[stream] * C  (fp32 residual, in place)
 //
-// Roles (192 threads): warp 0 issues TMA loads of 128x64 A and 256x64 B tiles
-// (128-byte swizzle) into a 4-stage ring; warp 1 owns the 512-column TMEM
-// allocation and issues 128x256x16 MMAs from one thread into one of two
-// accumulators; warps 2-5 drain the other accumulator through tcgen05.ld
-// (each warp reads its own 32-lane quarter, one output row per thread) and
-// run the epilogue, so the epilogue of tile i overlaps the MMAs of tile i+1.
+// CTA pairs (clusters of 2 on one TPC) share each 256 x 256 output tile:
+// the even CTA of the pair (the leader) issues tcgen05.mma.cta_group::2 with
+// M = 256, N = 256; each CTA holds its own 128 rows of the A tile and 128 of
+// the 256 B rows in shared memory, and its own 128 accumulator rows in tensor
+// memory.  Per SM that halves the B operand bytes the tensor core reads from
+// shared memory and the bytes TMA writes, against a one-CTA 128 x 256 tile.
+//
+// Roles (192 threads per CTA): warp 0 issues the CTA's TMA loads (128 x 64
+// of A, 128 x 64 of B, 128-byte swizzle) into a 6-stage ring, completing on
+// the leader's stage barrier; warp 1 owns the 512-column TMEM allocation (two
+// 256-column accumulators) and, in the leader, issues the MMAs from one
+// thread and commits to both CTAs' barriers; warps 2-5 drain the other
+// accumulator through tcgen05.ld (one output row per thread) and run the
+// epilogue, so the epilogue of tile i overlaps the MMAs of tile i+1.
 // Every wait is bounded (see mbar_wait); on a timeout the CTA drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 
@@ -25,18 +33,21 @@ namespace flux3 {
 
 namespace gemm_detail {
 
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;
-constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 2;   // 32 KB
+constexpr int kRowsPerCta = 128;               // A rows and B rows each CTA of a pair holds
+constexpr int kTileM = 2 * kRowsPerCta;        // 256 output rows per pair tile
+constexpr uint32_t kABytes = kRowsPerCta * kBK * 2;   // 16 KB
+constexpr uint32_t kBBytes = kRowsPerCta * kBK * 2;   // 16 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kTmemCols = 512;           // two 128 x 256 fp32 accumulators
+constexpr uint32_t kPairStageBytes = 2 * kStageBytes; // both CTAs' loads of one stage
+constexpr uint32_t kTmemCols = 512;                   // two 128-lane x 256-column fp32 accumulators
 
 struct SharedCtl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t tmem_full[2];
-  uint64_t tmem_empty[2];
+  uint64_t full[kStages];      // leader: both CTAs' TMA bytes of the stage landed
+  uint64_t empty[kStages];     // every CTA: the stage's MMAs are done
+  uint64_t tmem_full[2];       // every CTA: the accumulator holds a finished tile
+  uint64_t tmem_empty[2];      // leader: all 256 epilogue threads of the pair drained it
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -172,7 +183,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, int M, in
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
                 int K, EpiParams ep) {
   extern __shared__ uint8_t smem_raw[];
@@ -183,7 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int num_m = (M + kBM - 1) / kBM;
+  const uint32_t rank = cluster_ctarank();          // 0 = leader, 1 = peer
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x / 2, num_pairs = gridDim.x / 2;
+  const int num_m = (M + kTileM - 1) / kTileM;
   const int num_n = N / kBN;
   const int num_tiles = num_m * num_n;
   const int num_kb = K / kBK;
@@ -195,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tmem_full[a], 1);
-      mbar_init(&ctl->tmem_empty[a], 128);
+      mbar_init(&ctl->tmem_empty[a], 2 * 128);
     }
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -206,33 +220,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&ctl->tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();          // both CTAs' barriers are initialised before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (both CTAs): this CTA's 128 A rows and
+      // 128 B rows of each stage, completing on the leader's full barrier
       int last_phase[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
         const int m_blk = tile % num_m, n_blk = tile / num_m;
+        const int a_row = m_blk * kTileM + (int)rank * kRowsPerCta;
+        const int b_row = n_blk * kBN + (int)rank * kRowsPerCta;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
-          tma_load_2d(smA + stage * kABytes, &tmA, &ctl->full[stage], kb * kBK, m_blk * kBM);
-          tma_load_2d(smB + stage * kBBytes, &tmB, &ctl->full[stage], kb * kBK, n_blk * kBN);
+          const uint32_t full_leader = map_to_cta(smem_addr(&ctl->full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&ctl->full[stage], kPairStageBytes);
+          tma_load_2d_pair(smA + stage * kABytes, &tmA, full_leader, kb * kBK, a_row);
+          tma_load_2d_pair(smB + stage * kBBytes, &tmB, full_leader, kb * kBK, b_row);
           last_phase[stage] = (int)phase;
           if (++stage == kStages) {
             stage = 0;
@@ -240,19 +258,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {  // let every copy still in flight land before the CTA exits
+      if (!ok && leader) {  // both CTAs' copies complete on the leader's barriers
         for (int s = 0; s < kStages; ++s)
           if (last_phase[s] >= 0) drain_wait(&ctl->full[s], (uint32_t)last_phase[s]);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16(kBM, kBN, false);
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (leader only): 256 x 256 x 16 per instruction
+      constexpr uint32_t idesc = idesc_bf16(kTileM, kBN, false);
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1, abort)) break;
@@ -270,42 +288,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t adesc = smem_desc(a0 + k * 32, 16, 1024, kSwizzle128B);
             const uint64_t bdesc = smem_desc(b0 + k * 32, 16, 1024, kSwizzle128B);
-            mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+            mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
           }
-          mma_commit(&ctl->empty[stage]);
+          mma_commit_pair_mc(&ctl->empty[stage], 0x3);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
-        if (ok) mma_commit(&ctl->tmem_full[acc]);
+        if (ok) mma_commit_pair_mc(&ctl->tmem_full[acc], 0x3);
       }
       // all MMAs issued by this thread are complete once `drain` arrives
-      mma_commit(&ctl->drain);
+      mma_commit_pair(&ctl->drain);
       drain_wait(&ctl->drain, 0);
     }
   } else {
-    // ---------------- epilogue warps 2..5
+    // ---------------- epilogue warps 2..5 (both CTAs): this CTA's 128 rows
     const int quarter = warp & 3;
-    const int row_in_tile = quarter * 32 + lane;
+    const int row_in_tile = (int)rank * kRowsPerCta + quarter * 32 + lane;
+    const uint32_t empty_leader0 = map_to_cta(smem_addr(&ctl->tmem_empty[0]), 0);
+    const uint32_t empty_leader1 = map_to_cta(smem_addr(&ctl->tmem_empty[1]), 0);
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++local) {
       const int m_blk = tile % num_m, n_blk = tile / num_m;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait(&ctl->tmem_full[acc], acc_phase, abort)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kBN;
-      epilogue_tile<EPI>(taddr, m_blk * kBM + row_in_tile, M, n_blk, ep);
+      epilogue_tile<EPI>(taddr, m_blk * kTileM + row_in_tile, M, n_blk, ep);
       tc_fence_before();
-      mbar_arrive(&ctl->tmem_empty[acc]);
+      mbar_arrive_cluster(acc ? empty_leader1 : empty_leader0);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();          // neither CTA leaves while its pair may still touch its memory
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
 template <int EPI>
@@ -317,8 +338,9 @@ cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, i
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int tiles = ((M + kBM - 1) / kBM) * (N / kBN);
-  const int grid = tiles < num_sms() ? tiles : num_sms();
+  const int tiles = ((M + kTileM - 1) / kTileM) * (N / kBN);
+  const int pairs = num_sms() / 2;
+  const int grid = 2 * (tiles < pairs ? tiles : pairs);
   gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, M, N, K, ep);
   return cudaGetLastError();
 }
