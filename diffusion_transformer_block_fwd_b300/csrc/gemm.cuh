@@ -14,13 +14,14 @@
 // memory.  Per SM that halves the B operand bytes the tensor core reads from
 // shared memory and the bytes TMA writes, against a one-CTA 128 x 256 tile.
 //
-// Roles (192 threads per CTA): warp 0 issues the CTA's TMA loads (128 x 64
+// Roles (320 threads per CTA): warp 0 issues the CTA's TMA loads (128 x 64
 // of A, 128 x 64 of B, 128-byte swizzle) into a 6-stage ring, completing on
 // the leader's stage barrier; warp 1 owns the 512-column TMEM allocation (two
 // 256-column accumulators) and, in the leader, issues the MMAs from one
-// thread and commits to both CTAs' barriers; warps 2-5 drain the other
-// accumulator through tcgen05.ld (one output row per thread) and run the
-// epilogue, so the epilogue of tile i overlaps the MMAs of tile i+1.
+// thread and commits to both CTAs' barriers; warps 2-9 drain the other
+// accumulator through tcgen05.ld (one output row and one 128-column half per
+// thread) and run the epilogue, so the epilogue of tile i overlaps the MMAs
+// of tile i+1.
 // Every wait is bounded (see mbar_wait); on a timeout the CTA drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 
@@ -34,7 +35,7 @@ namespace flux3 {
 namespace gemm_detail {
 
 constexpr int kStages = 6;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kRowsPerCta = 128;               // A rows and B rows each CTA of a pair holds
 constexpr int kTileM = 2 * kRowsPerCta;        // 256 output rows per pair tile
 constexpr uint32_t kABytes = kRowsPerCta * kBK * 2;   // 16 KB
@@ -47,7 +48,7 @@ struct SharedCtl {
   uint64_t full[kStages];      // leader: both CTAs' TMA bytes of the stage landed
   uint64_t empty[kStages];     // every CTA: the stage's MMAs are done
   uint64_t tmem_full[2];       // every CTA: the accumulator holds a finished tile
-  uint64_t tmem_empty[2];      // leader: all 256 epilogue threads of the pair drained it
+  uint64_t tmem_empty[2];      // leader: all 512 epilogue threads of the pair drained it
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -77,17 +78,22 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_
                       pack_bf16x2(f32(r[8 * q + 4]), f32(r[8 * q + 5])), pack_bf16x2(f32(r[8 * q + 6]), f32(r[8 * q + 7])));
 }
 
-// Epilogue of one 128 x 256 accumulator tile for the thread's row.
-// taddr: TMEM address of (this warp's lane quarter, column 0 of the tile).
+// Epilogue of one half (128 of the 256 columns) of the thread's accumulator
+// row.  taddr: TMEM address of (this warp's lane quarter, column 0 of the
+// tile).  Column half `half` is: for q / k tiles head `half` of the tile's two
+// heads, for v and plain tiles columns 128*half .. +127, for MLP tiles the
+// SwiGLU outputs 64*half .. +63 (a in columns 0..127, b in 128..255).
 template <int EPI>
-__device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, int M, int n_blk, const EpiParams &ep) {
+__device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int M, int n_blk, int half,
+                                              const EpiParams &ep) {
   const bool live = row < M;
-  const int n0 = n_blk * kBN;
+  const int n0 = n_blk * kBN + half * 128;    // first output column of this half (not for MLP tiles)
+  const uint32_t th = taddr + half * 128;
   uint32_t r[32];
   if constexpr (EPI == EPI_STORE) {
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      tmem_ld32(taddr + c * 32, r);
+    for (int c = 0; c < 4; ++c) {
+      tmem_ld32(th + c * 32, r);
       if (live) store_row_bf16(ep.C + (size_t)row * ep.ldc + n0 + c * 32, r);
     }
   } else if constexpr (EPI == EPI_OUT_RESIDUAL) {
@@ -95,8 +101,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, int M, in
     const float4 *gate = reinterpret_cast<const float4 *>(ep.mod + (size_t)s * kModLen + 2 * kHidden + n0);
     float4 *xr = reinterpret_cast<float4 *>(ep.x + (size_t)(live ? row : 0) * kHidden + n0);
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      tmem_ld32(taddr + c * 32, r);
+    for (int c = 0; c < 4; ++c) {
+      tmem_ld32(th + c * 32, r);
       if (live) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -114,56 +120,67 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, int M, in
     constexpr int kQTiles = kHidden / kBN;          // 12
     constexpr int kVEnd = 3 * kHidden / kBN;        // 36
     if (n_blk < 2 * kQTiles) {
-      // q or k: two heads per tile; RMSNorm over the 128 dims of each head in
-      // fp32 straight from the accumulator, then RoPE on adjacent pairs; the
-      // 32 columns of chunk c are exactly RoPE axis c (t, h, w, l).
-      const float *nscale = n_blk < kQTiles ? ep.qnorm : ep.knorm;
+      // q or k, head `half` of the tile: RMSNorm over its 128 dims in fp32
+      // straight from the accumulator, then RoPE on adjacent pairs; the 32
+      // columns of chunk c are exactly RoPE axis c (t, h, w, l).
+      const float4 *nscale4 = reinterpret_cast<const float4 *>(n_blk < kQTiles ? ep.qnorm : ep.knorm);
       const int rrow = live ? row : 0;
-      const float *cs_row = ep.cos_tab + (size_t)rrow * kRopePairs;
-      const float *sn_row = ep.sin_tab + (size_t)rrow * kRopePairs;
+      const float4 *cs4 = reinterpret_cast<const float4 *>(ep.cos_tab + (size_t)rrow * kRopePairs);
+      const float4 *sn4 = reinterpret_cast<const float4 *>(ep.sin_tab + (size_t)rrow * kRopePairs);
+      float ss = 0.f;
 #pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        float ss = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(taddr + hh * 128 + c * 32, r);
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(th + c * 32, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ss = fmaf(f32(r[i]), f32(r[i]), ss);
+        for (int i = 0; i < 32; ++i) ss = fmaf(f32(r[i]), f32(r[i]), ss);
+      }
+      const float inv = rsqrtf(ss * (1.0f / kHeadDim) + ep.eps_rms);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        // this chunk's 16 RoPE pairs and 32 norm scales, 16-byte loads issued
+        // ahead of the TMEM read
+        float cs[16], sn[16], ns[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 a = __ldg(cs4 + c * 4 + q), b = __ldg(sn4 + c * 4 + q);
+          cs[4 * q] = a.x, cs[4 * q + 1] = a.y, cs[4 * q + 2] = a.z, cs[4 * q + 3] = a.w;
+          sn[4 * q] = b.x, sn[4 * q + 1] = b.y, sn[4 * q + 2] = b.z, sn[4 * q + 3] = b.w;
         }
-        const float inv = rsqrtf(ss * (1.0f / kHeadDim) + ep.eps_rms);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(taddr + hh * 128 + c * 32, r);
-          uint32_t o[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float x0 = f32(r[2 * j]) * inv * __ldg(nscale + c * 32 + 2 * j);
-            const float x1 = f32(r[2 * j + 1]) * inv * __ldg(nscale + c * 32 + 2 * j + 1);
-            const float cs = __ldg(cs_row + c * 16 + j);
-            const float sn = __ldg(sn_row + c * 16 + j);
-            o[j] = pack_bf16x2(x0 * cs - x1 * sn, x0 * sn + x1 * cs);
-          }
-          if (live) {
-            uint4 *d = reinterpret_cast<uint4 *>(ep.qkv + (size_t)row * kQkvCols + n0 + hh * 128 + c * 32);
+        for (int q = 0; q < 8; ++q) {
+          const float4 a = __ldg(nscale4 + c * 8 + q);
+          ns[4 * q] = a.x, ns[4 * q + 1] = a.y, ns[4 * q + 2] = a.z, ns[4 * q + 3] = a.w;
+        }
+        tmem_ld32(th + c * 32, r);
+        uint32_t o[16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-          }
+        for (int j = 0; j < 16; ++j) {
+          const float x0 = f32(r[2 * j]) * inv * ns[2 * j];
+          const float x1 = f32(r[2 * j + 1]) * inv * ns[2 * j + 1];
+          o[j] = pack_bf16x2(x0 * cs[j] - x1 * sn[j], x0 * sn[j] + x1 * cs[j]);
+        }
+        if (live) {
+          uint4 *d = reinterpret_cast<uint4 *>(ep.qkv + (size_t)row * kQkvCols + n0 + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
         }
       }
     } else if (n_blk < kVEnd) {
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        tmem_ld32(taddr + c * 32, r);
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(th + c * 32, r);
         if (live) store_row_bf16(ep.qkv + (size_t)row * kQkvCols + n0 + c * 32, r);
       }
     } else {
       // MLP tile m holds a[128m .. 128m+127] in columns 0..127 and the matching
-      // b rows in columns 128..255 (interleaved when the weights were packed).
+      // b rows in columns 128..255 (interleaved when the weights were packed);
+      // this half produces SwiGLU outputs 64*half .. 64*half+63 of the tile.
       const int m = n_blk - kVEnd;
       uint32_t b[32];
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32x2(taddr + c * 32, taddr + 128 + c * 32, r, b);
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t ca = taddr + half * 64 + c * 32;
+        tmem_ld32x2(ca, ca + 128, r, b);
         uint32_t o[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -173,12 +190,24 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, int M, in
           o[j] = pack_bf16x2(g0, g1);
         }
         if (live) {
-          uint4 *d = reinterpret_cast<uint4 *>(ep.cat + (size_t)row * kCatCols + kHidden + m * 128 + c * 32);
+          uint4 *d = reinterpret_cast<uint4 *>(ep.cat + (size_t)row * kCatCols + kHidden + m * 128 + half * 64 +
+                                               c * 32);
 #pragma unroll
           for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
         }
       }
     }
+  }
+}
+
+// Tile t of the pair schedule -> (row block, column block).
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, bool n_fast, int &m_blk, int &n_blk) {
+  if (n_fast) {
+    m_blk = t / num_n;
+    n_blk = t % num_n;
+  } else {
+    m_blk = t % num_m;
+    n_blk = t / num_m;
   }
 }
 
@@ -201,6 +230,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int num_n = N / kBN;
   const int num_tiles = num_m * num_n;
   const int num_kb = K / kBK;
+  // Tile order: consecutive pairs share the operand with more rows, so that
+  // it is read from DRAM about once and the smaller one is re-read from L2.
+  const bool n_fast = M > N;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -209,7 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tmem_full[a], 1);
-      mbar_init(&ctl->tmem_empty[a], 2 * 128);
+      mbar_init(&ctl->tmem_empty[a], 2 * 256);
     }
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -239,7 +271,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-        const int m_blk = tile % num_m, n_blk = tile / num_m;
+        int m_blk, n_blk;
+        tile_coords(tile, num_m, num_n, n_fast, m_blk, n_blk);
         const int a_row = m_blk * kTileM + (int)rank * kRowsPerCta;
         const int b_row = n_blk * kBN + (int)rank * kRowsPerCta;
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -303,22 +336,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       drain_wait(&ctl->drain, 0);
     }
   } else {
-    // ---------------- epilogue warps 2..5 (both CTAs): this CTA's 128 rows
+    // ---------------- epilogue warps 2..9 (both CTAs): this CTA's 128 rows;
+    // warp w reads TMEM lane quarter w % 4, and takes column half (w - 2) / 4
     const int quarter = warp & 3;
+    const int half = (warp - 2) / 4;
     const int row_in_tile = (int)rank * kRowsPerCta + quarter * 32 + lane;
     const uint32_t empty_leader0 = map_to_cta(smem_addr(&ctl->tmem_empty[0]), 0);
     const uint32_t empty_leader1 = map_to_cta(smem_addr(&ctl->tmem_empty[1]), 0);
     int local = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs, ++local) {
-      const int m_blk = tile % num_m, n_blk = tile / num_m;
+      int m_blk, n_blk;
+      tile_coords(tile, num_m, num_n, n_fast, m_blk, n_blk);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait(&ctl->tmem_full[acc], acc_phase, abort)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kBN;
-      epilogue_tile<EPI>(taddr, m_blk * kTileM + row_in_tile, M, n_blk, ep);
+      epilogue_half<EPI>(taddr, m_blk * kTileM + row_in_tile, M, n_blk, half, ep);
       tc_fence_before();
-      mbar_arrive_cluster(acc ? empty_leader1 : empty_leader0);
+      mbar_arrive_cluster_relaxed(acc ? empty_leader1 : empty_leader0);
     }
   }
 
