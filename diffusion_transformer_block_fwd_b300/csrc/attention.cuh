@@ -1,26 +1,30 @@
 // Bidirectional attention over all tokens of one sample (24 heads x 128, no
 // mask), tcgen05 / TMEM flash attention with two query tiles per CTA.
 //
-// CTA = (256 query rows as two 128-row tiles A and B, one head), 320 threads:
+// CTA = (256 query rows as two 128-row tiles A and B, one head), 384 threads
+// in three warpgroups:
 //   warps 0..3  softmax of tile A, one query row per thread (TMEM lane = row)
 //   warps 4..7  softmax of tile B
 //   warp 8      TMA producer: Q_A, Q_B once; K and V tiles of 128 keys in two
 //               independent 2-stage rings (128-byte swizzle, two 64-dim boxes
 //               per tile); K runs one tile ahead of V
 //   warp 9      owns the TMEM allocation and issues every MMA from one thread
+//   warps 10-11 complete the third warpgroup
+// The softmax warpgroups take 216 registers per thread and the third
+// warpgroup 72 (setmaxnreg), so a thread holds its row's 128 scores.
 // TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256..383, O_B 384..511.
 // P overwrites the first 64 columns of its S buffer as packed bf16 and is the
 // A operand of O += P V.  MMA order per key tile j:
 //   S_A(j), PV_B(j-1), S_B(j), PV_A(j)
 // so while softmax A works on S_A(j) the tensor core runs PV_B(j-1) and
 // S_B(j), and while softmax B works on S_B(j) it runs PV_A(j) and S_A(j+1).
-// Softmax, one row per thread, two passes over the S columns in TMEM (32 at
-// a time, so the scores never all sit in registers): the row max (3-input
-// max, 4 chains), then p = exp2(s * log2(e)/sqrt(128) - m) on the MUFU with
-// packed float-pair FMAs and adds, P rounded to bf16 and stored over the
-// columns already consumed.  Online max in the log2 domain with lazy rescale
-// (O is rescaled in TMEM only when a row's max grows by more than 2^8); row
-// sums in fp32.  Keys past T are masked to -inf (last key tile only).
+// Softmax per key tile: the row's 128 scores in one TMEM round trip (two
+// 64-column loads, one wait), the row max (3-input max, 4 chains), then
+// p = exp2(s * log2(e)/sqrt(128) - m) with packed float-pair FMAs and adds and
+// the MUFU exp2 (32 per clock per SM on this part), P rounded to bf16 and
+// stored over S.  Online max in the log2 domain with lazy rescale (O is
+// rescaled in TMEM only when a row's max grows by more than 2^8); row sums in
+// fp32.  Keys past T are masked to -inf (last key tile only).
 // Every wait is bounded; on a timeout the CTA drains, frees TMEM and returns.
 
 #pragma once
@@ -32,8 +36,14 @@ namespace flux3 {
 namespace attn_tc {
 
 constexpr int kRows = 128;                       // rows per query tile and keys per key tile
-constexpr int kThreads = 320;
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kThreads = 384;                     // three warpgroups
+constexpr int kWarpTma = 8, kWarpMma = 9;         // warps 10, 11 only complete the third warpgroup
+// Register split (setmaxnreg): the launch gives every thread kLaunchRegs; the
+// two softmax warpgroups take kSoftmaxRegs (a whole 128-column S row in
+// registers), the producer / MMA warpgroup keeps kOtherRegs.  The shares add
+// up to exactly the launch's allocation: 128 * (2 * 216 + 72) = 384 * 168.
+constexpr int kLaunchRegs = 168, kSoftmaxRegs = 216, kOtherRegs = 72;
+static_assert(128 * (2 * kSoftmaxRegs + kOtherRegs) == kThreads * kLaunchRegs, "register split");
 constexpr uint32_t kHalfBytes = kRows * 128;     // 128 rows x 64 bf16 (one 128-byte swizzle box)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 dims = 32 KB
 constexpr int kStages = 2;
@@ -61,13 +71,6 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
       return;
     }
   }
-}
-
-// Keys at or past `valid` (counted from the chunk's first column) get -inf.
-__device__ __forceinline__ void mask_keys(uint32_t (&r)[32], int valid) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (i >= valid) r[i] = __float_as_uint(-INFINITY);
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -134,6 +137,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
 
+  if (warp >= kWarpTma) {
+    // third warpgroup: one register share for all four of its warps (the
+    // reallocation is a warpgroup-wide instruction), then the TMA and MMA roles
+    regs_decrease<kOtherRegs>();
+  }
   if (warp == kWarpTma) {
     if (lane == 0) {
       // ---------------- TMA producer: K_0, then per tile j: K_{j+1}, V_j
@@ -225,8 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&ctl->drain);
       drain_wait(&ctl->drain, 0);
     }
-  } else {
+  } else if (warp < kWarpTma) {
     // ---------------- softmax / correction / epilogue of tile x, one row per thread
+    regs_increase<kSoftmaxRegs>();
     const int x = warp / 4;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -242,17 +251,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j > 0 && !(ok = mbar_wait(&ctl->o_done[x], (j - 1) & 1, abort))) break;
       tc_fence_after();
       const int valid = T - j * kRows;   // keys of this tile that exist (< 128 only in the last tile)
-      // pass 1: row max of the raw scores, 4 chains of 3-input max (scale > 0 commutes with max)
+      // the row's 128 scores in registers, one TMEM round trip
+      uint32_t sv[128];
+      tmem_ld128(t_s, sv);
+      if (valid < kRows) {               // the ragged last tile only (uniform branch)
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= valid) sv[i] = __float_as_uint(-INFINITY);
+      }
+      // row max of the raw scores, 4 chains of 3-input max (scale > 0 commutes with max)
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(t_s + c * 32, r);
-        if (valid < kRows) mask_keys(r, valid - c * 32);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          m4[i & 3] = max3(m4[i & 3], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-      }
+      for (int i = 0; i < 64; ++i)
+        m4[i & 3] = max3(m4[i & 3], __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
       const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;
       const float m_new = fmaxf(m, mx);
       const bool need = (j > 0) && (m_new > m + 8.0f);
@@ -271,27 +282,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(t_o + c * 32, o);
         }
       }
-      // pass 2: p = 2^(s * scale_log2 - m) in float pairs, rounded to bf16 and
-      // stored over the consumed S columns (chunk c -> columns 16c .. 16c+15);
-      // the row sum in 4 independent pair accumulators
+      // p = 2^(s * scale_log2 - m) in float pairs (packed FMA, MUFU exp2,
+      // packed row sum in 4 pair accumulators), rounded to bf16 and packed in
+      // place: pair k (columns 2k, 2k+1) -> sv[k]
       const float neg_m = -m;
       float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32], pk[16];
-        tmem_ld32(t_s + c * 32, r);
-        if (valid < kRows) mask_keys(r, valid - c * 32);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float a, b;
-          fma2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]), scale_log2, neg_m, a, b);
-          const float p0 = ex2_approx(a), p1 = ex2_approx(b);
-          add2(sum[2 * (k & 3)], sum[2 * (k & 3) + 1], p0, p1);
-          pk[k] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(t_s + c * 16, pk);
+      for (int k = 0; k < 64; ++k) {
+        float a, b;
+        fma2(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]), scale_log2, neg_m, a, b);
+        const float p0 = ex2_approx(a), p1 = ex2_approx(b);
+        add2(sum[2 * (k & 3)], sum[2 * (k & 3) + 1], p0, p1);
+        sv[k] = pack_bf16x2(p0, p1);
       }
       l += ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+      tmem_st32(t_s, *reinterpret_cast<uint32_t(*)[32]>(sv));
+      tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctl->p_full[x]);
@@ -330,7 +336,12 @@ cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat
   using namespace attn_tc;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    // the warpgroup register split assumes exactly kLaunchRegs per thread at launch
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attention_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
