@@ -349,6 +349,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tile_coords(tile, num_m, num_n, n_fast, m_blk, n_blk);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
+      if constexpr (EPI == EPI_OUT_RESIDUAL) {
+        // the residual row this thread updates does not depend on the
+        // accumulator: start its 512 bytes towards L2 while the MMAs run
+        const int row = m_blk * kTileM + row_in_tile;
+        if (row < M) {
+          const float *xr = ep.x + (size_t)row * kHidden + n_blk * kBN + half * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) prefetch_l2(xr + 32 * q);
+        }
+      }
       if (!mbar_wait(&ctl->tmem_full[acc], acc_phase, abort)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kBN;

@@ -93,6 +93,9 @@ WORKLOADS = {
     # 28-block stack, 1024x1024 + two 512x512 references, 16 calls
     "stack28_1024sq_2ref512_t6656": dict(spec=[("txt", 512), ("image", (64, 64))] + [("image_cond", (32, 32))] * 2,
                                          blocks=28, calls=16, wfmt="bf16"),
+    # 28-block stack, 1024x1024 target + one 1024x1024 reference (the one-block layout above)
+    "stack28_1024sq_ref1_t8704": dict(spec=[("txt", 512), ("image", (64, 64)), ("image_cond", (64, 64))],
+                                      blocks=28, calls=1, wfmt="bf16"),
     # 28-block stack, NVFP4 weights, 1024x1024 + ten 512x512 references
     "stack28_nvfp4_1024sq_10ref512_t14848": dict(
         spec=[("txt", 512), ("image", (64, 64))] + [("image_cond", (32, 32))] * 10,
