@@ -36,7 +36,7 @@ def _rank_main(rank, world, port, step_ms, out):
 def test_two_replicas_report_all_units_over_the_slowest_rank():
     world = 2
     step_ms = [1.0, 1.25]                    # rank 1 is the slower replica
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), step_ms, out), nprocs=world, join=True)
         res = dict(out)
