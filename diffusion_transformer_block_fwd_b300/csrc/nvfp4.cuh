@@ -11,8 +11,9 @@
 //               q = e2m1_RNE(w / (s_b g)), saturating at +-6, no negative zero.
 //               Every rounding decision is taken in float64 on exactly the
 //               quotients the definition names, so codes are reproducible.
-//   dequantize  the packed block weights -> bf16, each weight rounded once
-//               (to nearest even) from the exact product e2m1 * e4m3 * g.
+//   dequantize  the packed block weights -> bf16: e2m1 * e4m3 (exact in
+//               float32) times g, rounded to float32, then to bf16 (both
+//               nearest even).
 //
 // The dequantised bf16 matrices feed the same tcgen05 GEMMs as bf16
 // checkpoints (the activations stay bf16, so the FP4 tensor-core kinds, which
@@ -77,20 +78,6 @@ __device__ __forceinline__ float e2m1_decode(uint32_t c) {
 __device__ __forceinline__ float e4m3_decode_f(uint32_t c) {
   const uint32_t e = (c >> 3) & 15u, m = c & 7u;
   return e == 0 ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
-}
-
-// bf16 (round to nearest even) of the exact product p * g, p = e2m1 * e4m3
-// (exact in float32).  hi + lo is the product exactly; hi alone decides the
-// rounding except when hi lies exactly halfway between two bf16 values.
-__device__ __forceinline__ uint32_t bf16_of_product(float p, float g) {
-  const float hi = p * g;
-  const float lo = fmaf(p, g, -hi);
-  const uint32_t b = __float_as_uint(hi);
-  if ((b & 0xFFFFu) == 0x8000u && lo != 0.0f) {
-    const bool away = (lo > 0.0f) == (hi > 0.0f);
-    return away ? (b + 0x8000u) >> 16 : b >> 16;
-  }
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi));
 }
 
 // ---------------------------------------------------------------- quantiser
@@ -169,9 +156,23 @@ struct Fp4BlockView {
 constexpr uint32_t kInGroups = (uint32_t)kInRows * (kHidden / kGroup);     // 5,308,416
 constexpr uint32_t kOutGroups = (uint32_t)kHidden * (kCatCols / kGroup);   // 2,359,296
 
+// (a, b) *= (m, m) as one packed float-pair multiply (round to nearest even).
+__device__ __forceinline__ void mul2(float &a, float &b, float m) {
+  asm("{\n .reg .b64 x, y, d;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %2};\n mul.rn.f32x2 d, x, y;\n"
+      " mov.b64 {%0, %1}, d;\n}"
+      : "+f"(a), "+f"(b)
+      : "f"(m));
+}
+
+// One thread per 16-weight group: the 8 code bytes are decoded through a
+// 256-entry shared table (byte -> the two e2m1 values), scaled by the group's
+// e4m3 scale (exact) and the tensor's global scale with packed float-pair
+// multiplies, and packed to bf16 pairs.
 __global__ void __launch_bounds__(256)
     dequantize_block_kernel(Fp4BlockView v, __nv_bfloat16 *__restrict__ w_in, __nv_bfloat16 *__restrict__ w_out) {
+  __shared__ float2 pair_of_byte[256];
   __shared__ float gs[6];
+  pair_of_byte[threadIdx.x] = make_float2(e2m1_decode(threadIdx.x & 0xFu), e2m1_decode(threadIdx.x >> 4));
   if (threadIdx.x < 6) gs[threadIdx.x] = v.globals[threadIdx.x];
   __syncthreads();
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < kInGroups + kOutGroups; i += gridDim.x * blockDim.x) {
@@ -192,9 +193,10 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const uint32_t byte = ((k < 4 ? c.x : c.y) >> (8 * (k % 4))) & 0xFFu;
-      const uint32_t lo = bf16_of_product(e2m1_decode(byte & 0xFu) * s, g);
-      const uint32_t hi = bf16_of_product(e2m1_decode(byte >> 4) * s, g);
-      o[k] = lo | (hi << 16);
+      float2 e = pair_of_byte[byte];
+      mul2(e.x, e.y, s);   // exact: 2 x 4 significant bits
+      mul2(e.x, e.y, g);
+      o[k] = pack_bf16x2(e.x, e.y);
     }
     uint4 *dst = reinterpret_cast<uint4 *>((in ? w_in : w_out) + (size_t)gi * kGroup);
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);

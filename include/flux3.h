@@ -167,8 +167,8 @@ FLUX3_API flux3_status flux3_block_init(flux3_handle **out, const flux3_config *
 /* flux3_block_init for NVFP4 weights (cfg->wfmt == FLUX3_W_NVFP4): packs the
  * codes, block scales, global scales and norm scales into `packed`
  * (flux3_packed_weight_bytes(cfg) bytes).  Every forward call then expands
- * each block's weights to bf16 in the workspace (each weight rounded once, to
- * nearest even, from the exact product of its code and scales) just before
+ * each block's weights to bf16 in the workspace (e2m1 * e4m3, exact in float32,
+ * times the global scale rounded to float32, then to bf16; both nearest even) just before
  * the block runs, and the projections run as bf16 tensor-core GEMMs with bf16
  * activations.  Same errors as flux3_block_init. */
 FLUX3_API flux3_status flux3_block_init_nvfp4(flux3_handle **out, const flux3_config *cfg,

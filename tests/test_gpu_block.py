@@ -44,10 +44,15 @@ def test_block_full_oracle(blk, name, spec):
     assert_block_output(f64(y), parts["out"], f64(x), m[lay.stream_id, 6144:], parts["y"], name)
 
 
-@pytest.mark.parametrize("workload", ["block_1024sq_t4608", "block_1024sq_ref1_t8704"])
+# the default max_tokens (16384): 1024 text tokens + 64x64 image + eleven 32x32 references
+MAX_TOKENS_SPEC = [("txt", 1024), ("image", (64, 64))] + [("image_cond", (32, 32))] * 11
+
+
+@pytest.mark.parametrize("workload", ["block_1024sq_t4608", "block_1024sq_ref1_t8704", "max_tokens_t16384"])
 def test_block_full_size_sampled_rows(blk, workload):
     w, wf, blocks = blk
-    lay = synth.build_layout(synth.WORKLOADS[workload]["spec"])
+    spec = MAX_TOKENS_SPEC if workload == "max_tokens_t16384" else synth.WORKLOADS[workload]["spec"]
+    lay = synth.build_layout(spec)
     x = synth.activations(6, lay.T, device=DEV)
     mods = synth.modulation(6, device=DEV)
     y = run_block(blocks, lay, x, mods)
