@@ -54,7 +54,11 @@ struct SharedCtl {
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + sizeof(SharedCtl);
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kBoxBytes = 32 * 128;              // one epilogue output box: 32 rows x 64 bf16
+constexpr size_t kSmemBytes =
+    1024 /*alignment slack*/ + kStages * kStageBytes + kEpiWarps * kBoxBytes + sizeof(SharedCtl);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
@@ -70,12 +74,36 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_t (&r)[32]) {
-  uint4 *d = reinterpret_cast<uint4 *>(dst);
+// One 32-row x 64-column bf16 box of an epilogue warp's output: each lane
+// writes its row's eight 16-byte chunks into the warp's 4 KB staging buffer
+// in the 128-byte-swizzled layout of the tensor map, then one lane issues a
+// TMA store, so global memory sees whole 128-byte lines instead of 16-byte
+// pieces of 32 rows per instruction.
+struct BoxWriter {
+  uint8_t *buf;
+  uint32_t lane;
+  __device__ __forceinline__ void begin() const {   // the previous box has been read out of buf
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+  }
+  __device__ __forceinline__ void put(int q, uint32_t a, uint32_t b, uint32_t c, uint32_t d) const {
+    *reinterpret_cast<uint4 *>(buf + lane * 128 + ((q ^ (lane & 7)) * 16)) = make_uint4(a, b, c, d);
+  }
+  __device__ __forceinline__ void store(const CUtensorMap *tm, int x, int y) const {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm, buf, x, y);
+      bulk_commit();
+    }
+  }
+};
+
+__device__ __forceinline__ void put_chunk_bf16(const BoxWriter &bw, int q0, const uint32_t (&r)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    d[q] = make_uint4(pack_bf16x2(f32(r[8 * q + 0]), f32(r[8 * q + 1])), pack_bf16x2(f32(r[8 * q + 2]), f32(r[8 * q + 3])),
-                      pack_bf16x2(f32(r[8 * q + 4]), f32(r[8 * q + 5])), pack_bf16x2(f32(r[8 * q + 6]), f32(r[8 * q + 7])));
+    bw.put(q0 + q, pack_bf16x2(f32(r[8 * q + 0]), f32(r[8 * q + 1])), pack_bf16x2(f32(r[8 * q + 2]), f32(r[8 * q + 3])),
+           pack_bf16x2(f32(r[8 * q + 4]), f32(r[8 * q + 5])), pack_bf16x2(f32(r[8 * q + 6]), f32(r[8 * q + 7])));
 }
 
 // Epilogue of one half (128 of the 256 columns) of the thread's accumulator
@@ -83,18 +111,27 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const uint32_
 // tile).  Column half `half` is: for q / k tiles head `half` of the tile's two
 // heads, for v and plain tiles columns 128*half .. +127, for MLP tiles the
 // SwiGLU outputs 64*half .. +63 (a in columns 0..127, b in 128..255).
+// bf16 outputs leave through the warp's staging box and TMA stores (tm0: C or
+// qkv, tm1: cat); row0 is the first of the warp's 32 rows (stores clip rows
+// past M).
 template <int EPI>
-__device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int M, int n_blk, int half,
-                                              const EpiParams &ep) {
+__device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int row0, int M, int n_blk, int half,
+                                              const EpiParams &ep, const BoxWriter &bw, const CUtensorMap *tm0,
+                                              const CUtensorMap *tm1) {
   const bool live = row < M;
   const int n0 = n_blk * kBN + half * 128;    // first output column of this half (not for MLP tiles)
   const uint32_t th = taddr + half * 128;
   uint32_t r[32];
   if constexpr (EPI == EPI_STORE) {
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      tmem_ld32(th + c * 32, r);
-      if (live) store_row_bf16(ep.C + (size_t)row * ep.ldc + n0 + c * 32, r);
+    for (int b = 0; b < 2; ++b) {
+      bw.begin();
+#pragma unroll 1
+      for (int c2 = 0; c2 < 2; ++c2) {
+        tmem_ld32(th + (2 * b + c2) * 32, r);
+        put_chunk_bf16(bw, 4 * c2, r);
+      }
+      bw.store(tm0, n0 + 64 * b, row0);
     }
   } else if constexpr (EPI == EPI_OUT_RESIDUAL) {
     const int s = live ? ep.sid[row] : 0;
@@ -137,6 +174,7 @@ __device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int M, in
       const float inv = rsqrtf(ss * (1.0f / kHeadDim) + ep.eps_rms);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
+        if ((c & 1) == 0) bw.begin();
         // this chunk's 16 RoPE pairs and 32 norm scales, 16-byte loads issued
         // ahead of the TMEM read
         float cs[16], sn[16], ns[32];
@@ -159,17 +197,20 @@ __device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int M, in
           const float x1 = f32(r[2 * j + 1]) * inv * ns[2 * j + 1];
           o[j] = pack_bf16x2(x0 * cs[j] - x1 * sn[j], x0 * sn[j] + x1 * cs[j]);
         }
-        if (live) {
-          uint4 *d = reinterpret_cast<uint4 *>(ep.qkv + (size_t)row * kQkvCols + n0 + c * 32);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        }
+        for (int q = 0; q < 4; ++q) bw.put(4 * (c & 1) + q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        if (c & 1) bw.store(tm0, n0 + 64 * (c >> 1), row0);
       }
     } else if (n_blk < kVEnd) {
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(th + c * 32, r);
-        if (live) store_row_bf16(ep.qkv + (size_t)row * kQkvCols + n0 + c * 32, r);
+      for (int b = 0; b < 2; ++b) {
+        bw.begin();
+#pragma unroll 1
+        for (int c2 = 0; c2 < 2; ++c2) {
+          tmem_ld32(th + (2 * b + c2) * 32, r);
+          put_chunk_bf16(bw, 4 * c2, r);
+        }
+        bw.store(tm0, n0 + 64 * b, row0);
       }
     } else {
       // MLP tile m holds a[128m .. 128m+127] in columns 0..127 and the matching
@@ -177,6 +218,7 @@ __device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int M, in
       // this half produces SwiGLU outputs 64*half .. 64*half+63 of the tile.
       const int m = n_blk - kVEnd;
       uint32_t b[32];
+      bw.begin();
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         const uint32_t ca = taddr + half * 64 + c * 32;
@@ -189,13 +231,10 @@ __device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int M, in
           const float g1 = a1 / (1.0f + __expf(-a1)) * f32(b[2 * j + 1]);
           o[j] = pack_bf16x2(g0, g1);
         }
-        if (live) {
-          uint4 *d = reinterpret_cast<uint4 *>(ep.cat + (size_t)row * kCatCols + kHidden + m * 128 + half * 64 +
-                                               c * 32);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        }
+        for (int q = 0; q < 4; ++q) bw.put(4 * c + q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
       }
+      bw.store(tm1, kHidden + m * 128 + half * 64, row0);
     }
   }
 }
@@ -213,13 +252,15 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, bool n_
 
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
                 int K, EpiParams ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *smA = smem;
   uint8_t *smB = smem + kStages * kABytes;
-  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(smem + kStages * kStageBytes);
+  uint8_t *sOut = smem + kStages * kStageBytes;     // [epilogue warp] 4 KB output box
+  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(sOut + kEpiWarps * kBoxBytes);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -341,6 +382,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 2) / 4;
     const int row_in_tile = (int)rank * kRowsPerCta + quarter * 32 + lane;
+    const BoxWriter bw{sOut + (warp - 2) * kBoxBytes, (uint32_t)lane};
+    if (EPI != EPI_OUT_RESIDUAL && lane == 0) {
+      tma_prefetch_desc(&tmO0);
+      tma_prefetch_desc(&tmO1);
+    }
     const uint32_t empty_leader0 = map_to_cta(smem_addr(&ctl->tmem_empty[0]), 0);
     const uint32_t empty_leader1 = map_to_cta(smem_addr(&ctl->tmem_empty[1]), 0);
     int local = 0;
@@ -362,10 +408,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&ctl->tmem_full[acc], acc_phase, abort)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kBN;
-      epilogue_half<EPI>(taddr, m_blk * kTileM + row_in_tile, M, n_blk, half, ep);
+      epilogue_half<EPI>(taddr, m_blk * kTileM + row_in_tile, m_blk * kTileM + row_in_tile - lane, M, n_blk, half,
+                         ep, bw, &tmO0, &tmO1);
       tc_fence_before();
       mbar_arrive_cluster_relaxed(acc ? empty_leader1 : empty_leader0);
     }
+    if (lane == 0) bulk_wait_all();   // this warp's output stores are complete before the CTA exits
   }
 
   tc_fence_before();
@@ -384,10 +432,16 @@ cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, i
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  // output boxes of 32 rows x 64 columns for the bf16 epilogues
+  CUtensorMap tmO0 = tmA, tmO1 = tmA;
+  if (EPI == EPI_STORE && !make_tmap_bf16(&tmO0, ep.C, (uint64_t)M, (uint64_t)ep.ldc, 32)) return cudaErrorInvalidValue;
+  if (EPI == EPI_IN_PROJ && (!make_tmap_bf16(&tmO0, ep.qkv, (uint64_t)M, kQkvCols, 32) ||
+                             !make_tmap_bf16(&tmO1, ep.cat, (uint64_t)M, kCatCols, 32)))
+    return cudaErrorInvalidValue;
   const int tiles = ((M + kTileM - 1) / kTileM) * (N / kBN);
   const int pairs = num_sms() / 2;
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, M, N, K, ep);
+  gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmO0, tmO1, M, N, K, ep);
   return cudaGetLastError();
 }
 
