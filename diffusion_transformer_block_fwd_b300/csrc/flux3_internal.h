@@ -50,6 +50,10 @@ struct EpiParams {
 // {64 cols, box_rows} box and 128-byte swizzle.  Returns false on failure.
 bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
+// Encodes a 2-D float32 tensor map over a row-major [rows, cols] matrix with a
+// {32 cols, 32 rows} box and 128-byte swizzle.  Returns false on failure.
+bool make_tmap_f32_box32(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols);
+
 int num_sms();
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K,

@@ -50,6 +50,7 @@ struct SharedCtl {
   uint64_t tmem_full[2];       // every CTA: the accumulator holds a finished tile
   uint64_t tmem_empty[2];      // leader: all 512 epilogue threads of the pair drained it
   uint64_t drain;
+  uint64_t xbar[8];            // per epilogue warp: its residual box landed (out-projection)
   uint32_t tmem_base;
   int abort;
 };
@@ -99,6 +100,16 @@ struct BoxWriter {
   }
 };
 
+// The out-projection's residual x goes through the same box (32 rows x 32
+// fp32 columns): a TMA load fills it, each lane updates its row in place, and a
+// TMA store writes it back.
+__device__ __forceinline__ void load_x_box(const BoxWriter &bw, const CUtensorMap *tm, uint64_t *bar, int x, int y) {
+  if (bw.lane == 0) {
+    mbar_arrive_expect_tx(bar, kBoxBytes);
+    tma_load_2d(bw.buf, tm, bar, x, y);
+  }
+}
+
 __device__ __forceinline__ void put_chunk_bf16(const BoxWriter &bw, int q0, const uint32_t (&r)[32]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q)
@@ -115,9 +126,10 @@ __device__ __forceinline__ void put_chunk_bf16(const BoxWriter &bw, int q0, cons
 // qkv, tm1: cat); row0 is the first of the warp's 32 rows (stores clip rows
 // past M).
 template <int EPI>
-__device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int row0, int M, int n_blk, int half,
+__device__ __forceinline__ bool epilogue_half(uint32_t taddr, int row, int row0, int M, int n_blk, int half,
                                               const EpiParams &ep, const BoxWriter &bw, const CUtensorMap *tm0,
-                                              const CUtensorMap *tm1) {
+                                              const CUtensorMap *tm1, uint64_t *xbar, uint32_t &xphase,
+                                              volatile int *abort) {
   const bool live = row < M;
   const int n0 = n_blk * kBN + half * 128;    // first output column of this half (not for MLP tiles)
   const uint32_t th = taddr + half * 128;
@@ -134,23 +146,30 @@ __device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int row0,
       bw.store(tm0, n0 + 64 * b, row0);
     }
   } else if constexpr (EPI == EPI_OUT_RESIDUAL) {
+    // x[row, n0 .. n0+127] += gate[stream(row)] * acc, as four 32-column boxes;
+    // box 0's load was issued before the accumulator was waited for
     const int s = live ? ep.sid[row] : 0;
     const float4 *gate = reinterpret_cast<const float4 *>(ep.mod + (size_t)s * kModLen + 2 * kHidden + n0);
-    float4 *xr = reinterpret_cast<float4 *>(ep.x + (size_t)(live ? row : 0) * kHidden + n0);
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
+      if (!mbar_wait(xbar, xphase, abort)) return false;
+      xphase ^= 1;
       tmem_ld32(th + c * 32, r);
-      if (live) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 g = __ldg(gate + c * 8 + q);
-          float4 xv = xr[c * 8 + q];
-          xv.x = fmaf(g.x, f32(r[4 * q + 0]), xv.x);
-          xv.y = fmaf(g.y, f32(r[4 * q + 1]), xv.y);
-          xv.z = fmaf(g.z, f32(r[4 * q + 2]), xv.z);
-          xv.w = fmaf(g.w, f32(r[4 * q + 3]), xv.w);
-          xr[c * 8 + q] = xv;
-        }
+      for (int q = 0; q < 8; ++q) {
+        float4 *p = reinterpret_cast<float4 *>(bw.buf + bw.lane * 128 + ((q ^ (bw.lane & 7)) * 16));
+        const float4 g = __ldg(gate + c * 8 + q);
+        float4 xv = *p;
+        xv.x = fmaf(g.x, f32(r[4 * q + 0]), xv.x);
+        xv.y = fmaf(g.y, f32(r[4 * q + 1]), xv.y);
+        xv.z = fmaf(g.z, f32(r[4 * q + 2]), xv.z);
+        xv.w = fmaf(g.w, f32(r[4 * q + 3]), xv.w);
+        *p = xv;
+      }
+      bw.store(tm0, n0 + 32 * c, row0);
+      if (c < 3) {
+        bw.begin();
+        load_x_box(bw, tm0, xbar, n0 + 32 * (c + 1), row0);
       }
     }
   } else {  // EPI_IN_PROJ
@@ -237,6 +256,7 @@ __device__ __forceinline__ void epilogue_half(uint32_t taddr, int row, int row0,
       bw.store(tm1, kHidden + m * 128 + half * 64, row0);
     }
   }
+  return true;
 }
 
 // Tile t of the pair schedule -> (row block, column block).
@@ -285,6 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->tmem_empty[a], 2 * 256);
     }
     mbar_init(&ctl->drain, 1);
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(&ctl->xbar[w], 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -383,10 +404,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) / 4;
     const int row_in_tile = (int)rank * kRowsPerCta + quarter * 32 + lane;
     const BoxWriter bw{sOut + (warp - 2) * kBoxBytes, (uint32_t)lane};
-    if (EPI != EPI_OUT_RESIDUAL && lane == 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tmO0);
       tma_prefetch_desc(&tmO1);
     }
+    uint64_t *xbar = &ctl->xbar[warp - 2];
+    uint32_t xphase = 0;
+    bool x_in_flight = false;   // broke out with a residual box load outstanding
     const uint32_t empty_leader0 = map_to_cta(smem_addr(&ctl->tmem_empty[0]), 0);
     const uint32_t empty_leader1 = map_to_cta(smem_addr(&ctl->tmem_empty[1]), 0);
     int local = 0;
@@ -396,24 +420,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if constexpr (EPI == EPI_OUT_RESIDUAL) {
-        // the residual row this thread updates does not depend on the
-        // accumulator: start its 512 bytes towards L2 while the MMAs run
-        const int row = m_blk * kTileM + row_in_tile;
-        if (row < M) {
-          const float *xr = ep.x + (size_t)row * kHidden + n_blk * kBN + half * 128;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) prefetch_l2(xr + 32 * q);
-        }
+        // the residual does not depend on the accumulator: its first box is
+        // loaded while the MMAs of this tile still run
+        bw.begin();
+        load_x_box(bw, &tmO0, xbar, n_blk * kBN + half * 128, m_blk * kTileM + row_in_tile - lane);
       }
-      if (!mbar_wait(&ctl->tmem_full[acc], acc_phase, abort)) break;
+      if (!mbar_wait(&ctl->tmem_full[acc], acc_phase, abort)) {
+        x_in_flight = EPI == EPI_OUT_RESIDUAL;
+        break;
+      }
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kBN;
-      epilogue_half<EPI>(taddr, m_blk * kTileM + row_in_tile, m_blk * kTileM + row_in_tile - lane, M, n_blk, half,
-                         ep, bw, &tmO0, &tmO1);
+      if (!epilogue_half<EPI>(taddr, m_blk * kTileM + row_in_tile, m_blk * kTileM + row_in_tile - lane, M, n_blk,
+                              half, ep, bw, &tmO0, &tmO1, xbar, xphase, abort)) {
+        x_in_flight = true;   // only the residual box wait can fail
+        break;
+      }
       tc_fence_before();
       mbar_arrive_cluster_relaxed(acc ? empty_leader1 : empty_leader0);
     }
     if (lane == 0) bulk_wait_all();   // this warp's output stores are complete before the CTA exits
+    if (x_in_flight && lane == 0) drain_wait(xbar, xphase);   // the box must land before the CTA exits
   }
 
   tc_fence_before();
@@ -438,6 +465,7 @@ cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, i
   if (EPI == EPI_IN_PROJ && (!make_tmap_bf16(&tmO0, ep.qkv, (uint64_t)M, kQkvCols, 32) ||
                              !make_tmap_bf16(&tmO1, ep.cat, (uint64_t)M, kCatCols, 32)))
     return cudaErrorInvalidValue;
+  if (EPI == EPI_OUT_RESIDUAL && !make_tmap_f32_box32(&tmO0, ep.x, (uint64_t)M, kHidden)) return cudaErrorInvalidValue;
   const int tiles = ((M + kTileM - 1) / kTileM) * (N / kBN);
   const int pairs = num_sms() / 2;
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
