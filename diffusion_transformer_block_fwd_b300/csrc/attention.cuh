@@ -184,25 +184,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- MMA issuer
       constexpr uint32_t idesc_s = idesc_bf16(kRows, kRows, false);   // B = K tile, K-major
       constexpr uint32_t idesc_o = idesc_bf16(kRows, kHeadDim, true); // B = V tile, MN-major
-      const uint32_t q_addr = smem_addr(sQ);
+      // descriptors encoded once, moved by constant offsets per MMA (a few
+      // instructions per MMA keep the issue ahead of the tensor core while the
+      // softmax warps load the same sub-partitions)
+      const SmemDesc dq = smem_desc_split(smem_addr(sQ), 16, 1024, kSwizzle128B);
+      const SmemDesc dk = smem_desc_split(smem_addr(sK), 16, 1024, kSwizzle128B);
+      const SmemDesc dv = smem_desc_split(smem_addr(sV), kHalfBytes, 1024, kSwizzle128B);
       auto issue_s = [&](int x, int s) {
-        const uint32_t qa = q_addr + x * kTileBytes, ka = smem_addr(sK + s * kTileBytes);
 #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k) {
           const uint32_t off = (uint32_t)(k / 4) * kHalfBytes + (uint32_t)(k % 4) * 32;
-          mma_bf16_ss(tmem + col_s(x), smem_desc(qa + off, 16, 1024, kSwizzle128B),
-                      smem_desc(ka + off, 16, 1024, kSwizzle128B), idesc_s, k > 0);
+          mma_bf16_ss_at(tmem + col_s(x), dq, x * kTileBytes + off, dk, s * kTileBytes + off, idesc_s, k > 0);
         }
         mma_commit(&ctl->s_full[x]);
       };
       // O_x += P_x V: 16 keys per MMA (P columns 8k.., V rows 16k..); V is
       // MN-major: 64-dim halves 16 KB apart, 8-row groups 1 KB apart.
       auto issue_pv = [&](int x, int s, bool first) {
-        const uint32_t va = smem_addr(sV + s * kTileBytes);
 #pragma unroll
         for (int k = 0; k < kRows / 16; ++k)
-          mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + k * 8,
-                      smem_desc(va + k * 2048, kHalfBytes, 1024, kSwizzle128B), idesc_o, !(first && k == 0));
+          mma_bf16_ts_at(tmem + col_o(x), tmem + col_s(x) + k * 8, dv, s * kTileBytes + k * 2048, idesc_o,
+                         !(first && k == 0));
         mma_commit(&ctl->o_done[x]);
       };
       bool ok = mbar_wait(&ctl->q_full, 0, abort);

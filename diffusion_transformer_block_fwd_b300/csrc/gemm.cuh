@@ -362,6 +362,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0 && leader) {
       // ---------------- MMA issuer (leader only): 256 x 256 x 16 per instruction
       constexpr uint32_t idesc = idesc_bf16(kTileM, kBN, false);
+      // descriptors encoded once and moved by constant offsets per MMA
+      const SmemDesc da = smem_desc_split(smem_addr(smA), 16, 1024, kSwizzle128B);
+      const SmemDesc db = smem_desc_split(smem_addr(smB), 16, 1024, kSwizzle128B);
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
@@ -377,14 +380,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_addr(smA + stage * kABytes);
-          const uint32_t b0 = smem_addr(smB + stage * kBBytes);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t adesc = smem_desc(a0 + k * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bdesc = smem_desc(b0 + k * 32, 16, 1024, kSwizzle128B);
-            mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
-          }
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_ss_pair_at(d_tmem, da, stage * kABytes + k * 32, db, stage * kBBytes + k * 32, idesc,
+                                (kb | k) != 0);
           mma_commit_pair_mc(&ctl->empty[stage], 0x3);
           if (++stage == kStages) {
             stage = 0;

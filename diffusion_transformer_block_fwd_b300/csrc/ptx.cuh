@@ -53,15 +53,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the phase with the given parity to complete.  Returns false if
 // another role of the CTA has already given up (*abort != 0) or if the wait
 // itself ran past kWaitTimeoutNs (then it sets *abort and the error word).
+// With kCluster the observation is an acquire at cluster scope (the phase was
+// completed by arrivals that release writes of the other CTA of a pair).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           unsigned long long timeout_ns = kWaitTimeoutNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if ((n & 63u) == 0) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > timeout_ns) {
@@ -128,6 +142,12 @@ __device__ __forceinline__ void cluster_sync() {
 // callers use it only after their TMEM reads have completed (wait::ld).
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster
+// address: the thread's earlier shared-memory writes are visible to a thread of
+// the other CTA that observes the phase with an acquire at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // 2-D tiled load into this CTA's shared memory, completing on an mbarrier of
 // either CTA of the pair (bar_cluster: shared::cluster address).
@@ -291,6 +311,49 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 constexpr uint32_t kSwizzle128B = 2;
+
+// A shared-memory matrix descriptor kept as its two 32-bit halves.  The start
+// address sits in bits 0..13 of the low half (address >> 4), so moving the
+// descriptor by a byte offset (a multiple of 16 that keeps the address below
+// 256 KB) is one 32-bit add to the low half: an MMA issue loop then spends a
+// few instructions per MMA instead of re-encoding both descriptors.
+struct SmemDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SmemDesc smem_desc_split(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                                    uint32_t swizzle_mode) {
+  const uint64_t d = smem_desc(saddr, lbo_bytes, sbo_bytes, swizzle_mode);
+  return SmemDesc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
+// D[tmem] (+)= A[smem] * B[smem]^T with A, B given as descriptors moved by
+// byte offsets a_off, b_off (one CTA).
+__device__ __forceinline__ void mma_bf16_ss_at(uint32_t d_tmem, SmemDesc a, uint32_t a_off, SmemDesc b,
+                                               uint32_t b_off, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 ad, bd;\n setp.ne.b32 p, %6, 0;\n mov.b64 ad, {%1, %2};\n"
+      " mov.b64 bd, {%3, %4};\n tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo + (a_off >> 4)), "r"(a.hi), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem], B given as a descriptor moved by b_off (one CTA).
+__device__ __forceinline__ void mma_bf16_ts_at(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t b_off,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 bd;\n setp.ne.b32 p, %5, 0;\n mov.b64 bd, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A * B on the CTA pair with A, B given as descriptors moved by
+// byte offsets a_off, b_off.
+__device__ __forceinline__ void mma_bf16_ss_pair_at(uint32_t d_tmem, SmemDesc a, uint32_t a_off, SmemDesc b,
+                                                    uint32_t b_off, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 ad, bd;\n setp.ne.b32 p, %6, 0;\n mov.b64 ad, {%1, %2};\n"
+      " mov.b64 bd, {%3, %4};\n tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo + (a_off >> 4)), "r"(a.hi), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 // Instruction descriptor for kind::f16 with bf16 A/B, fp32 D.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
