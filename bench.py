@@ -274,6 +274,8 @@ def run_ours(args):
     rank, world, local, dev = dist_setup()
     F3.lib()   # fail loudly if the library is missing
     wl = synth.WORKLOADS[args.workload]
+    if wl.get("stage") == "modes":
+        return run_modes(args, rank, world, local, dev)
     if wl["blocks"] > 1:
         return run_stack(args, rank, world, local, dev)
     spec = wl["spec"]
@@ -546,6 +548,95 @@ def run_stack(args, rank, world, local, dev):
     if rank == 0:
         print(json.dumps(line), flush=True)
     blocks.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_modes(args, rank, world, local, dev):
+    """The per-mode blocks: a step is one flux3_mode_blocks_forward call (each
+    mode's tokens through that mode's own `blocks` blocks, attending only among
+    themselves).  FLOPs are the per-mode blocks' algorithmic FLOPs, i.e. the
+    block formula at each mode's own token count."""
+    import torch
+    import torch.distributed as dist
+
+    import diffusion_transformer_block_fwd_b300 as F3
+    from diffusion_transformer_block_fwd_b300.model import mode_blocks_forward
+    import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    lay = synth.build_layout(wl["spec"])
+    T, nb = lay.T, wl["blocks"]
+    counts = [int((lay.stream_id == m).sum()) for m in range(3)]
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+    mb = []
+    for m in range(3):
+        ws = [synth.block_weights(1 + m, b, device=dev) for b in range(nb)]
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            mb.append(F3.Flux3Blocks(ws, max_tokens=max(1, counts[m]), stream=stream) if counts[m] else None)
+        del ws
+    torch.cuda.synchronize(dev)
+    x0 = synth.activations(1, T, device=dev)
+    x = x0.clone()
+    mods = synth.modulation(1, device=dev)
+    pos = torch.from_numpy(lay.pos).to(dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        mode_blocks_forward(mb, x, lay.segments, pos, mods, stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+
+    launches = sum(2 + nb * 4 for c in counts if c)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            x.copy_(x0)
+            step()
+        st = F3.flux3_check_error(sp)
+        assert st == 0, F3.status_string(st)
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(local)
+        sampler.start()
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            x.copy_(x0)
+            flush.zero_()
+            step(events[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+        clocks = sampler.stop()
+    st = F3.flux3_check_error(sp)
+    assert st == 0, F3.status_string(st)
+    value, step_ms = replica_throughput(T, statistics.mean(e[0].elapsed_time(e[1]) for e in events), world, dev)
+    flops = nb * sum(block_flops(c) for c in counts if c)
+    hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
+    tflops = world * flops / (step_ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s (per-mode blocks)",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (random-init N(0,0.02) weights, one set per mode)",
+            "config": {"workload": args.workload, "T": T, "tokens_per_mode": counts, "blocks_per_mode": nb,
+                       "segments": lay.segments, "l2": "flushed between timed steps",
+                       "launch": "stream launches through flux3_mode_blocks_forward"},
+            "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
+            "frac_of_bf16_sustained": (tflops / world / bf16_sust) if bf16_sust else None,
+            "roofline": {"kernel": "per-mode blocks", "bound": "tensor", "achieved": tflops / world,
+                         "peak": bf16_burst, "unit": "TFLOP/s", "frac": tflops / world / bf16_burst,
+                         "traffic": None, "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)"},
+            "gpu_launches": launches * args.steps, "clocks": clocks, "wall_s_timed_region": t_wall}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for b in mb:
+        if b is not None:
+            b.close()
     if world > 1:
         dist.destroy_process_group()
 

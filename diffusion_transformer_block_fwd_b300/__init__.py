@@ -36,7 +36,7 @@ EXPORTED = (
     "flux3_block_forward", "flux3_stack_forward", "flux3_check_error", "flux3_status_string", "flux3_destroy",
     "flux3_stream_ids", "flux3_rope_tables", "flux3_ln_modulate", "flux3_in_projection", "flux3_attention",
     "flux3_out_projection", "flux3_gemm_bf16", "flux3_selftest_wait_timeout", "flux3_block_forward_noalloc",
-    "flux3_block_init_nvfp4", "flux3_quantize_nvfp4", "flux3_dequantize_block",
+    "flux3_block_init_nvfp4", "flux3_quantize_nvfp4", "flux3_dequantize_block", "flux3_mode_blocks_forward",
 )
 
 
@@ -111,6 +111,7 @@ def lib():
                                            vp, sz, vp]),
             "flux3_quantize_nvfp4": (i, [vp, i, i, vp, vp, vp, vp]),
             "flux3_dequantize_block": (i, [vp, i, vp, vp, vp]),
+            "flux3_mode_blocks_forward": (i, [ctypes.POINTER(vp), i, vp, i, segp, i, vp, vp, vp, sz, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -195,6 +196,16 @@ def flux3_block_forward(h, block_idx, x, T, segments, pos_ids, mod, workspace, w
     segs = segments_array(segments)
     _check(lib().flux3_block_forward(h, block_idx, x, T, segs, len(segments), pos_ids, mod, workspace, ws_bytes,
                                      stream), "flux3_block_forward")
+
+
+def flux3_mode_blocks_forward(mode_handles, n_blocks, x, T, segments, pos_ids, early_mod, workspace, ws_bytes,
+                              stream=0):
+    """mode_handles: three handles (ints, or None for a mode without tokens),
+    indexed by stream id."""
+    hs = (ctypes.c_void_p * 3)(*[(int(h) if h else None) for h in mode_handles])
+    segs = segments_array(segments)
+    _check(lib().flux3_mode_blocks_forward(hs, n_blocks, x, T, segs, len(segments), pos_ids, early_mod, workspace,
+                                           ws_bytes, stream), "flux3_mode_blocks_forward")
 
 
 def flux3_stack_forward(h, first_block, n_blocks, x, T, segments, pos_ids, mod, workspace, ws_bytes, stream=0):

@@ -501,6 +501,36 @@ flux3_status flux3_stack_forward(const flux3_handle *h, int first_block, int n_b
                         static_cast<cudaStream_t>(stream));
 }
 
+flux3_status flux3_mode_blocks_forward(const flux3_handle *const *mode_handles, int n_blocks, float *x, int T,
+                                       const flux3_segment *segs, int n_segs, const float *pos_ids,
+                                       const float *early_mod, void *workspace, size_t ws_bytes, void *stream) {
+  if (!mode_handles || !x || !pos_ids || !early_mod || n_blocks < 1) return FLUX3_ERR_INVALID_ARG;
+  F3_TRY(segments_ok(segs, n_segs, T));
+  // each present mode must be one run of rows [row0, row0 + Tm)
+  int first[3] = {-1, -1, -1}, last[3] = {-1, -1, -1};
+  for (int i = 0; i < n_segs; ++i) {
+    const int m = segs[i].stream;
+    if (first[m] < 0) first[m] = i;
+    last[m] = i;
+  }
+  for (int m = 0; m < 3; ++m) {
+    if (first[m] < 0) continue;
+    for (int i = first[m]; i <= last[m]; ++i)
+      if (segs[i].stream != m) return FLUX3_ERR_INVALID_ARG;
+    if (!mode_handles[m] || n_blocks > mode_handles[m]->n_blocks) return FLUX3_ERR_INVALID_ARG;
+  }
+  for (int m = 0; m < 3; ++m) {
+    if (first[m] < 0) continue;
+    const int row0 = segs[first[m]].start;
+    const int tm = segs[last[m]].start + segs[last[m]].len - row0;
+    const flux3_segment one{0, tm, m};
+    F3_TRY(forward_common(mode_handles[m], 0, n_blocks, x + (size_t)row0 * kHidden, tm, &one, 1,
+                          pos_ids + (size_t)row0 * 4, early_mod, workspace, ws_bytes,
+                          static_cast<cudaStream_t>(stream)));
+  }
+  return FLUX3_OK;
+}
+
 flux3_status flux3_check_error(void *stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return FLUX3_ERR_CUDA;

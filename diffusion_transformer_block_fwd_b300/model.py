@@ -1,12 +1,13 @@
 """Flux3Blocks: a handle plus the torch-allocated device buffers it needs
 (packed weights, workspace).  Argument marshalling only; the forward pass is
-flux3_stack_forward / flux3_block_forward of the C library."""
+flux3_stack_forward / flux3_block_forward / flux3_mode_blocks_forward of the C
+library."""
 
 import torch
 
 from . import (FLUX3_W_BF16, FLUX3_W_NVFP4, NVFP4_MATRICES, flux3_block_forward, flux3_block_init,
-               flux3_block_init_nvfp4, flux3_default_config, flux3_destroy, flux3_packed_weight_bytes,
-               flux3_quantize_nvfp4, flux3_stack_forward, flux3_workspace_bytes)
+               flux3_block_init_nvfp4, flux3_default_config, flux3_destroy, flux3_mode_blocks_forward,
+               flux3_packed_weight_bytes, flux3_quantize_nvfp4, flux3_stack_forward, flux3_workspace_bytes)
 
 WEIGHT_KEYS = ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out", "query_norm", "key_norm")
 
@@ -114,3 +115,27 @@ class Flux3Blocks:
             self.close()
         except Exception:
             pass
+
+
+def mode_blocks_forward(mode_blocks, x, segments, pos_ids, early_mod, n_blocks=None, stream=None):
+    """The per-mode blocks through flux3_mode_blocks_forward, in place on x.
+
+    mode_blocks: three Flux3Blocks (or None for a mode without tokens), indexed
+    by stream id (image, image_cond, txt), each holding that mode's blocks.
+    x: float32 [T, 3072]; pos_ids: float32 [T, 4]; early_mod: float32 [3, 9216];
+    the segments of one stream must be adjacent."""
+    used = [b for b in mode_blocks if b is not None]
+    assert used, "no mode blocks"
+    dev = used[0].device
+    for t in (x, pos_ids, early_mod):
+        assert t.dtype == torch.float32 and t.is_contiguous() and t.device == dev
+    n = min(b.n_blocks for b in used) if n_blocks is None else n_blocks
+    counts = [0, 0, 0]
+    for _, ln, st in segments:
+        counts[st] += ln
+    big = max(range(3), key=lambda m: counts[m])   # the workspace is sized for the largest mode
+    ws = mode_blocks[big].workspace(counts[big])
+    flux3_mode_blocks_forward([b.handle if b is not None else None for b in mode_blocks], n, x.data_ptr(),
+                              x.shape[0], segments, pos_ids.data_ptr(), early_mod.data_ptr(), ws.data_ptr(),
+                              ws.numel(), _stream_ptr(stream))
+    return x

@@ -221,6 +221,33 @@ FLUX3_API flux3_status flux3_stack_forward(const flux3_handle *h, int first_bloc
                                            const float *pos_ids, const float *mod,
                                            void *workspace, size_t ws_bytes, void *stream);
 
+/* The per-mode blocks that precede the joint stack ("FLUX.3 Image Klein
+ * support", comment "Structure (from dit.py)": the first 5 blocks are per
+ * mode, each mode runs through its own weights, attends only to its own
+ * tokens of the same sample, and takes its modulation from the mode's
+ * early_stream_modulations; tensor names content_mode_blocks.{image,
+ * image_cond}.{0..4} and txt_mode_blocks.{0..4}).  Each mode's tokens run
+ * through blocks 0 .. n_blocks-1 of that mode's handle as a sequence of their
+ * own (attention block-diagonal by mode); x is updated in place.
+ *   mode_handles  host array [3] indexed by flux3_stream: the handle holding
+ *                 that mode's blocks; may be NULL for a mode with no tokens
+ *   n_blocks      blocks per mode (5 in the checkpoint); 1 <= n_blocks <= each
+ *                 used handle's block count
+ *   x, T, segs, n_segs, pos_ids: as flux3_block_forward.  The segments of one
+ *                 stream must be adjacent (one run of rows), as in the
+ *                 pipeline's token order; otherwise FLUX3_ERR_INVALID_ARG.
+ *   early_mod     device float32 [3, 9216]: per stream the shift | scale |
+ *                 gate of early_stream_modulations
+ *   workspace     device buffer of at least flux3_workspace_bytes(cfg, Tm)
+ *                 bytes, Tm the largest mode's token count (T always
+ *                 suffices); each used handle's max_tokens >= its mode's count
+ * The modes run one after another on `stream`, each through the same kernels
+ * as flux3_stack_forward on its rows. */
+FLUX3_API flux3_status flux3_mode_blocks_forward(const flux3_handle *const *mode_handles, int n_blocks, float *x,
+                                                 int T, const flux3_segment *segs, int n_segs,
+                                                 const float *pos_ids, const float *early_mod, void *workspace,
+                                                 size_t ws_bytes, void *stream);
+
 /* Largest T flux3_block_forward_noalloc accepts (its scratch is ~25 MB). */
 #define FLUX3_NOALLOC_MAX_TOKENS 512
 

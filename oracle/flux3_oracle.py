@@ -39,7 +39,7 @@ __all__ = [
     "block_weight_shapes", "checkpoint_inventory", "rope_ids_from_table",
     "split_modulation", "layer_norm", "modulate", "rms_norm", "rope_frequencies",
     "rope_angles", "apply_rope", "attention", "silu", "swiglu", "qkv_heads",
-    "single_block", "single_block_parts", "stack_forward",
+    "single_block", "single_block_parts", "stack_forward", "mode_blocks_forward",
 ]
 
 
@@ -286,4 +286,30 @@ def stack_forward(x, blocks, mods, stream_id, pos):
     x = np.asarray(x, np.float64)
     for w in blocks:
         x = single_block(x, w, mods, stream_id, pos)
+    return x
+
+
+def mode_blocks_forward(x, mode_blocks, early_mods, stream_id, pos):
+    """The per-mode blocks that come before the joint ones ("FLUX.3 Image
+    Klein support", comment "Structure (from dit.py)": the first 5 blocks are
+    per mode; each mode runs through its own weights and attends only to its
+    own tokens of the same sample; its modulation is the mode's
+    early_stream_modulations; names content_mode_blocks.{image,image_cond}.*
+    and txt_mode_blocks.* in "Tensor names (distilled checkpoint)").
+
+    mode_blocks: for each stream id (image, image_cond, txt) the list of that
+    mode's block weights, in order.  early_mods: [3, 3D].  The tokens of each
+    mode are taken out of the sequence (keeping their order), run through that
+    mode's blocks as a sequence of their own, and written back in place."""
+    x = np.array(x, dtype=np.float64)
+    stream_id = np.asarray(stream_id)
+    pos = np.asarray(pos, np.float64)
+    for m in range(N_STREAMS):
+        idx = np.nonzero(stream_id == m)[0]
+        if idx.size == 0:
+            continue
+        xm = x[idx]
+        for w in mode_blocks[m]:
+            xm = single_block(xm, w, early_mods, stream_id[idx], pos[idx])
+        x[idx] = xm
     return x

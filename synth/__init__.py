@@ -96,6 +96,12 @@ WORKLOADS = {
     # 28-block stack, 1024x1024 target + one 1024x1024 reference (the one-block layout above)
     "stack28_1024sq_ref1_t8704": dict(spec=[("txt", 512), ("image", (64, 64)), ("image_cond", (64, 64))],
                                       blocks=28, calls=1, wfmt="bf16"),
+    # the per-mode blocks (5 per mode, each mode attending only to itself): a small case
+    # and the 1024x1024 + one 1024x1024 reference layout
+    "modes5_t112": dict(spec=[("txt", 32), ("image", (8, 8)), ("image_cond", (4, 4))],
+                        blocks=5, calls=1, wfmt="bf16", stage="modes"),
+    "modes5_1024sq_ref1_t8704": dict(spec=[("txt", 512), ("image", (64, 64)), ("image_cond", (64, 64))],
+                                     blocks=5, calls=1, wfmt="bf16", stage="modes"),
     # 28-block stack, NVFP4 weights, 1024x1024 + ten 512x512 references
     "stack28_nvfp4_1024sq_10ref512_t14848": dict(
         spec=[("txt", 512), ("image", (64, 64))] + [("image_cond", (32, 32))] * 10,

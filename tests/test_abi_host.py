@@ -160,3 +160,27 @@ def test_nvfp4_sizes_and_validation():
     assert L.flux3_quantize_nvfp4(16, 0, 32, 16, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_quantize_nvfp4(18, 4, 32, 16, 16, 16, None) == F3.FLUX3_ERR_ALIGNMENT
     assert L.flux3_dequantize_block(None, 0, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+
+
+def test_mode_blocks_validation_before_any_launch():
+    L = F3.lib()
+    none3 = (ctypes.c_void_p * 3)(None, None, None)
+    ok_segs, n_ok = _segs([(0, 4, 2), (4, 8, 0), (12, 4, 1)])
+    # no handle array, zero blocks, null buffers
+    assert L.flux3_mode_blocks_forward(None, 5, 16, 16, ok_segs, n_ok, 16, 16, 16, 1 << 20, None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_mode_blocks_forward(none3, 0, 16, 16, ok_segs, n_ok, 16, 16, 16, 1 << 20, None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_mode_blocks_forward(none3, 5, None, 16, ok_segs, n_ok, 16, 16, 16, 1 << 20, None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    # a mode split into two runs of rows (txt | image | txt)
+    split, n_split = _segs([(0, 4, 2), (4, 8, 0), (12, 4, 2)])
+    assert L.flux3_mode_blocks_forward(none3, 5, 16, 16, split, n_split, 16, 16, 16, 1 << 20, None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    # a mode with tokens but no handle
+    assert L.flux3_mode_blocks_forward(none3, 5, 16, 16, ok_segs, n_ok, 16, 16, 16, 1 << 20, None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    # a bad segment table
+    bad, n_bad = _segs([(0, 4, 2), (5, 11, 0)])
+    assert L.flux3_mode_blocks_forward(none3, 5, 16, 16, bad, n_bad, 16, 16, 16, 1 << 20, None) == \
+        F3.FLUX3_ERR_INVALID_ARG

@@ -414,3 +414,93 @@ def test_stack_is_blocks_in_sequence_sharing_modulation():
     for w in ws:
         y = _torch_block(y, w, mods, sid, pos)
     np.testing.assert_allclose(O.stack_forward(x, ws, mods, sid, pos), y, rtol=1e-9, atol=1e-10)
+
+
+# --------------------------------------------------------------------------
+# Per-mode blocks ("FLUX.3 Image Klein support", "Structure (from dit.py)":
+# the first 5 blocks are per mode, own weights, attention only among the
+# mode's own tokens, modulation from early_stream_modulations)
+# --------------------------------------------------------------------------
+def _torch_mode_block(x, w_by_mode, mods, sid, pos):
+    """Independent restatement over the whole sequence at once: each token's
+    projections, norm scales and output projections are those of its mode
+    (computed with all three modes' weights, the token's row selected), and
+    attention is scaled_dot_product_attention with a block-diagonal boolean
+    mask (query and key of the same mode).  fp64 torch."""
+    T, D = x.shape
+    d = len(w_by_mode[0]["query_norm"])
+    H = D // d
+    tx = torch.from_numpy(x)
+    ts = torch.from_numpy(sid).long()
+    tm = torch.from_numpy(mods)[ts]
+    shift, scale, gate = tm[:, :D], tm[:, D:2 * D], tm[:, 2 * D:]
+    h = (1 + scale) * F.layer_norm(tx, (D,), eps=1e-6) + shift
+    Ws = [{k: torch.from_numpy(np.asarray(v)) for k, v in w.items()} for w in w_by_mode]
+    rows = torch.arange(T)
+
+    def per_mode(fn):
+        return torch.stack([fn(W) for W in Ws])[ts, rows]
+
+    def rms(t, s):
+        return t * torch.rsqrt(t.pow(2).mean(-1, keepdim=True) + 1e-6) * s
+
+    n = d // 4
+    freqs = torch.cat([1e4 ** (-torch.arange(0, n, 2, dtype=torch.float64) / n)] * 4)
+    axis = torch.arange(d // 2) // (n // 2)
+    ang = torch.from_numpy(pos)[:, axis] * freqs
+    rot = torch.polar(torch.ones_like(ang), ang)[:, None, :]
+
+    def rope(t):
+        return torch.view_as_real(torch.view_as_complex(t.reshape(T, H, d // 2, 2).contiguous()) * rot).reshape(T, H, d)
+
+    q = per_mode(lambda W: rope(rms(F.linear(h, W["q_proj"]).view(T, H, d), W["query_norm"])))
+    k = per_mode(lambda W: rope(rms(F.linear(h, W["k_proj"]).view(T, H, d), W["key_norm"])))
+    v = per_mode(lambda W: F.linear(h, W["v_proj"]).view(T, H, d))
+    mask = ts[:, None] == ts[None, :]
+    o = F.scaled_dot_product_attention(q.transpose(0, 1), k.transpose(0, 1), v.transpose(0, 1),
+                                       attn_mask=mask).transpose(0, 1).reshape(T, D)
+
+    def mlp(W):
+        a, b = F.linear(h, W["mlp_in"]).chunk(2, dim=-1)
+        return F.linear(F.silu(a) * b, W["mlp_out"])
+
+    out = per_mode(lambda W: F.linear(o, W["attn_out"])) + per_mode(mlp)
+    return (tx + gate * out).numpy()
+
+
+def test_mode_blocks_match_masked_restatement():
+    """Modes interleaved (each mode in several runs), two blocks per mode with
+    different weights: the oracle's per-mode sub-sequences against one
+    block-diagonal masked pass over the whole sequence per block."""
+    rng = _rng(30)
+    blocks = [[_tiny_block(rng) for _ in range(2)] for _ in range(3)]
+    x, mods, sid, pos = _tiny_inputs(rng, T=14)
+    y = x
+    for b in range(2):
+        y = _torch_mode_block(y, [blocks[m][b] for m in range(3)], mods, sid, pos)
+    np.testing.assert_allclose(O.mode_blocks_forward(x, blocks, mods, sid, pos), y, rtol=1e-9, atol=1e-10)
+
+
+def test_mode_blocks_attend_within_their_mode_only():
+    rng = _rng(31)
+    blocks = [[_tiny_block(rng)] for _ in range(3)]
+    x, mods, sid, pos = _tiny_inputs(rng, T=12)
+    out = O.mode_blocks_forward(x, blocks, mods, sid, pos)
+    x2 = x.copy()
+    x2[sid == 2] += rng.standard_normal(x2[sid == 2].shape)   # change only the txt tokens
+    out2 = O.mode_blocks_forward(x2, blocks, mods, sid, pos)
+    assert np.array_equal(out[sid != 2], out2[sid != 2])
+    assert np.all(np.any(out[sid == 2] != out2[sid == 2], axis=1))
+    # and the joint block mixes them
+    j1 = O.single_block(x, blocks[0][0], mods, sid, pos)
+    j2 = O.single_block(x2, blocks[0][0], mods, sid, pos)
+    assert np.all(np.any(j1[sid == 0] != j2[sid == 0], axis=1))
+
+
+def test_mode_blocks_one_mode_is_that_modes_stack():
+    rng = _rng(32)
+    blocks = [[_tiny_block(rng) for _ in range(2)] for _ in range(3)]
+    x, mods, _, pos = _tiny_inputs(rng, T=9)
+    sid = np.full(9, 1)
+    np.testing.assert_allclose(O.mode_blocks_forward(x, blocks, mods, sid, pos),
+                               O.stack_forward(x, blocks[1], mods, sid, pos), rtol=1e-12, atol=1e-13)
