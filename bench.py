@@ -469,12 +469,14 @@ def run_stack(args, rank, world, local, dev):
 
     wl = synth.WORKLOADS[args.workload]
     lay = synth.build_layout(wl["spec"])
-    T, nb, calls, fp4 = lay.T, wl["blocks"], wl["calls"], wl["wfmt"] == "nvfp4"
+    T, nb, calls = lay.T, wl["blocks"], wl["calls"]
+    fp4, fp8 = wl["wfmt"] == "nvfp4", wl["wfmt"] == "fp8r"
     ws = []
     for b in range(nb):
         w = synth.block_weights(1, b, device=dev)
-        if fp4:
-            q = {k: F3.quantize_nvfp4(w[k]) for k in F3.NVFP4_MATRICES}
+        if fp4 or fp8:
+            quant = F3.quantize_nvfp4 if fp4 else F3.quantize_fp8r
+            q = {k: quant(w[k]) for k in F3.NVFP4_MATRICES}
             q.update({k: w[k] for k in ("query_norm", "key_norm")})
             w = q
         ws.append(w)
@@ -500,7 +502,7 @@ def run_stack(args, rank, world, local, dev):
         if evs is not None:
             evs[1].record(stream)
 
-    per_call_launches = 2 + nb * (4 + (1 if fp4 else 0))
+    per_call_launches = 2 + nb * (4 + (1 if fp4 or fp8 else 0))
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             x.copy_(x0)
@@ -531,8 +533,10 @@ def run_stack(args, rank, world, local, dev):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s (per stack call)",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" + (" (NVFP4 weights dequantised per block)" if fp4 else ""),
-            "data": "synthetic (random-init N(0,0.02) weights" + (", NVFP4-quantised on the device)" if fp4 else ")"),
+            "dtype": "bf16" + (" (NVFP4 weights dequantised per block)" if fp4 else
+                               " (fp8r weights expanded per block)" if fp8 else ""),
+            "data": "synthetic (random-init N(0,0.02) weights" + (", NVFP4-quantised on the device)" if fp4 else
+                                                                    ", fp8r-quantised on the device)" if fp8 else ")"),
             "config": {"workload": args.workload, "T": T, "blocks": nb, "calls_per_step": calls,
                        "segments": lay.segments, "l2": "flushed between timed steps",
                        "launch": "stream launches through flux3_stack_forward"},

@@ -25,6 +25,7 @@ FLUX3_ERR_DEVICE = -7
 
 FLUX3_W_BF16 = 0
 FLUX3_W_NVFP4 = 1
+FLUX3_W_FP8R = 2
 FLUX3_STREAM_IMAGE = 0
 FLUX3_STREAM_IMAGE_COND = 1
 FLUX3_STREAM_TXT = 2
@@ -37,6 +38,7 @@ EXPORTED = (
     "flux3_stream_ids", "flux3_rope_tables", "flux3_ln_modulate", "flux3_in_projection", "flux3_attention",
     "flux3_out_projection", "flux3_gemm_bf16", "flux3_selftest_wait_timeout", "flux3_block_forward_noalloc",
     "flux3_block_init_nvfp4", "flux3_quantize_nvfp4", "flux3_dequantize_block", "flux3_mode_blocks_forward",
+    "flux3_block_init_fp8r", "flux3_quantize_fp8r",
 )
 
 
@@ -68,6 +70,15 @@ NVFP4_MATRICES = ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out")
 class flux3_block_weights_nvfp4(ctypes.Structure):
     _fields_ = [(n, flux3_nvfp4_tensor) for n in NVFP4_MATRICES] + [("query_norm", ctypes.c_void_p),
                                                                     ("key_norm", ctypes.c_void_p)]
+
+
+class flux3_fp8r_tensor(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+class flux3_block_weights_fp8r(ctypes.Structure):
+    _fields_ = [(n, flux3_fp8r_tensor) for n in NVFP4_MATRICES] + [("query_norm", ctypes.c_void_p),
+                                                                   ("key_norm", ctypes.c_void_p)]
 
 
 class flux3_segment(ctypes.Structure):
@@ -112,6 +123,9 @@ def lib():
             "flux3_quantize_nvfp4": (i, [vp, i, i, vp, vp, vp, vp]),
             "flux3_dequantize_block": (i, [vp, i, vp, vp, vp]),
             "flux3_mode_blocks_forward": (i, [ctypes.POINTER(vp), i, vp, i, segp, i, vp, vp, vp, sz, vp]),
+            "flux3_block_init_fp8r": (i, [ctypes.POINTER(vp), cfgp, ctypes.POINTER(flux3_block_weights_fp8r), i,
+                                          vp, sz, vp]),
+            "flux3_quantize_fp8r": (i, [vp, i, i, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -186,6 +200,27 @@ def flux3_block_init_nvfp4(cfg, weights, packed_ptr, packed_bytes, stream=0):
 
 def flux3_quantize_nvfp4(w, rows, cols, codes, scales, global_scale, stream=0):
     _check(lib().flux3_quantize_nvfp4(w, rows, cols, codes, scales, global_scale, stream), "flux3_quantize_nvfp4")
+
+
+def flux3_block_init_fp8r(cfg, weights, packed_ptr, packed_bytes, stream=0):
+    """weights: list of dicts: for each matrix name a (codes, scales) pair of
+    device pointers, and query_norm / key_norm device pointers."""
+    n = len(weights)
+    arr = (flux3_block_weights_fp8r * n)()
+    for b, w in enumerate(weights):
+        for k in NVFP4_MATRICES:
+            c, sc = w[k]
+            t = getattr(arr[b], k)
+            t.codes, t.scales = int(c), int(sc)
+        arr[b].query_norm, arr[b].key_norm = int(w["query_norm"]), int(w["key_norm"])
+    h = ctypes.c_void_p()
+    _check(lib().flux3_block_init_fp8r(ctypes.byref(h), ctypes.byref(cfg), arr, n, packed_ptr, packed_bytes, stream),
+           "flux3_block_init_fp8r")
+    return h.value
+
+
+def flux3_quantize_fp8r(w, rows, cols, codes, scales, stream=0):
+    _check(lib().flux3_quantize_fp8r(w, rows, cols, codes, scales, stream), "flux3_quantize_fp8r")
 
 
 def flux3_dequantize_block(h, block_idx, w_in, w_out, stream=0):
@@ -263,4 +298,4 @@ def flux3_selftest_wait_timeout(timeout_us, stream=0):
     _check(lib().flux3_selftest_wait_timeout(timeout_us, stream), "flux3_selftest_wait_timeout")
 
 
-from .model import Flux3Blocks, quantize_nvfp4  # noqa: E402,F401  (torch-owned buffers around the handle)
+from .model import Flux3Blocks, quantize_fp8r, quantize_nvfp4  # noqa: E402,F401  (torch-owned buffers around the handle)

@@ -15,6 +15,7 @@
 #include "elementwise.cuh"
 #include "gemm.cuh"
 #include "nvfp4.cuh"
+#include "fp8r.cuh"
 
 struct flux3_handle {
   flux3_config cfg;
@@ -24,6 +25,7 @@ struct flux3_handle {
   const float *norms;          // [n_blocks][2][kHeadDim]
   std::vector<CUtensorMap> tm_in, tm_out;               // bf16 only
   std::vector<flux3::fp4_detail::Fp4BlockView> fp4;    // NVFP4 only
+  std::vector<flux3::fp8r_detail::Fp8rBlockView> fp8;  // fp8r only
 };
 
 namespace flux3 {
@@ -60,7 +62,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool config_ok(const flux3_config *c) {
   return c && c->hidden == kHidden && c->heads == kHeads && c->head_dim == kHeadDim && c->mlp_hidden == kMlp &&
          c->n_blocks >= 1 && c->max_tokens >= 1 && c->max_tokens <= kMaxTokensLimit &&
-         (c->wfmt == FLUX3_W_BF16 || c->wfmt == FLUX3_W_NVFP4) &&
+         (c->wfmt == FLUX3_W_BF16 || c->wfmt == FLUX3_W_NVFP4 || c->wfmt == FLUX3_W_FP8R) &&
          c->rope_theta > 0.f && c->eps_ln > 0.f && c->eps_rms > 0.f;
 }
 
@@ -81,11 +83,23 @@ constexpr size_t kFp4OutScales = (size_t)kHidden * kCatCols / 16;
 constexpr size_t kFp4BlockBytes =
     ws_round(kFp4InCodes) + ws_round(kFp4InScales) + ws_round(kFp4OutCodes) + ws_round(kFp4OutScales) + 256;
 
+// fp8r packed block: in-projection codes and row scales, out-projection codes
+// and its two scales per row (attn_out's, mlp_out's).
+constexpr size_t kFp8InCodes = (size_t)kInRows * kHidden;
+constexpr size_t kFp8InScales = (size_t)kInRows * 4;
+constexpr size_t kFp8OutCodes = (size_t)kHidden * kCatCols;
+constexpr size_t kFp8OutScales = (size_t)kHidden * 2 * 4;
+constexpr size_t kFp8BlockBytes =
+    ws_round(kFp8InCodes) + ws_round(kFp8InScales) + ws_round(kFp8OutCodes) + ws_round(kFp8OutScales);
+
+// Weights stored below bf16 are expanded to bf16 in the workspace, one block at a time.
+bool lowp(int wfmt) { return wfmt == FLUX3_W_NVFP4 || wfmt == FLUX3_W_FP8R; }
+
 struct Workspace {
   uint8_t *sid;
   float *cos_tab, *sin_tab;
   __nv_bfloat16 *h, *qkv, *cat;
-  __nv_bfloat16 *w_in, *w_out;   // NVFP4 handles: the running block's weights in bf16
+  __nv_bfloat16 *w_in, *w_out;   // NVFP4 / fp8r handles: the running block's weights in bf16
 };
 
 size_t workspace_layout(int T, uint8_t *base, Workspace *ws, bool fp4_weights = false) {
@@ -173,7 +187,7 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
   if (T < 1 || T > h->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
   F3_TRY(segments_ok(segs, n_segs, T));
   if (!aligned16(x) || !aligned16(pos) || !aligned16(mod) || !aligned16(workspace)) return FLUX3_ERR_ALIGNMENT;
-  const bool fp4 = h->cfg.wfmt == FLUX3_W_NVFP4;
+  const bool fp4 = lowp(h->cfg.wfmt);
   Workspace ws;
   if (ws_bytes < workspace_layout(T, nullptr, nullptr, fp4)) return FLUX3_ERR_WORKSPACE;
   workspace_layout(T, static_cast<uint8_t *>(workspace), &ws, fp4);
@@ -187,7 +201,8 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
               !make_tmap_bf16(&tmWout, ws.w_out, kHidden, kCatCols, kBoxB)))
     return FLUX3_ERR_CUDA;
   for (int b = first; b < first + count; ++b) {
-    if (fp4) F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s));
+    if (h->cfg.wfmt == FLUX3_W_NVFP4) F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s));
+    if (h->cfg.wfmt == FLUX3_W_FP8R) F3_CUDA(launch_dequantize_fp8r_block(h->fp8[b], ws.w_in, ws.w_out, s));
     F3_CUDA(launch_ln_modulate(x, T, ws.sid, mod, h->cfg.eps_ln, ws.h, s));
     EpiParams ep{};
     ep.qkv = ws.qkv;
@@ -297,13 +312,15 @@ void flux3_default_config(flux3_config *cfg) {
 
 size_t flux3_packed_weight_bytes(const flux3_config *cfg) {
   if (!config_ok(cfg)) return 0;
-  const size_t per_block = cfg->wfmt == FLUX3_W_NVFP4 ? kFp4BlockBytes : align_up(kWInElems * 2) + align_up(kWOutElems * 2);
+  const size_t per_block = cfg->wfmt == FLUX3_W_NVFP4  ? kFp4BlockBytes
+                           : cfg->wfmt == FLUX3_W_FP8R ? kFp8BlockBytes
+                                                        : align_up(kWInElems * 2) + align_up(kWOutElems * 2);
   return (size_t)cfg->n_blocks * (per_block + align_up(2 * kHeadDim * 4));
 }
 
 size_t flux3_workspace_bytes(const flux3_config *cfg, int T) {
   if (!config_ok(cfg) || T < 1 || T > cfg->max_tokens) return 0;
-  return workspace_layout(T, nullptr, nullptr, cfg->wfmt == FLUX3_W_NVFP4);
+  return workspace_layout(T, nullptr, nullptr, lowp(cfg->wfmt));
 }
 
 flux3_status flux3_block_init(flux3_handle **out, const flux3_config *cfg, const flux3_block_weights *w, int n_blocks,
@@ -311,7 +328,7 @@ flux3_status flux3_block_init(flux3_handle **out, const flux3_config *cfg, const
   if (!out) return FLUX3_ERR_INVALID_ARG;
   *out = nullptr;
   if (!cfg || !w || !packed) return FLUX3_ERR_INVALID_ARG;
-  if (cfg->wfmt != FLUX3_W_BF16) return FLUX3_ERR_INVALID_ARG;   // NVFP4: flux3_block_init_nvfp4
+  if (cfg->wfmt != FLUX3_W_BF16) return FLUX3_ERR_INVALID_ARG;   // NVFP4 / fp8r: their own init
   if (!config_ok(cfg)) return FLUX3_ERR_UNSUPPORTED;
   if (n_blocks != cfg->n_blocks) return FLUX3_ERR_INVALID_ARG;
   if (packed_bytes < flux3_packed_weight_bytes(cfg)) return FLUX3_ERR_WORKSPACE;
@@ -481,10 +498,97 @@ flux3_status flux3_quantize_nvfp4(const void *w, int rows, int cols, void *codes
 
 flux3_status flux3_dequantize_block(const flux3_handle *h, int block_idx, void *w_in, void *w_out, void *stream) {
   if (!h || !w_in || !w_out || block_idx < 0 || block_idx >= h->n_blocks) return FLUX3_ERR_INVALID_ARG;
-  if (h->cfg.wfmt != FLUX3_W_NVFP4) return FLUX3_ERR_UNSUPPORTED;
+  if (!lowp(h->cfg.wfmt)) return FLUX3_ERR_UNSUPPORTED;
   if (!aligned16(w_in) || !aligned16(w_out)) return FLUX3_ERR_ALIGNMENT;
-  return cuda_status(launch_dequantize_block(h->fp4[block_idx], static_cast<__nv_bfloat16 *>(w_in),
-                                             static_cast<__nv_bfloat16 *>(w_out), static_cast<cudaStream_t>(stream)));
+  auto *wi = static_cast<__nv_bfloat16 *>(w_in);
+  auto *wo = static_cast<__nv_bfloat16 *>(w_out);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(h->cfg.wfmt == FLUX3_W_NVFP4 ? launch_dequantize_block(h->fp4[block_idx], wi, wo, s)
+                                                   : launch_dequantize_fp8r_block(h->fp8[block_idx], wi, wo, s));
+}
+
+flux3_status flux3_quantize_fp8r(const void *w, int rows, int cols, void *codes, float *scales, void *stream) {
+  if (!w || !codes || !scales || rows < 1 || cols < 16 || cols % 16 != 0) return FLUX3_ERR_INVALID_ARG;
+  if ((size_t)rows * (size_t)cols > (size_t)1 << 34) return FLUX3_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u)) return FLUX3_ERR_ALIGNMENT;
+  return cuda_status(launch_quantize_fp8r(static_cast<const __nv_bfloat16 *>(w), rows, cols,
+                                          static_cast<uint8_t *>(codes), scales, static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_block_init_fp8r(flux3_handle **out, const flux3_config *cfg, const flux3_block_weights_fp8r *w,
+                                   int n_blocks, void *packed, size_t packed_bytes, void *stream) {
+  if (!out) return FLUX3_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !w || !packed) return FLUX3_ERR_INVALID_ARG;
+  if (cfg->wfmt != FLUX3_W_FP8R) return FLUX3_ERR_INVALID_ARG;
+  if (!config_ok(cfg)) return FLUX3_ERR_UNSUPPORTED;
+  if (n_blocks != cfg->n_blocks) return FLUX3_ERR_INVALID_ARG;
+  if (packed_bytes < flux3_packed_weight_bytes(cfg)) return FLUX3_ERR_WORKSPACE;
+  if (!aligned16(packed)) return FLUX3_ERR_ALIGNMENT;
+  for (int b = 0; b < n_blocks; ++b) {
+    const flux3_block_weights_fp8r &bw = w[b];
+    const flux3_fp8r_tensor *ts[6] = {&bw.q_proj, &bw.k_proj, &bw.v_proj, &bw.attn_out, &bw.mlp_in, &bw.mlp_out};
+    for (const flux3_fp8r_tensor *t : ts) {
+      if (!t->codes || !t->scales) return FLUX3_ERR_INVALID_ARG;
+      if (!aligned16(t->codes) || (reinterpret_cast<uintptr_t>(t->scales) & 3u)) return FLUX3_ERR_ALIGNMENT;
+    }
+    if (!bw.query_norm || !bw.key_norm) return FLUX3_ERR_INVALID_ARG;
+    if (!aligned16(bw.query_norm) || !aligned16(bw.key_norm)) return FLUX3_ERR_ALIGNMENT;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  flux3_handle *h = new (std::nothrow) flux3_handle();
+  if (!h) return FLUX3_ERR_CUDA;
+  h->cfg = *cfg;
+  h->n_blocks = n_blocks;
+  h->w_in = h->w_out = nullptr;
+  uint8_t *base = static_cast<uint8_t *>(packed);
+  auto *norms = reinterpret_cast<float *>(base + n_blocks * kFp8BlockBytes);
+  h->norms = norms;
+  h->fp8.resize(n_blocks);
+  cudaError_t e = cudaSuccess;
+  auto copy = [&](void *dst, const void *src, size_t bytes) {
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+  };
+  auto copy2d = [&](void *dst, size_t dpitch, const void *src, size_t spitch, size_t width, size_t height) {
+    if (e == cudaSuccess) e = cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, cudaMemcpyDeviceToDevice, s);
+  };
+  for (int b = 0; b < n_blocks && e == cudaSuccess; ++b) {
+    const flux3_block_weights_fp8r &bw = w[b];
+    uint8_t *blk = base + b * kFp8BlockBytes;
+    uint8_t *in_c = blk;
+    float *in_s = reinterpret_cast<float *>(in_c + ws_round(kFp8InCodes));
+    uint8_t *out_c = reinterpret_cast<uint8_t *>(in_s) + ws_round(kFp8InScales);
+    float *out_s = reinterpret_cast<float *>(out_c + ws_round(kFp8OutCodes));
+    // in-projection rows q | k | v | mlp_in (a and b interleaved in groups of 128), codes and row scales alike
+    const flux3_fp8r_tensor *qkv[3] = {&bw.q_proj, &bw.k_proj, &bw.v_proj};
+    for (int i = 0; i < 3; ++i) {
+      copy(in_c + (size_t)i * kHidden * kHidden, qkv[i]->codes, (size_t)kHidden * kHidden);
+      copy(in_s + (size_t)i * kHidden, qkv[i]->scales, kHidden * 4);
+    }
+    const uint8_t *mc = static_cast<const uint8_t *>(bw.mlp_in.codes);
+    const float *ms = bw.mlp_in.scales;
+    uint8_t *wc = in_c + (size_t)3 * kHidden * kHidden;
+    float *wsc = in_s + 3 * kHidden;
+    copy2d(wc, 256 * (size_t)kHidden, mc, 128 * (size_t)kHidden, 128 * (size_t)kHidden, kMlp / 128);
+    copy2d(wc + 128 * (size_t)kHidden, 256 * (size_t)kHidden, mc + (size_t)kMlp * kHidden, 128 * (size_t)kHidden,
+           128 * (size_t)kHidden, kMlp / 128);
+    copy2d(wsc, 256 * 4, ms, 128 * 4, 128 * 4, kMlp / 128);
+    copy2d(wsc + 128, 256 * 4, ms + kMlp, 128 * 4, 128 * 4, kMlp / 128);
+    // out-projection rows: attn_out's inputs then mlp_out's; scales (attn_out's, mlp_out's) per row
+    copy2d(out_c, kCatCols, bw.attn_out.codes, kHidden, kHidden, kHidden);
+    copy2d(out_c + kHidden, kCatCols, bw.mlp_out.codes, kMlp, kMlp, kHidden);
+    copy2d(out_s, 8, bw.attn_out.scales, 4, 4, kHidden);
+    copy2d(out_s + 1, 8, bw.mlp_out.scales, 4, 4, kHidden);
+    copy(norms + (size_t)b * 2 * kHeadDim, bw.query_norm, kHeadDim * 4);
+    copy(norms + (size_t)b * 2 * kHeadDim + kHeadDim, bw.key_norm, kHeadDim * 4);
+    h->fp8[b] = fp8r_detail::Fp8rBlockView{in_c, in_s, out_c, out_s};
+  }
+  if (e != cudaSuccess) {
+    delete h;
+    return FLUX3_ERR_CUDA;
+  }
+  *out = h;
+  return FLUX3_OK;
 }
 
 flux3_status flux3_block_forward(const flux3_handle *h, int block_idx, float *x, int T, const flux3_segment *segs,

@@ -5,9 +5,10 @@ library."""
 
 import torch
 
-from . import (FLUX3_W_BF16, FLUX3_W_NVFP4, NVFP4_MATRICES, flux3_block_forward, flux3_block_init,
-               flux3_block_init_nvfp4, flux3_default_config, flux3_destroy, flux3_mode_blocks_forward,
-               flux3_packed_weight_bytes, flux3_quantize_nvfp4, flux3_stack_forward, flux3_workspace_bytes)
+from . import (FLUX3_W_BF16, FLUX3_W_FP8R, FLUX3_W_NVFP4, NVFP4_MATRICES, flux3_block_forward, flux3_block_init,
+               flux3_block_init_fp8r, flux3_block_init_nvfp4, flux3_default_config, flux3_destroy,
+               flux3_mode_blocks_forward, flux3_packed_weight_bytes, flux3_quantize_fp8r, flux3_quantize_nvfp4,
+               flux3_stack_forward, flux3_workspace_bytes)
 
 WEIGHT_KEYS = ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out", "query_norm", "key_norm")
 
@@ -31,25 +32,40 @@ def quantize_nvfp4(w, stream=None):
     return codes, scales, g
 
 
+def quantize_fp8r(w, stream=None):
+    """Row-wise FP8 of a bf16 [rows, cols] device matrix through
+    flux3_quantize_fp8r: returns (codes uint8 [rows, cols], scales float32
+    [rows]) device tensors."""
+    assert w.dtype == torch.bfloat16 and w.is_contiguous() and w.dim() == 2
+    rows, cols = w.shape
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=w.device)
+    scales = torch.empty(rows, dtype=torch.float32, device=w.device)
+    flux3_quantize_fp8r(w.data_ptr(), rows, cols, codes.data_ptr(), scales.data_ptr(), _stream_ptr(stream))
+    return codes, scales
+
+
 class Flux3Blocks:
     """Joint single_blocks on one CUDA device.
 
     weights: list (one per block) of dicts of device tensors.  bf16 format:
     bf16 [out, in] matrices q_proj, k_proj, v_proj, attn_out, mlp_in, mlp_out.
     nvfp4 format: each of those is a (codes, scales, global) triple as
-    quantize_nvfp4 returns.  Both: float32 [128] query_norm, key_norm.  The
+    quantize_nvfp4 returns; fp8r format: a (codes, scales) pair as
+    quantize_fp8r returns.  All: float32 [128] query_norm, key_norm.  The
     weights are copied into the packed buffer at construction and not
     referenced afterwards."""
 
     def __init__(self, weights, max_tokens=16384, stream=None, wfmt="bf16"):
         fp4 = wfmt == "nvfp4"
-        dev = (weights[0]["q_proj"][0] if fp4 else weights[0]["q_proj"]).device
+        fp8 = wfmt == "fp8r"
+        lowp = fp4 or fp8
+        dev = (weights[0]["q_proj"][0] if lowp else weights[0]["q_proj"]).device
         self.device = dev
         self.wfmt = wfmt
         self.cfg = flux3_default_config()
         self.cfg.n_blocks = len(weights)
         self.cfg.max_tokens = int(max_tokens)
-        self.cfg.wfmt = FLUX3_W_NVFP4 if fp4 else FLUX3_W_BF16
+        self.cfg.wfmt = FLUX3_W_NVFP4 if fp4 else FLUX3_W_FP8R if fp8 else FLUX3_W_BF16
         nbytes = flux3_packed_weight_bytes(self.cfg)
         if nbytes == 0:
             raise ValueError("unsupported configuration")
@@ -66,12 +82,20 @@ class Flux3Blocks:
                 d = {k: tuple(t.data_ptr() for t in w[k]) for k in NVFP4_MATRICES}
                 d.update({k: w[k].data_ptr() for k in WEIGHT_KEYS[6:]})
                 ptrs.append(d)
+            elif fp8:
+                for k in NVFP4_MATRICES:
+                    c, sc = w[k]
+                    assert c.dtype == torch.uint8 and sc.dtype == torch.float32, k
+                    assert c.is_contiguous() and sc.is_contiguous() and c.device == dev, k
+                d = {k: (w[k][0].data_ptr(), w[k][1].data_ptr()) for k in NVFP4_MATRICES}
+                d.update({k: w[k].data_ptr() for k in WEIGHT_KEYS[6:]})
+                ptrs.append(d)
             else:
                 for k in WEIGHT_KEYS[:6]:
                     assert w[k].dtype == torch.bfloat16 and w[k].is_contiguous() and w[k].device == dev, k
                 ptrs.append({k: w[k].data_ptr() for k in WEIGHT_KEYS})
         sp = _stream_ptr(stream)
-        init = flux3_block_init_nvfp4 if fp4 else flux3_block_init
+        init = flux3_block_init_nvfp4 if fp4 else flux3_block_init_fp8r if fp8 else flux3_block_init
         self.handle = init(self.cfg, ptrs, self.packed.data_ptr(), nbytes, sp)
         (stream or torch.cuda.current_stream()).synchronize()   # source weights may be freed after this
         self._ws = torch.empty(0, dtype=torch.uint8, device=dev)

@@ -55,9 +55,10 @@ typedef enum flux3_status {
 } flux3_status;
 
 /* Weight formats.  NVFP4 = e2m1 values with one e4m3 scale per 16 inputs and a
- * float32 per-tensor scale ("Welcome FLUX.3 Image Klein in Diffusers", section
- * "Single-file format checkpoints", names nvfp4 and fp8r variants). */
-typedef enum flux3_wfmt { FLUX3_W_BF16 = 0, FLUX3_W_NVFP4 = 1 } flux3_wfmt;
+ * float32 per-tensor scale; FP8R = e4m3 values with one float32 scale per row
+ * ("Welcome FLUX.3 Image Klein in Diffusers", section "Single-file format
+ * checkpoints", names the nvfp4 and fp8r variants). */
+typedef enum flux3_wfmt { FLUX3_W_BF16 = 0, FLUX3_W_NVFP4 = 1, FLUX3_W_FP8R = 2 } flux3_wfmt;
 
 /* Token streams ("modes"): each selects its own modulation vector. */
 typedef enum flux3_stream {
@@ -122,6 +123,27 @@ typedef struct flux3_block_weights_nvfp4 {
   const float *key_norm;
 } flux3_block_weights_nvfp4;
 
+/* One weight matrix [rows, cols] in row-wise FP8 ("fp8r"):
+ *   codes   device uint8 [rows, cols]: E4M3 bit patterns (sign 7, exponent
+ *           6..3 with bias 7, mantissa 2..0); 0x7F / 0xFF (NaN) must not occur
+ *   scales  device float32 [rows]: one scale per row (output feature)
+ * weight[r, c] = e4m3(code[r, c]) * scales[r].  The pages name the fp8r
+ * checkpoint variant ("Welcome FLUX.3 Image Klein in Diffusers", section
+ * "Single-file format checkpoints") but not its layout; this is the layout
+ * flux3_quantize_fp8r writes. */
+typedef struct flux3_fp8r_tensor {
+  const void *codes;
+  const float *scales;
+} flux3_fp8r_tensor;
+
+/* One block's weights in fp8r (shapes as flux3_block_weights); the norm scales
+ * stay float32.  codes and norm pointers 16-byte aligned, scales 4-byte. */
+typedef struct flux3_block_weights_fp8r {
+  flux3_fp8r_tensor q_proj, k_proj, v_proj, attn_out, mlp_in, mlp_out;
+  const float *query_norm;
+  const float *key_norm;
+} flux3_block_weights_fp8r;
+
 /* A contiguous run of tokens of one stream.  A forward call's segments must be
  * in increasing order, non-overlapping, non-empty, and cover [0, T) exactly;
  * at most FLUX3_MAX_SEGMENTS of them.  Any stream order is accepted. */
@@ -140,18 +162,19 @@ typedef struct flux3_handle flux3_handle;
  * eps 1e-6). */
 FLUX3_API void flux3_default_config(flux3_config *cfg);
 
-/* Bytes of the caller-owned buffer flux3_block_init (bf16) or
- * flux3_block_init_nvfp4 (cfg->wfmt == FLUX3_W_NVFP4) packs the weights into
- * (per block: the q/k/v/mlp_in rows concatenated, the attn_out/mlp_out
- * columns concatenated, and the two norm scales; NVFP4 keeps codes, block
- * scales and the six global scales, 69.0 MB per block instead of 245.4 MB).
- * 0 if cfg is invalid. */
+/* Bytes of the caller-owned buffer flux3_block_init (bf16),
+ * flux3_block_init_nvfp4 (cfg->wfmt == FLUX3_W_NVFP4) or
+ * flux3_block_init_fp8r (FLUX3_W_FP8R) packs the weights into (per block: the
+ * q/k/v/mlp_in rows concatenated, the attn_out/mlp_out columns concatenated,
+ * and the two norm scales; NVFP4 keeps codes, block scales and the six global
+ * scales, 69.0 MB per block, fp8r codes and row scales, 122.9 MB, instead of
+ * 245.4 MB).  0 if cfg is invalid. */
 FLUX3_API size_t flux3_packed_weight_bytes(const flux3_config *cfg);
 
 /* Bytes of workspace a forward call with T tokens needs (stream ids, RoPE
- * tables, modulated input, q/k/v, attention + SwiGLU output; with NVFP4
- * weights also one block's weights dequantised to bf16, 245.4 MB).  0 if cfg
- * is invalid or T is out of range. */
+ * tables, modulated input, q/k/v, attention + SwiGLU output; with NVFP4 or
+ * fp8r weights also one block's weights expanded to bf16, 245.4 MB).  0 if
+ * cfg is invalid or T is out of range. */
 FLUX3_API size_t flux3_workspace_bytes(const flux3_config *cfg, int T);
 
 /* Creates a handle for n_blocks blocks (n_blocks == cfg->n_blocks).
@@ -190,13 +213,31 @@ FLUX3_API flux3_status flux3_block_init_nvfp4(flux3_handle **out, const flux3_co
 FLUX3_API flux3_status flux3_quantize_nvfp4(const void *w, int rows, int cols, void *codes, void *scales,
                                             float *global_scale, void *stream);
 
-/* The bf16 weights an NVFP4 handle's block_idx runs with, as the forward pass
+/* The bf16 weights an NVFP4 or fp8r handle's block_idx runs with, as the forward pass
  * expands them: w_in device bf16 [27648, 3072] = rows of q | k | v | mlp_in
  * (mlp_in's a and b halves interleaved in groups of 128 rows: a[128m..],
  * b[128m..], ...), w_out device bf16 [3072, 12288] = [attn_out | mlp_out]
  * along the input dimension.  FLUX3_ERR_UNSUPPORTED for a bf16 handle. */
 FLUX3_API flux3_status flux3_dequantize_block(const flux3_handle *h, int block_idx, void *w_in, void *w_out,
                                               void *stream);
+
+/* A handle over fp8r weights (cfg->wfmt = FLUX3_W_FP8R), same conventions as
+ * flux3_block_init_nvfp4: the codes and scales are copied into `packed`
+ * (flux3_packed_weight_bytes(cfg) bytes: 122.9 MB per block), and every
+ * forward call expands the running block's weights to bf16 in the workspace
+ * (e4m3 * scale rounded to float32, then to bf16, both nearest even) before
+ * the bf16 GEMMs. */
+FLUX3_API flux3_status flux3_block_init_fp8r(flux3_handle **out, const flux3_config *cfg,
+                                             const flux3_block_weights_fp8r *w, int n_blocks, void *packed,
+                                             size_t packed_bytes, void *stream);
+
+/* Row-wise FP8 quantisation of a device bf16 [rows, cols] matrix (cols a
+ * multiple of 16, w and codes 16-byte aligned): per row s = amax / 448
+ * rounded to float32 (1 for an all-zero row), codes = E4M3 of w / s, round to
+ * nearest even, saturating at +-448, no negative zero (the decision taken in
+ * float64).  codes: device uint8 [rows, cols]; scales: device float32 [rows]. */
+FLUX3_API flux3_status flux3_quantize_fp8r(const void *w, int rows, int cols, void *codes, float *scales,
+                                           void *stream);
 
 /* One joint block (block_idx of the handle) applied in place.
  *   x        device float32 [T, 3072]: the residual stream, updated in place
@@ -265,7 +306,7 @@ FLUX3_API flux3_status flux3_mode_blocks_forward(const flux3_handle *const *mode
  * every GPU that loads the library holds until the process exits.  It calls no
  * cudaMalloc, cudaFree or other allocating routine.
  *   - T > FLUX3_NOALLOC_MAX_TOKENS returns FLUX3_ERR_WORKSPACE; a handle with
- *     NVFP4 weights returns FLUX3_ERR_UNSUPPORTED (its dequantised weights
+ *     NVFP4 or fp8r weights returns FLUX3_ERR_UNSUPPORTED (its expanded weights
  *     would not fit); other errors as flux3_block_forward.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
@@ -313,8 +354,8 @@ FLUX3_API flux3_status flux3_ln_modulate(const float *x, int T, const uint8_t *s
                                          const float *mod, float eps, void *h, void *stream);
 
 /* Step entry points flux3_in_projection and flux3_out_projection use the
- * handle's packed bf16 weights: with an NVFP4 handle they return
- * FLUX3_ERR_UNSUPPORTED (the forward calls expand NVFP4 weights themselves). */
+ * handle's packed bf16 weights: with an NVFP4 or fp8r handle they return
+ * FLUX3_ERR_UNSUPPORTED (the forward calls expand those weights themselves). */
 
 /* The block's input projections with their fused epilogues (one tensor-core
  * GEMM over the concatenated [Wq; Wk; Wv; Wmlp_in] rows):

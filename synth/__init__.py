@@ -102,6 +102,9 @@ WORKLOADS = {
                         blocks=5, calls=1, wfmt="bf16", stage="modes"),
     "modes5_1024sq_ref1_t8704": dict(spec=[("txt", 512), ("image", (64, 64)), ("image_cond", (64, 64))],
                                      blocks=5, calls=1, wfmt="bf16", stage="modes"),
+    # 28-block stack, row-wise FP8 weights, 1024x1024 + one 1024x1024 reference
+    "stack28_fp8r_1024sq_ref1_t8704": dict(spec=[("txt", 512), ("image", (64, 64)), ("image_cond", (64, 64))],
+                                           blocks=28, calls=1, wfmt="fp8r"),
     # 28-block stack, NVFP4 weights, 1024x1024 + ten 512x512 references
     "stack28_nvfp4_1024sq_10ref512_t14848": dict(
         spec=[("txt", 512), ("image", (64, 64))] + [("image_cond", (32, 32))] * 10,

@@ -184,3 +184,44 @@ def test_mode_blocks_validation_before_any_launch():
     bad, n_bad = _segs([(0, 4, 2), (5, 11, 0)])
     assert L.flux3_mode_blocks_forward(none3, 5, 16, 16, bad, n_bad, 16, 16, 16, 1 << 20, None) == \
         F3.FLUX3_ERR_INVALID_ARG
+
+
+def test_fp8r_sizes_and_validation():
+    L = F3.lib()
+    cfg = F3.flux3_default_config()
+    cfg.wfmt = F3.FLUX3_W_FP8R
+    per_block = 27648 * 3072 + 27648 * 4 + 3072 * 12288 + 3072 * 2 * 4
+    assert per_block == 122_818_560                     # 8 bits per weight + one float per row
+    assert 28 * per_block <= F3.flux3_packed_weight_bytes(cfg) < 28 * (per_block + 8 * 256)
+    bf = F3.flux3_default_config()
+    assert F3.flux3_workspace_bytes(cfg, 4608) - F3.flux3_workspace_bytes(bf, 4608) >= (27648 + 12288) * 3072 * 2
+    cfg.n_blocks = 1
+    h = ctypes.c_void_p()
+    w = (F3.flux3_block_weights_fp8r * 1)()
+    # the other formats' inits refuse an fp8r config and the fp8r init refuses theirs
+    wb = (F3.flux3_block_weights * 1)()
+    for k, _ in F3.flux3_block_weights._fields_:
+        setattr(wb[0], k, 4096)
+    assert L.flux3_block_init(ctypes.byref(h), ctypes.byref(cfg), wb, 1, 256, 1 << 40, None) == F3.FLUX3_ERR_INVALID_ARG
+    w4 = (F3.flux3_block_weights_nvfp4 * 1)()
+    assert L.flux3_block_init_nvfp4(ctypes.byref(h), ctypes.byref(cfg), w4, 1, 256, 1 << 40, None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    bf.n_blocks = 1
+    assert L.flux3_block_init_fp8r(ctypes.byref(h), ctypes.byref(bf), w, 1, 256, 1 << 40, None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_block_init_fp8r(ctypes.byref(h), ctypes.byref(cfg), w, 1, 256, 1 << 40, None) == \
+        F3.FLUX3_ERR_INVALID_ARG                         # null tensors
+    for k in F3.NVFP4_MATRICES:
+        t = getattr(w[0], k)
+        t.codes, t.scales = 4096, 8192
+    w[0].query_norm, w[0].key_norm = 256, 512
+    assert L.flux3_block_init_fp8r(ctypes.byref(h), ctypes.byref(cfg), w, 1, 256, 1024, None) == \
+        F3.FLUX3_ERR_WORKSPACE
+    w[0].mlp_in.scales = 8194
+    assert L.flux3_block_init_fp8r(ctypes.byref(h), ctypes.byref(cfg), w, 1, 256, 1 << 40, None) == \
+        F3.FLUX3_ERR_ALIGNMENT
+    assert h.value is None
+    assert L.flux3_quantize_fp8r(16, 4, 40, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_quantize_fp8r(16, 0, 32, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_quantize_fp8r(18, 4, 32, 16, 16, None) == F3.FLUX3_ERR_ALIGNMENT
+    assert L.flux3_quantize_fp8r(16, 4, 32, 16, 18, None) == F3.FLUX3_ERR_ALIGNMENT
