@@ -63,11 +63,10 @@ def kernel_bytes(T):
 # DRAM traffic per launch from an ncu capture, valid only for the kernel
 # source it was taken on (sha256 of the file); null otherwise.
 TRAFFIC = {
-    # gemm_kernel<EPI_IN_PROJ>, T = 4608: dram__bytes_read.sum 205.66 MB + dram__bytes_write.sum 154.44 MB
-    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "a190b047c0fa204b", "T": 4608,
-                      "bytes_per_launch": 360_104_192},
+    # gemm_kernel<EPI_IN_PROJ>, T = 4608: dram__bytes_read.sum 204.91 MB + dram__bytes_write.sum 154.32 MB
+    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "8cee6e7fb6257e47", "T": 4608,
+                      "bytes_per_launch": 359_235_584},
 }
-
 
 def src_sha(path):
     with open(os.path.join(ROOT, path), "rb") as f:
@@ -276,6 +275,8 @@ def run_ours(args):
     wl = synth.WORKLOADS[args.workload]
     if wl.get("stage") == "modes":
         return run_modes(args, rank, world, local, dev)
+    if wl.get("stage") == "model":
+        return run_model(args, rank, world, local, dev)
     if wl["blocks"] > 1:
         return run_stack(args, rank, world, local, dev)
     spec = wl["spec"]
@@ -641,6 +642,124 @@ def run_modes(args, rank, world, local, dev):
     for b in mb:
         if b is not None:
             b.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def model_call_flops(counts, n_mode_blocks, n_joint):
+    """Algorithmic FLOPs of one transformer call: embedders, the per-mode
+    blocks at each mode's token count, the joint blocks, the output linear
+    (the conditioning linears are ~0.2 GFLOP and not counted)."""
+    T = sum(counts)
+    emb = 2 * 3072 * ((counts[0] + counts[1]) * 128 + counts[2] * 20480)
+    modes = n_mode_blocks * sum(block_flops(c) for c in counts if c)
+    return emb + modes + n_joint * block_flops(T) + 2 * counts[0] * 3072 * 128
+
+
+def run_model(args, rank, world, local, dev):
+    """The flow-map sampler: a step is `calls` sampler steps, each one
+    transformer call (flux3_transformer_forward: conditioning, embedders, the
+    per-mode blocks, the joint blocks, the output layer) and the Euler update
+    of the image latents (flux3_euler_step)."""
+    import torch
+    import torch.distributed as dist
+
+    import diffusion_transformer_block_fwd_b300 as F3
+    import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    lay = synth.build_layout(wl["spec"])
+    T, nb, steps, nm = lay.T, wl["blocks"], wl["calls"], wl["mode_blocks"]
+    counts = [int((lay.stream_id == m).sum()) for m in range(3)]
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        cw = synth.cond_weights(1, device=dev)
+        stream.synchronize()
+        cond = F3.Flux3Conditioning(cw, stream=stream)
+        del cw
+        mb = []
+        for m in range(3):
+            if counts[m] == 0:
+                mb.append(None)
+                continue
+            ws = [synth.block_weights(10 + m, b, device=dev) for b in range(nm)]
+            stream.synchronize()
+            mb.append(F3.Flux3Blocks(ws, max_tokens=counts[m], stream=stream))
+            del ws
+        ws = [synth.block_weights(1, b, device=dev) for b in range(nb)]
+        stream.synchronize()
+        joint = F3.Flux3Blocks(ws, max_tokens=T, stream=stream)
+        del ws
+    torch.cuda.synchronize(dev)
+    model = F3.Flux3Transformer(cond, mb, joint)
+    ins = synth.stream_inputs(1, lay, device=dev)
+    noise = ins[0].float()
+    lat = noise.clone()
+    pos = torch.from_numpy(lay.pos).to(dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        model.sample(lat, ins, lay.segments, pos, steps=steps, stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            lat.copy_(noise)
+            step()
+        st = F3.flux3_check_error(sp)
+        assert st == 0, F3.status_string(st)
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(local)
+        sampler.start()
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            lat.copy_(noise)
+            flush.zero_()
+            step(events[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+        clocks = sampler.stop()
+    st = F3.flux3_check_error(sp)
+    assert st == 0, F3.status_string(st)
+    assert torch.isfinite(lat).all()
+    value, step_ms = replica_throughput(T * steps, statistics.mean(e[0].elapsed_time(e[1]) for e in events), world,
+                                        dev)
+    flops = steps * model_call_flops(counts, nm, nb)
+    hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
+    tflops = world * flops / (step_ms * 1e-3) / 1e12
+    per_call_launches = (15 + sum(1 for c in counts if c) * (2 + 4 * nm) + 2 + 4 * nb + 1
+                         + sum(1 for s_ in lay.segments) + 2 + 1)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s (transformer calls of the sampler)",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (random-init N(0,0.02) weights, N(0,1) latents and text features)",
+            "config": {"workload": args.workload, "T": T, "tokens_per_mode": counts, "sampler_steps": steps,
+                       "mode_blocks": nm, "joint_blocks": nb, "segments": lay.segments,
+                       "l2": "flushed between timed steps",
+                       "launch": "stream launches through flux3_transformer_forward and flux3_euler_step"},
+            "ms_per_image": step_ms, "ms_per_call": step_ms / steps,
+            "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
+            "frac_of_bf16_sustained": (tflops / world / bf16_sust) if bf16_sust else None,
+            "roofline": {"kernel": "whole sampler", "bound": "tensor", "achieved": tflops / world,
+                         "peak": bf16_sust or bf16_burst, "unit": "TFLOP/s",
+                         "frac": tflops / world / (bf16_sust or bf16_burst), "traffic": None,
+                         "peak_source": "measured bf16 sustained (MEASURED_PEAKS.json)"},
+            "gpu_launches": per_call_launches * steps * args.steps, "clocks": clocks, "wall_s_timed_region": t_wall}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for b in mb + [joint]:
+        if b is not None:
+            b.close()
+    cond.close()
     if world > 1:
         dist.destroy_process_group()
 

@@ -39,6 +39,9 @@ EXPORTED = (
     "flux3_out_projection", "flux3_gemm_bf16", "flux3_selftest_wait_timeout", "flux3_block_forward_noalloc",
     "flux3_block_init_nvfp4", "flux3_quantize_nvfp4", "flux3_dequantize_block", "flux3_mode_blocks_forward",
     "flux3_block_init_fp8r", "flux3_quantize_fp8r",
+    "flux3_cond_packed_bytes", "flux3_cond_init", "flux3_cond_destroy", "flux3_cond_workspace_bytes",
+    "flux3_conditioning", "flux3_embed_tokens", "flux3_final_layer_workspace_bytes", "flux3_final_layer",
+    "flux3_transformer_workspace_bytes", "flux3_transformer_forward", "flux3_sigma_schedule", "flux3_euler_step",
 )
 
 
@@ -79,6 +82,18 @@ class flux3_fp8r_tensor(ctypes.Structure):
 class flux3_block_weights_fp8r(ctypes.Structure):
     _fields_ = [(n, flux3_fp8r_tensor) for n in NVFP4_MATRICES] + [("query_norm", ctypes.c_void_p),
                                                                    ("key_norm", ctypes.c_void_p)]
+
+
+COND_KEYS = ("time_in_in", "time_in_out", "ref_time_in_in", "ref_time_in_out", "early_mod", "single_mod",
+             "emb_in_image", "emb_in_image_cond", "txt_in", "final_adaln", "final_linear")
+
+
+class flux3_cond_weights(ctypes.Structure):
+    _fields_ = [("time_in_in", ctypes.c_void_p), ("time_in_out", ctypes.c_void_p),
+                ("ref_time_in_in", ctypes.c_void_p), ("ref_time_in_out", ctypes.c_void_p),
+                ("early_mod", ctypes.c_void_p * 3), ("single_mod", ctypes.c_void_p * 3),
+                ("emb_in_image", ctypes.c_void_p), ("emb_in_image_cond", ctypes.c_void_p),
+                ("txt_in", ctypes.c_void_p), ("final_adaln", ctypes.c_void_p), ("final_linear", ctypes.c_void_p)]
 
 
 class flux3_segment(ctypes.Structure):
@@ -126,6 +141,19 @@ def lib():
             "flux3_block_init_fp8r": (i, [ctypes.POINTER(vp), cfgp, ctypes.POINTER(flux3_block_weights_fp8r), i,
                                           vp, sz, vp]),
             "flux3_quantize_fp8r": (i, [vp, i, i, vp, vp, vp]),
+            "flux3_cond_packed_bytes": (sz, []),
+            "flux3_cond_init": (i, [ctypes.POINTER(vp), ctypes.POINTER(flux3_cond_weights), vp, sz, vp]),
+            "flux3_cond_destroy": (None, [vp]),
+            "flux3_cond_workspace_bytes": (sz, []),
+            "flux3_conditioning": (i, [vp, f, f, vp, vp, vp, vp, sz, vp]),
+            "flux3_embed_tokens": (i, [vp, ctypes.POINTER(vp), i, segp, i, vp, vp]),
+            "flux3_final_layer_workspace_bytes": (sz, [i]),
+            "flux3_final_layer": (i, [vp, vp, i, segp, i, vp, vp, vp, sz, vp]),
+            "flux3_transformer_workspace_bytes": (sz, [cfgp, i]),
+            "flux3_transformer_forward": (i, [vp, ctypes.POINTER(vp), i, vp, ctypes.POINTER(vp), i, segp, i, vp, f, f,
+                                              vp, vp, sz, vp]),
+            "flux3_sigma_schedule": (i, [i, ctypes.c_double, ctypes.POINTER(ctypes.c_float)]),
+            "flux3_euler_step": (i, [vp, vp, sz, f, f, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -223,6 +251,82 @@ def flux3_quantize_fp8r(w, rows, cols, codes, scales, stream=0):
     _check(lib().flux3_quantize_fp8r(w, rows, cols, codes, scales, stream), "flux3_quantize_fp8r")
 
 
+def _ptr3(ptrs):
+    return (ctypes.c_void_p * 3)(*[(int(p) if p else None) for p in ptrs])
+
+
+def flux3_cond_packed_bytes():
+    return int(lib().flux3_cond_packed_bytes())
+
+
+def flux3_cond_init(weights, packed_ptr, packed_bytes, stream=0):
+    """weights: dict of device pointers keyed like flux3_cond_weights
+    (early_mod / single_mod: three pointers each; ref_time_in_*: 0 or None
+    without the flow-map timestep).  Returns the handle (an int)."""
+    w = flux3_cond_weights()
+    for k in COND_KEYS:
+        v = weights.get(k)
+        if k in ("early_mod", "single_mod"):
+            for j in range(3):
+                getattr(w, k)[j] = int(v[j])
+        else:
+            setattr(w, k, int(v) if v else None)
+    h = ctypes.c_void_p()
+    _check(lib().flux3_cond_init(ctypes.byref(h), ctypes.byref(w), packed_ptr, packed_bytes, stream),
+           "flux3_cond_init")
+    return h.value
+
+
+def flux3_cond_destroy(c):
+    lib().flux3_cond_destroy(c)
+
+
+def flux3_cond_workspace_bytes():
+    return int(lib().flux3_cond_workspace_bytes())
+
+
+def flux3_conditioning(c, t, t_next, early_mod, single_mod, final_mod, workspace, ws_bytes, stream=0):
+    _check(lib().flux3_conditioning(c, t, t_next, early_mod, single_mod, final_mod, workspace, ws_bytes, stream),
+           "flux3_conditioning")
+
+
+def flux3_embed_tokens(c, inputs, T, segments, x, stream=0):
+    segs = segments_array(segments)
+    _check(lib().flux3_embed_tokens(c, _ptr3(inputs), T, segs, len(segments), x, stream), "flux3_embed_tokens")
+
+
+def flux3_final_layer_workspace_bytes(T):
+    return int(lib().flux3_final_layer_workspace_bytes(int(T)))
+
+
+def flux3_final_layer(c, x, T, segments, final_mod, velocity, workspace, ws_bytes, stream=0):
+    segs = segments_array(segments)
+    _check(lib().flux3_final_layer(c, x, T, segs, len(segments), final_mod, velocity, workspace, ws_bytes, stream),
+           "flux3_final_layer")
+
+
+def flux3_transformer_workspace_bytes(cfg, T):
+    return int(lib().flux3_transformer_workspace_bytes(ctypes.byref(cfg), int(T)))
+
+
+def flux3_transformer_forward(c, mode_handles, n_mode_blocks, joint, inputs, T, segments, pos_ids, t, t_next,
+                              velocity, workspace, ws_bytes, stream=0):
+    segs = segments_array(segments)
+    _check(lib().flux3_transformer_forward(c, _ptr3(mode_handles), n_mode_blocks, joint, _ptr3(inputs), T, segs,
+                                           len(segments), pos_ids, t, t_next, velocity, workspace, ws_bytes,
+                                           stream), "flux3_transformer_forward")
+
+
+def flux3_sigma_schedule(steps, alpha=6.93):
+    out = (ctypes.c_float * (steps + 1))()
+    _check(lib().flux3_sigma_schedule(steps, alpha, out), "flux3_sigma_schedule")
+    return list(out)
+
+
+def flux3_euler_step(latent, velocity, n, sigma, sigma_next, stream=0):
+    _check(lib().flux3_euler_step(latent, velocity, n, sigma, sigma_next, stream), "flux3_euler_step")
+
+
 def flux3_dequantize_block(h, block_idx, w_in, w_out, stream=0):
     _check(lib().flux3_dequantize_block(h, block_idx, w_in, w_out, stream), "flux3_dequantize_block")
 
@@ -298,4 +402,4 @@ def flux3_selftest_wait_timeout(timeout_us, stream=0):
     _check(lib().flux3_selftest_wait_timeout(timeout_us, stream), "flux3_selftest_wait_timeout")
 
 
-from .model import Flux3Blocks, quantize_fp8r, quantize_nvfp4  # noqa: E402,F401  (torch-owned buffers around the handle)
+from .model import Flux3Blocks, Flux3Conditioning, Flux3Transformer, quantize_fp8r, quantize_nvfp4  # noqa: E402,F401  (torch-owned buffers around the handle)

@@ -16,6 +16,7 @@
 #include "gemm.cuh"
 #include "nvfp4.cuh"
 #include "fp8r.cuh"
+#include "cond.cuh"
 
 struct flux3_handle {
   flux3_config cfg;
@@ -26,6 +27,15 @@ struct flux3_handle {
   std::vector<CUtensorMap> tm_in, tm_out;               // bf16 only
   std::vector<flux3::fp4_detail::Fp4BlockView> fp4;    // NVFP4 only
   std::vector<flux3::fp8r_detail::Fp8rBlockView> fp8;  // fp8r only
+};
+
+// The non-block weights, copied into the caller's packed buffer.
+struct flux3_cond {
+  bool flow;                                            // ref_time_in present
+  const __nv_bfloat16 *time_in_in, *time_in_out, *ref_in, *ref_out;
+  const __nv_bfloat16 *early[3], *single[3], *final_adaln;
+  CUtensorMap tm_emb[3];     // B operands of the embedders, by stream: emb_in.image, emb_in.image_cond, txt_in
+  CUtensorMap tm_final;      // final_linear zero-padded to 256 rows (one N tile)
 };
 
 namespace flux3 {
@@ -743,6 +753,293 @@ flux3_status flux3_block_forward_noalloc(const flux3_handle *h, int block_idx, f
 flux3_status flux3_selftest_wait_timeout(int timeout_us, void *stream) {
   if (timeout_us < 1 || timeout_us > 1000000) return FLUX3_ERR_INVALID_ARG;
   return cuda_status(launch_selftest_wait(1000ull * (unsigned long long)timeout_us, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- conditioning and the transformer call
+namespace {
+
+constexpr int kTimeDim = 256, kLatent = 128, kTxtFeat = 20480, kFinalPad = 256;
+
+// packed cond weights: element counts, in this order
+constexpr size_t kCondElems[] = {
+    (size_t)kHidden * kTimeDim, (size_t)kHidden * kHidden,     // time_in
+    (size_t)kHidden * kTimeDim, (size_t)kHidden * kHidden,     // ref_time_in
+    (size_t)kModLen * kHidden, (size_t)kModLen * kHidden, (size_t)kModLen * kHidden,   // early
+    (size_t)kModLen * kHidden, (size_t)kModLen * kHidden, (size_t)kModLen * kHidden,   // single
+    (size_t)2 * kHidden * kHidden,                             // final adaLN [6144, 3072]
+    (size_t)kHidden * kLatent, (size_t)kHidden * kLatent,      // emb_in image, image_cond
+    (size_t)kHidden * kTxtFeat,                                // txt_in
+    (size_t)kFinalPad * kHidden};                              // final linear, padded
+constexpr int kCondParts = sizeof(kCondElems) / sizeof(kCondElems[0]);
+
+size_t cond_offset(int part) {
+  size_t off = 0;
+  for (int i = 0; i < part; ++i) off += align_up(kCondElems[i] * 2);
+  return off;
+}
+
+// conditioning scratch (floats): temb [3, 256], a [2, 3072], vec [2, 3072], ra [3072], r [3072]
+constexpr size_t kCondScratchFloats = 3 * kTimeDim + 2 * kHidden + 2 * kHidden + kHidden + kHidden;
+
+flux3_status run_conditioning(const flux3_cond *c, float t, float t_next, float *early, float *single, float *fin,
+                              float *scratch, cudaStream_t s) {
+  float *temb = scratch, *a = temb + 3 * kTimeDim, *vec = a + 2 * kHidden, *ra = vec + 2 * kHidden,
+        *r = ra + kHidden;
+  F3_CUDA(launch_timestep_embed((double)t, 0.0, (double)t_next, temb, s));
+  F3_CUDA(launch_rows_linear(c->time_in_in, kHidden, kTimeDim, temb, kTimeDim, 2, a, kHidden, false, false, s));
+  F3_CUDA(launch_rows_linear(c->time_in_out, kHidden, kHidden, a, kHidden, 2, vec, kHidden, true, false, s));
+  if (c->flow) {
+    F3_CUDA(launch_rows_linear(c->ref_in, kHidden, kTimeDim, temb + 2 * kTimeDim, kTimeDim, 1, ra, kHidden, false,
+                               false, s));
+    F3_CUDA(launch_rows_linear(c->ref_out, kHidden, kHidden, ra, kHidden, 1, r, kHidden, true, false, s));
+    F3_CUDA(launch_add_row(vec, kHidden, 2, r, kHidden, s));
+  }
+  for (int st = 0; st < 3; ++st) {
+    const float *v = vec + (st == FLUX3_STREAM_IMAGE ? 0 : kHidden);   // image at t, the others at 0
+    F3_CUDA(launch_rows_linear(c->early[st], kModLen, kHidden, v, kHidden, 1, early + (size_t)st * kModLen, kModLen,
+                               true, false, s));
+    F3_CUDA(launch_rows_linear(c->single[st], kModLen, kHidden, v, kHidden, 1, single + (size_t)st * kModLen,
+                               kModLen, true, false, s));
+  }
+  F3_CUDA(cudaMemsetAsync(fin + 2 * kHidden, 0, kHidden * 4, s));
+  F3_CUDA(launch_rows_linear(c->final_adaln, 2 * kHidden, kHidden, vec, kHidden, 1, fin, 2 * kHidden, true, false,
+                             s));
+  return FLUX3_OK;
+}
+
+flux3_status inputs_ok(const void *const *inputs, const flux3_segment *segs, int n_segs) {
+  if (!inputs) return FLUX3_ERR_INVALID_ARG;
+  for (int i = 0; i < n_segs; ++i) {
+    const void *p = inputs[segs[i].stream];
+    if (!p) return FLUX3_ERR_INVALID_ARG;
+    if (!aligned16(p)) return FLUX3_ERR_ALIGNMENT;
+  }
+  return FLUX3_OK;
+}
+
+flux3_status run_embed(const flux3_cond *c, const void *const *inputs, const flux3_segment *segs, int n_segs,
+                       float *x, cudaStream_t s) {
+  int row_of[3] = {0, 0, 0};   // next input row of each stream
+  for (int i = 0; i < n_segs; ++i) {
+    const int st = segs[i].stream, len = segs[i].len;
+    const int K = st == FLUX3_STREAM_TXT ? kTxtFeat : kLatent;
+    const __nv_bfloat16 *in = static_cast<const __nv_bfloat16 *>(inputs[st]) + (size_t)row_of[st] * K;
+    row_of[st] += len;
+    CUtensorMap tmA;
+    if (!make_tmap_bf16(&tmA, in, (uint64_t)len, (uint64_t)K, kBM)) return FLUX3_ERR_CUDA;
+    EpiParams ep{};
+    ep.x = x + (size_t)segs[i].start * kHidden;
+    ep.ldc = kHidden;
+    F3_CUDA(launch_gemm(EPI_STORE_F32, tmA, c->tm_emb[st], len, kHidden, K, ep, s));
+  }
+  return FLUX3_OK;
+}
+
+size_t final_ws_bytes(int T) { return align_up((size_t)T) + align_up((size_t)T * kHidden * 2); }
+
+flux3_status run_final(const flux3_cond *c, const float *x, const flux3_segment *segs, int n_segs, int T,
+                       const float *fin, float *vel, uint8_t *ws, cudaStream_t s) {
+  uint8_t *sid0 = ws;                                               // stream id 0 for every row: final_mod's row
+  auto *h = reinterpret_cast<__nv_bfloat16 *>(ws + align_up((size_t)T));
+  F3_CUDA(cudaMemsetAsync(sid0, 0, (size_t)T, s));
+  int n_img = 0;
+  for (int i = 0; i < n_segs; ++i) {
+    if (segs[i].stream != FLUX3_STREAM_IMAGE) continue;
+    F3_CUDA(launch_ln_modulate(x + (size_t)segs[i].start * kHidden, segs[i].len, sid0, fin, 1e-6f,
+                               h + (size_t)n_img * kHidden, s));
+    n_img += segs[i].len;
+  }
+  if (n_img == 0) return FLUX3_OK;
+  CUtensorMap tmA;
+  if (!make_tmap_bf16(&tmA, h, (uint64_t)n_img, kHidden, kBM)) return FLUX3_ERR_CUDA;
+  EpiParams ep{};
+  ep.x = vel;
+  ep.ldc = kLatent;
+  F3_CUDA(launch_gemm(EPI_STORE_F32, tmA, c->tm_final, n_img, kFinalPad, kHidden, ep, s));
+  return FLUX3_OK;
+}
+
+// transformer workspace: x, early, single, final mods, cond scratch, final-layer scratch, block workspace
+struct ModelWs {
+  float *x, *early, *single, *fin, *scratch;
+  uint8_t *final_ws, *block_ws;
+  size_t block_bytes;
+};
+size_t model_ws_layout(const flux3_config *cfg, int T, uint8_t *base, ModelWs *w) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes);
+    return base ? base + o : nullptr;
+  };
+  uint8_t *x = take((size_t)T * kHidden * 4);
+  uint8_t *e = take((size_t)3 * kModLen * 4);
+  uint8_t *sg = take((size_t)3 * kModLen * 4);
+  uint8_t *f = take((size_t)kModLen * 4);
+  uint8_t *sc = take(kCondScratchFloats * 4);
+  uint8_t *fw = take(final_ws_bytes(T));
+  const size_t bb = workspace_layout(T, nullptr, nullptr, lowp(cfg->wfmt));
+  uint8_t *bw = take(bb);
+  if (w) {
+    w->x = reinterpret_cast<float *>(x);
+    w->early = reinterpret_cast<float *>(e);
+    w->single = reinterpret_cast<float *>(sg);
+    w->fin = reinterpret_cast<float *>(f);
+    w->scratch = reinterpret_cast<float *>(sc);
+    w->final_ws = fw;
+    w->block_ws = bw;
+    w->block_bytes = bb;
+  }
+  return off;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t flux3_cond_packed_bytes(void) { return cond_offset(kCondParts); }
+
+flux3_status flux3_cond_init(flux3_cond **out, const flux3_cond_weights *w, void *packed, size_t packed_bytes,
+                             void *stream) {
+  if (!out) return FLUX3_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!w || !packed) return FLUX3_ERR_INVALID_ARG;
+  if (packed_bytes < flux3_cond_packed_bytes()) return FLUX3_ERR_WORKSPACE;
+  if (!aligned16(packed)) return FLUX3_ERR_ALIGNMENT;
+  const bool flow = w->ref_time_in_in != nullptr;
+  if (flow != (w->ref_time_in_out != nullptr)) return FLUX3_ERR_INVALID_ARG;
+  const void *src[kCondParts] = {w->time_in_in, w->time_in_out, w->ref_time_in_in, w->ref_time_in_out,
+                                 w->early_mod[0], w->early_mod[1], w->early_mod[2], w->single_mod[0],
+                                 w->single_mod[1], w->single_mod[2], w->final_adaln, w->emb_in_image,
+                                 w->emb_in_image_cond, w->txt_in, w->final_linear};
+  for (int i = 0; i < kCondParts; ++i) {
+    if (!src[i] && !(i == 2 || i == 3)) return FLUX3_ERR_INVALID_ARG;
+    if (src[i] && !aligned16(src[i])) return FLUX3_ERR_ALIGNMENT;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  flux3_cond *c = new (std::nothrow) flux3_cond();
+  if (!c) return FLUX3_ERR_CUDA;
+  uint8_t *base = static_cast<uint8_t *>(packed);
+  auto part = [&](int i) { return reinterpret_cast<__nv_bfloat16 *>(base + cond_offset(i)); };
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < kCondParts && e == cudaSuccess; ++i) {
+    if (!src[i]) continue;
+    const size_t bytes = (i == kCondParts - 1 ? (size_t)kLatent * kHidden : kCondElems[i]) * 2;
+    e = cudaMemcpyAsync(part(i), src[i], bytes, cudaMemcpyDeviceToDevice, s);
+  }
+  // rows 128..255 of the padded output linear are zero (their outputs are not stored either)
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(part(kCondParts - 1) + (size_t)kLatent * kHidden, 0, (size_t)kLatent * kHidden * 2, s);
+  if (e != cudaSuccess) {
+    delete c;
+    return FLUX3_ERR_CUDA;
+  }
+  c->flow = flow;
+  c->time_in_in = part(0);
+  c->time_in_out = part(1);
+  c->ref_in = part(2);
+  c->ref_out = part(3);
+  for (int st = 0; st < 3; ++st) {
+    c->early[st] = part(4 + st);
+    c->single[st] = part(7 + st);
+  }
+  c->final_adaln = part(10);
+  if (!make_tmap_bf16(&c->tm_emb[FLUX3_STREAM_IMAGE], part(11), kHidden, kLatent, kBoxB) ||
+      !make_tmap_bf16(&c->tm_emb[FLUX3_STREAM_IMAGE_COND], part(12), kHidden, kLatent, kBoxB) ||
+      !make_tmap_bf16(&c->tm_emb[FLUX3_STREAM_TXT], part(13), kHidden, kTxtFeat, kBoxB) ||
+      !make_tmap_bf16(&c->tm_final, part(14), kFinalPad, kHidden, kBoxB)) {
+    delete c;
+    return FLUX3_ERR_CUDA;
+  }
+  *out = c;
+  return FLUX3_OK;
+}
+
+void flux3_cond_destroy(flux3_cond *c) { delete c; }
+
+size_t flux3_cond_workspace_bytes(void) { return align_up(kCondScratchFloats * 4); }
+
+flux3_status flux3_conditioning(const flux3_cond *c, float t, float t_next, float *early_mod, float *single_mod,
+                                float *final_mod, void *workspace, size_t ws_bytes, void *stream) {
+  if (!c || !early_mod || !single_mod || !final_mod || !workspace) return FLUX3_ERR_INVALID_ARG;
+  if (!(t >= 0.f && t <= 1.f) || (c->flow && !(t_next >= 0.f && t_next <= 1.f))) return FLUX3_ERR_INVALID_ARG;
+  if (ws_bytes < flux3_cond_workspace_bytes()) return FLUX3_ERR_WORKSPACE;
+  if (!aligned16(early_mod) || !aligned16(single_mod) || !aligned16(final_mod) || !aligned16(workspace))
+    return FLUX3_ERR_ALIGNMENT;
+  return run_conditioning(c, t, c->flow ? t_next : 0.f, early_mod, single_mod, final_mod,
+                          static_cast<float *>(workspace), static_cast<cudaStream_t>(stream));
+}
+
+flux3_status flux3_embed_tokens(const flux3_cond *c, const void *const *inputs, int T, const flux3_segment *segs,
+                                int n_segs, float *x, void *stream) {
+  if (!c || !x) return FLUX3_ERR_INVALID_ARG;
+  F3_TRY(segments_ok(segs, n_segs, T));
+  F3_TRY(inputs_ok(inputs, segs, n_segs));
+  if (!aligned16(x)) return FLUX3_ERR_ALIGNMENT;
+  return run_embed(c, inputs, segs, n_segs, x, static_cast<cudaStream_t>(stream));
+}
+
+size_t flux3_final_layer_workspace_bytes(int T) { return T < 1 ? 0 : final_ws_bytes(T); }
+
+flux3_status flux3_final_layer(const flux3_cond *c, const float *x, int T, const flux3_segment *segs, int n_segs,
+                               const float *final_mod, float *velocity, void *workspace, size_t ws_bytes,
+                               void *stream) {
+  if (!c || !x || !final_mod || !velocity || !workspace) return FLUX3_ERR_INVALID_ARG;
+  F3_TRY(segments_ok(segs, n_segs, T));
+  if (ws_bytes < final_ws_bytes(T)) return FLUX3_ERR_WORKSPACE;
+  if (!aligned16(x) || !aligned16(final_mod) || !aligned16(velocity) || !aligned16(workspace))
+    return FLUX3_ERR_ALIGNMENT;
+  return run_final(c, x, segs, n_segs, T, final_mod, velocity, static_cast<uint8_t *>(workspace),
+                   static_cast<cudaStream_t>(stream));
+}
+
+size_t flux3_transformer_workspace_bytes(const flux3_config *joint_cfg, int T) {
+  if (!config_ok(joint_cfg) || T < 1 || T > joint_cfg->max_tokens) return 0;
+  return model_ws_layout(joint_cfg, T, nullptr, nullptr);
+}
+
+flux3_status flux3_transformer_forward(const flux3_cond *c, const flux3_handle *const *mode_handles,
+                                       int n_mode_blocks, const flux3_handle *joint, const void *const *inputs,
+                                       int T, const flux3_segment *segs, int n_segs, const float *pos_ids, float t,
+                                       float t_next, float *velocity, void *workspace, size_t ws_bytes,
+                                       void *stream) {
+  if (!c || !joint || !pos_ids || !velocity || !workspace || n_mode_blocks < 0) return FLUX3_ERR_INVALID_ARG;
+  if (n_mode_blocks > 0 && !mode_handles) return FLUX3_ERR_INVALID_ARG;
+  if (T < 1 || T > joint->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
+  F3_TRY(segments_ok(segs, n_segs, T));
+  F3_TRY(inputs_ok(inputs, segs, n_segs));
+  if (!(t >= 0.f && t <= 1.f) || (c->flow && !(t_next >= 0.f && t_next <= 1.f))) return FLUX3_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || !aligned16(velocity) || !aligned16(pos_ids)) return FLUX3_ERR_ALIGNMENT;
+  if (ws_bytes < model_ws_layout(&joint->cfg, T, nullptr, nullptr)) return FLUX3_ERR_WORKSPACE;
+  ModelWs w;
+  model_ws_layout(&joint->cfg, T, static_cast<uint8_t *>(workspace), &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  F3_TRY(run_conditioning(c, t, c->flow ? t_next : 0.f, w.early, w.single, w.fin, w.scratch, s));
+  F3_TRY(run_embed(c, inputs, segs, n_segs, w.x, s));
+  if (n_mode_blocks > 0)
+    F3_TRY(flux3_mode_blocks_forward(mode_handles, n_mode_blocks, w.x, T, segs, n_segs, pos_ids, w.early,
+                                     w.block_ws, w.block_bytes, stream));
+  F3_TRY(forward_common(joint, 0, joint->n_blocks, w.x, T, segs, n_segs, pos_ids, w.single, w.block_ws,
+                        w.block_bytes, s));
+  return run_final(c, w.x, segs, n_segs, T, w.fin, velocity, w.final_ws, s);
+}
+
+flux3_status flux3_sigma_schedule(int steps, double alpha, float *sigmas) {
+  if (steps < 1 || !(alpha > 0.0) || !sigmas) return FLUX3_ERR_INVALID_ARG;
+  for (int k = 0; k <= steps; ++k) {
+    const double t = 1.0 - (double)k / (double)steps;
+    sigmas[k] = (float)(alpha * t / (1.0 + (alpha - 1.0) * t));
+  }
+  return FLUX3_OK;
+}
+
+flux3_status flux3_euler_step(float *latent, const float *velocity, size_t n, float sigma, float sigma_next,
+                              void *stream) {
+  if (!latent || !velocity || n == 0) return FLUX3_ERR_INVALID_ARG;
+  const float dt = (float)((double)sigma_next - (double)sigma);
+  return cuda_status(launch_euler(latent, velocity, n, dt, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -28,10 +28,11 @@ constexpr int kBN = 256;      // output columns of a tile
 constexpr int kBoxB = 128;    // rows of one B box (one CTA's share of the tile's 256 B rows)
 constexpr int kBK = 64;
 
-enum EpiMode : int { EPI_STORE = 0, EPI_IN_PROJ = 1, EPI_OUT_RESIDUAL = 2 };
+enum EpiMode : int { EPI_STORE = 0, EPI_IN_PROJ = 1, EPI_OUT_RESIDUAL = 2, EPI_STORE_F32 = 3 };
 
 struct EpiParams {
-  // EPI_STORE
+  // EPI_STORE (bf16 C) and EPI_STORE_F32 (float32 C in x, ldc columns; tile
+  // columns at or past ldc are not stored)
   __nv_bfloat16 *C;
   int ldc;
   // EPI_IN_PROJ
@@ -41,7 +42,7 @@ struct EpiParams {
   const float *qnorm, *knorm;      // [128]
   float eps_rms;
   // EPI_OUT_RESIDUAL
-  float *x;             // [M, 3072]
+  float *x;             // [M, 3072] (EPI_STORE_F32: the float32 output [M, ldc])
   const uint8_t *sid;   // [M]
   const float *mod;     // [3, 9216]
 };

@@ -6,6 +6,8 @@
 //                     per-head RMSNorm + 4-axis RoPE of q and k, plain v, and
 //                     silu(a) * b of the MLP half
 //   EPI_OUT_RESIDUAL  x += gate[stream] * C  (fp32 residual, in place)
+//   EPI_STORE_F32     float32 store of C's first ldc columns (the embedders
+//                     and the image output layer)
 //
 // CTA pairs (clusters of 2 on one TPC) share each 256 x 256 output tile:
 // the even CTA of the pair (the leader) issues tcgen05.mma.cta_group::2 with
@@ -144,6 +146,20 @@ __device__ __forceinline__ bool epilogue_half(uint32_t taddr, int row, int row0,
         put_chunk_bf16(bw, 4 * c2, r);
       }
       bw.store(tm0, n0 + 64 * b, row0);
+    }
+  } else if constexpr (EPI == EPI_STORE_F32) {
+    // four 32-row x 32-column float32 boxes; columns past ldc (rows of a
+    // weight padded to the 256-column tile) are not stored
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      if (n0 + 32 * c >= ep.ldc) break;
+      bw.begin();
+      tmem_ld32(th + c * 32, r);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4 *>(bw.buf + bw.lane * 128 + ((q ^ (bw.lane & 7)) * 16)) =
+            make_float4(f32(r[4 * q]), f32(r[4 * q + 1]), f32(r[4 * q + 2]), f32(r[4 * q + 3]));
+      bw.store(tm0, n0 + 32 * c, row0);
     }
   } else if constexpr (EPI == EPI_OUT_RESIDUAL) {
     // x[row, n0 .. n0+127] += gate[stream(row)] * acc, as four 32-column boxes;
@@ -465,6 +481,8 @@ cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, i
                              !make_tmap_bf16(&tmO1, ep.cat, (uint64_t)M, kCatCols, 32)))
     return cudaErrorInvalidValue;
   if (EPI == EPI_OUT_RESIDUAL && !make_tmap_f32_box32(&tmO0, ep.x, (uint64_t)M, kHidden)) return cudaErrorInvalidValue;
+  if (EPI == EPI_STORE_F32 && !make_tmap_f32_box32(&tmO0, ep.x, (uint64_t)M, (uint64_t)ep.ldc))
+    return cudaErrorInvalidValue;
   const int tiles = ((M + kTileM - 1) / kTileM) * (N / kBN);
   const int pairs = num_sms() / 2;
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
@@ -481,6 +499,7 @@ cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB
     case EPI_STORE: return launch_mode<EPI_STORE>(tmA, tmB, M, N, K, ep, s);
     case EPI_IN_PROJ: return launch_mode<EPI_IN_PROJ>(tmA, tmB, M, N, K, ep, s);
     case EPI_OUT_RESIDUAL: return launch_mode<EPI_OUT_RESIDUAL>(tmA, tmB, M, N, K, ep, s);
+    case EPI_STORE_F32: return launch_mode<EPI_STORE_F32>(tmA, tmB, M, N, K, ep, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -8,7 +8,10 @@ import torch
 from . import (FLUX3_W_BF16, FLUX3_W_FP8R, FLUX3_W_NVFP4, NVFP4_MATRICES, flux3_block_forward, flux3_block_init,
                flux3_block_init_fp8r, flux3_block_init_nvfp4, flux3_default_config, flux3_destroy,
                flux3_mode_blocks_forward, flux3_packed_weight_bytes, flux3_quantize_fp8r, flux3_quantize_nvfp4,
-               flux3_stack_forward, flux3_workspace_bytes)
+               flux3_stack_forward, flux3_workspace_bytes, flux3_cond_packed_bytes, flux3_cond_init,
+               flux3_cond_destroy, flux3_cond_workspace_bytes, flux3_conditioning, flux3_embed_tokens,
+               flux3_final_layer_workspace_bytes, flux3_final_layer, flux3_transformer_workspace_bytes,
+               flux3_transformer_forward, flux3_sigma_schedule, flux3_euler_step)
 
 WEIGHT_KEYS = ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out", "query_norm", "key_norm")
 
@@ -163,3 +166,108 @@ def mode_blocks_forward(mode_blocks, x, segments, pos_ids, early_mod, n_blocks=N
                               x.shape[0], segments, pos_ids.data_ptr(), early_mod.data_ptr(), ws.data_ptr(),
                               ws.numel(), _stream_ptr(stream))
     return x
+
+
+class Flux3Conditioning:
+    """The non-block weights (time_in, ref_time_in, the stream modulation
+    linears, the embedders, the output layer) on one device, through
+    flux3_cond_init.  weights: dict of bf16 device tensors keyed like the C
+    struct (early_mod / single_mod: lists of three; ref_time_in_* may be
+    absent)."""
+
+    def __init__(self, weights, stream=None):
+        dev = weights["time_in_in"].device
+        self.device = dev
+        ptrs = {}
+        for k, v in weights.items():
+            if v is None:
+                continue
+            ts = v if isinstance(v, (list, tuple)) else [v]
+            for t in ts:
+                assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.device == dev, k
+            ptrs[k] = [t.data_ptr() for t in ts] if isinstance(v, (list, tuple)) else v.data_ptr()
+        nbytes = flux3_cond_packed_bytes()
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.handle = flux3_cond_init(ptrs, self.packed.data_ptr(), nbytes, _stream_ptr(stream))
+        (stream or torch.cuda.current_stream()).synchronize()
+        self._ws = torch.empty(flux3_cond_workspace_bytes(), dtype=torch.uint8, device=dev)
+
+    def modulations(self, t, t_next=0.0, stream=None):
+        """(early [3, 9216], single [3, 9216], final [9216]) float32."""
+        early = torch.empty((3, 9216), dtype=torch.float32, device=self.device)
+        single = torch.empty((3, 9216), dtype=torch.float32, device=self.device)
+        fin = torch.empty(9216, dtype=torch.float32, device=self.device)
+        flux3_conditioning(self.handle, float(t), float(t_next), early.data_ptr(), single.data_ptr(), fin.data_ptr(),
+                           self._ws.data_ptr(), self._ws.numel(), _stream_ptr(stream))
+        return early, single, fin
+
+    def embed(self, inputs, segments, T, stream=None):
+        """inputs: three bf16 tensors (or None) indexed by stream id; returns x
+        float32 [T, 3072]."""
+        x = torch.empty((T, 3072), dtype=torch.float32, device=self.device)
+        flux3_embed_tokens(self.handle, [t.data_ptr() if t is not None else None for t in inputs], T, segments,
+                           x.data_ptr(), _stream_ptr(stream))
+        return x
+
+    def final_layer(self, x, segments, final_mod, stream=None):
+        T = x.shape[0]
+        n_img = sum(n for _, n, st in segments if st == 0)
+        v = torch.empty((n_img, 128), dtype=torch.float32, device=self.device)
+        ws = torch.empty(flux3_final_layer_workspace_bytes(T), dtype=torch.uint8, device=self.device)
+        flux3_final_layer(self.handle, x.data_ptr(), T, segments, final_mod.data_ptr(), v.data_ptr(), ws.data_ptr(),
+                          ws.numel(), _stream_ptr(stream))
+        return v
+
+    def close(self):
+        if getattr(self, "handle", None):
+            flux3_cond_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Flux3Transformer:
+    """One transformer call through flux3_transformer_forward: conditioning,
+    embedders, the per-mode blocks, the joint blocks, the output layer."""
+
+    def __init__(self, cond, mode_blocks, joint, n_mode_blocks=None):
+        self.cond, self.mode_blocks, self.joint = cond, list(mode_blocks), joint
+        used = [b for b in self.mode_blocks if b is not None]
+        self.n_mode_blocks = (min(b.n_blocks for b in used) if used else 0) if n_mode_blocks is None else n_mode_blocks
+        self._ws = torch.empty(0, dtype=torch.uint8, device=joint.device)
+
+    def forward(self, inputs, segments, pos_ids, t, t_next=0.0, stream=None, velocity=None):
+        T = pos_ids.shape[0]
+        need = flux3_transformer_workspace_bytes(self.joint.cfg, T)
+        if self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.joint.device)
+        n_img = sum(n for _, n, st in segments if st == 0)
+        if velocity is None:
+            velocity = torch.empty((n_img, 128), dtype=torch.float32, device=self.joint.device)
+        flux3_transformer_forward(self.cond.handle, [b.handle if b is not None else None for b in self.mode_blocks],
+                                  self.n_mode_blocks, self.joint.handle,
+                                  [t_.data_ptr() if t_ is not None else None for t_ in inputs], T, segments,
+                                  pos_ids.data_ptr(), float(t), float(t_next), velocity.data_ptr(),
+                                  self._ws.data_ptr(), self._ws.numel(), _stream_ptr(stream))
+        return velocity
+
+    def sample(self, latents, inputs, segments, pos_ids, steps=16, alpha=6.93, flow_map=True, stream=None):
+        """The flow-map sampler: for k < steps, v = forward(sigma_k, sigma_{k+1})
+        on the current latents (bf16 copy as the image input), then
+        latents += (sigma_{k+1} - sigma_k) v.  latents: float32 [T_image, 128],
+        updated in place."""
+        sig = flux3_sigma_schedule(steps, alpha)
+        v = torch.empty_like(latents)
+        img = torch.empty(latents.shape, dtype=torch.bfloat16, device=latents.device)
+        ins = list(inputs)
+        ins[0] = img
+        for k in range(steps):
+            img.copy_(latents)
+            self.forward(ins, segments, pos_ids, sig[k], sig[k + 1] if flow_map else 0.0, stream=stream, velocity=v)
+            flux3_euler_step(latents.data_ptr(), v.data_ptr(), latents.numel(), sig[k], sig[k + 1],
+                             _stream_ptr(stream))
+        return latents

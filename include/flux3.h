@@ -289,6 +289,109 @@ FLUX3_API flux3_status flux3_mode_blocks_forward(const flux3_handle *const *mode
                                                  const float *pos_ids, const float *early_mod, void *workspace,
                                                  size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------
+ * One transformer call around the block stacks ("FLUX.3 Image Klein support",
+ * comment "Structure (from dit.py)"): timestep conditioning, per-stream
+ * modulation vectors, input embedders, the image output layer; comment
+ * "Sampling": the sigma schedule and the flow-map Euler update.
+ * ------------------------------------------------------------------------ */
+
+/* The non-block weights, device bf16 [out, in] (no biases), 16-byte aligned.
+ * ref_time_in_* are NULL for a checkpoint without the flow-map timestep. */
+typedef struct flux3_cond_weights {
+  const void *time_in_in;       /* [3072, 256]   */
+  const void *time_in_out;      /* [3072, 3072]  */
+  const void *ref_time_in_in;   /* [3072, 256] or NULL */
+  const void *ref_time_in_out;  /* [3072, 3072] or NULL */
+  const void *early_mod[3];     /* [9216, 3072] per stream (image, image_cond, txt) */
+  const void *single_mod[3];    /* [9216, 3072] per stream */
+  const void *emb_in_image;     /* [3072, 128]   */
+  const void *emb_in_image_cond;/* [3072, 128]   */
+  const void *txt_in;           /* [3072, 20480] */
+  const void *final_adaln;      /* [6144, 3072]  */
+  const void *final_linear;     /* [128, 3072]   */
+} flux3_cond_weights;
+
+typedef struct flux3_cond flux3_cond;
+
+/* Bytes of the caller-owned buffer flux3_cond_init copies the weights into. */
+FLUX3_API size_t flux3_cond_packed_bytes(void);
+
+/* Creates the conditioning handle; copies the weights into `packed`
+ * (flux3_cond_packed_bytes() bytes, device, 16-byte aligned) on `stream`.  The
+ * source weights may be freed once the stream has passed the copies. */
+FLUX3_API flux3_status flux3_cond_init(flux3_cond **out, const flux3_cond_weights *w, void *packed,
+                                       size_t packed_bytes, void *stream);
+FLUX3_API void flux3_cond_destroy(flux3_cond *c);
+
+/* Device workspace of flux3_conditioning (a few tens of KB). */
+FLUX3_API size_t flux3_cond_workspace_bytes(void);
+
+/* The modulation vectors of one call.  Per stream s the conditioning vector
+ * vec_s = time_in(emb(t_s)) (+ ref_time_in(emb(t_next)) with the flow-map
+ * weights), t_image = t and t_image_cond = t_txt = 0, emb(t) = [cos, sin] of
+ * 1000 t 10000^(-i/128), i < 128, time_in = Linear, SiLU, Linear; then
+ *   early_mod[s]  = early_stream_modulations[s](SiLU(vec_s))    device float32 [3, 9216]
+ *   single_mod[s] = single_stream_modulations[s](SiLU(vec_s))   device float32 [3, 9216]
+ *   final_mod     = adaLN(SiLU(vec_image)) = shift | scale, then 3072 zeros
+ *                                                               device float32 [9216]
+ * (SiLU before the modulation linears is a reading: the pages name only the
+ * linear; the output layer's adaLN is stated as SiLU, Linear.)  t_next is
+ * ignored without ref_time_in. */
+FLUX3_API flux3_status flux3_conditioning(const flux3_cond *c, float t, float t_next, float *early_mod,
+                                          float *single_mod, float *final_mod, void *workspace, size_t ws_bytes,
+                                          void *stream);
+
+/* The input embedders: x[row] = emb_s(input_s[k]) for the k-th token of
+ * stream s in sequence order (emb_in.image / emb_in.image_cond on 128 latent
+ * channels, txt_in on 20480 text features), float32, written for all T rows.
+ *   inputs  host array [3] of device bf16 pointers indexed by flux3_stream:
+ *           image [T_image, 128], image_cond [T_ref, 128], txt [T_txt, 20480]
+ *           (16-byte aligned; NULL for a stream without tokens)
+ *   x       device float32 [T, 3072]; segs as flux3_block_forward. */
+FLUX3_API flux3_status flux3_embed_tokens(const flux3_cond *c, const void *const *inputs, int T,
+                                          const flux3_segment *segs, int n_segs, float *x, void *stream);
+
+/* Device workspace of flux3_final_layer for T tokens. */
+FLUX3_API size_t flux3_final_layer_workspace_bytes(int T);
+
+/* The output layer on the image tokens (in sequence order): h = (1 + scale) *
+ * LayerNorm(x) + shift (eps 1e-6, shift | scale = final_mod's first 6144
+ * values), velocity = h final_linear^T.
+ *   x         device float32 [T, 3072]
+ *   final_mod device float32 [9216] as flux3_conditioning writes it
+ *   velocity  device float32 [T_image, 128] */
+FLUX3_API flux3_status flux3_final_layer(const flux3_cond *c, const float *x, int T, const flux3_segment *segs,
+                                         int n_segs, const float *final_mod, float *velocity, void *workspace,
+                                         size_t ws_bytes, void *stream);
+
+/* Device workspace of flux3_transformer_forward for T tokens with the joint
+ * handle's configuration. */
+FLUX3_API size_t flux3_transformer_workspace_bytes(const flux3_config *joint_cfg, int T);
+
+/* One transformer call: conditioning, embedders, n_mode_blocks per-mode
+ * blocks (flux3_mode_blocks_forward with the early modulations; 0 skips
+ * them), the joint handle's blocks (single-stream modulations), the output
+ * layer.  Arguments as the functions above; velocity device float32
+ * [T_image, 128].  Each mode's token count must fit its mode handle's
+ * max_tokens and T the joint handle's. */
+FLUX3_API flux3_status flux3_transformer_forward(const flux3_cond *c, const flux3_handle *const *mode_handles,
+                                                 int n_mode_blocks, const flux3_handle *joint,
+                                                 const void *const *inputs, int T, const flux3_segment *segs,
+                                                 int n_segs, const float *pos_ids, float t, float t_next,
+                                                 float *velocity, void *workspace, size_t ws_bytes, void *stream);
+
+/* Host: sigma_k = alpha t_k / (1 + (alpha - 1) t_k), t_k = 1 - k / steps,
+ * k = 0..steps, into sigmas[steps + 1] (host float32; alpha 6.93 in the
+ * pages). */
+FLUX3_API flux3_status flux3_sigma_schedule(int steps, double alpha, float *sigmas);
+
+/* latent[i] += (sigma_next - sigma) * velocity[i], i < n (device float32; the
+ * difference is taken in double and rounded to float, the update is one fused
+ * multiply-add). */
+FLUX3_API flux3_status flux3_euler_step(float *latent, const float *velocity, size_t n, float sigma,
+                                        float sigma_next, void *stream);
+
 /* Largest T flux3_block_forward_noalloc accepts (its scratch is ~25 MB). */
 #define FLUX3_NOALLOC_MAX_TOKENS 512
 

@@ -25,3 +25,4 @@ docstring.
 from .flux3_oracle import *  # noqa: F401,F403
 from . import nvfp4  # noqa: F401
 from . import fp8r  # noqa: F401
+from . import flux3_model  # noqa: F401

@@ -1,0 +1,138 @@
+"""fp64 NumPy oracle of the parts around the block stacks: timestep
+conditioning, per-stream modulation vectors, input embedders, the image output
+layer, the sigma schedule and the sampler step.  Together with
+``flux3_oracle.mode_blocks_forward`` and ``flux3_oracle.stack_forward`` they
+make one transformer call.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Sources:
+* "FLUX.3 Image Klein support" (stable-diffusion.cpp issue #2142), comment
+  "Structure (from dit.py)": timestep_embedding(t) = [cos, sin] of
+  1000 * t * freqs (dim 256, max_period 10000) into an MLPEmbedder (Linear,
+  SiLU, Linear); image tokens carry the current t, the other modes 0; for the
+  flow-map checkpoint vec += ref_time_in(timestep_embedding(t_next)) for every
+  mode; output on the image tokens only: LayerNorm with shift/scale from
+  adaLN_modulation (SiLU, Linear to 2 x 3072), then a linear to 128 channels.
+  Comment "Sampling (sampling.py, pipeline.py)": t = linspace(1, 0, steps+1),
+  sigma = alpha t / (1 + (alpha - 1) t), alpha = 6.93; the flow map is called
+  with (sigma_k, sigma_{k+1}) and updates x += (sigma_{k+1} - sigma_k) v.
+  Tensor list: emb_in.{image,image_cond} [3072,128], txt_in [3072,20480],
+  time_in / ref_time_in in_layer [3072,256] and out_layer [3072,3072], the
+  modulation linears [9216,3072], final_layer adaLN [6144,3072] and linear
+  [128,3072].
+* "Welcome FLUX.3 Image Klein in Diffusers", "Every token gets its own
+  timestep" (text and reference tokens at timestep 0; the flow map's second
+  timestep embedding added to every token's modulation), "The denoising loop"
+  (shift 6.93; 44 of the 50 steps above sigma = 0.5; sigma about 0.97 at step
+  10), "Two stages" (only the image tokens reach the output layers).
+
+Readings (the pages are silent): the frequency ladder freqs_i =
+max_period^(-i/128), i = 0..127; the modulation vectors are Linear(SiLU(vec))
+like the output layer's adaLN (the pages name only the linear); the output
+LayerNorm is the blocks' one (no affine, eps 1e-6); adaLN chunk order shift,
+scale; the embedders, like every matrix of the checkpoint, have no bias.
+"""
+
+import numpy as np
+
+from .flux3_oracle import (EPS_LN, N_STREAMS, STREAM_IMAGE, STREAM_IMAGE_COND, STREAM_TXT, layer_norm,
+                           mode_blocks_forward, silu, stack_forward)
+
+TIME_DIM = 256
+MAX_PERIOD = 10000.0
+TIME_FACTOR = 1000.0
+LATENT_CH = 128
+TXT_FEAT = 20480
+SHIFT = 6.93
+
+__all__ = ["TIME_DIM", "MAX_PERIOD", "TIME_FACTOR", "LATENT_CH", "TXT_FEAT", "SHIFT",
+           "timestep_embedding", "mlp_embedder", "stream_vectors", "modulation_vectors", "embed_tokens",
+           "final_layer", "transformer_forward", "sigma_schedule", "euler_step"]
+
+
+def timestep_embedding(t, dim=TIME_DIM, max_period=MAX_PERIOD, time_factor=TIME_FACTOR):
+    """[cos(a), sin(a)] with a_i = time_factor * t * max_period^(-i/half),
+    i = 0..half-1 (the cosines first)."""
+    half = dim // 2
+    freqs = np.exp(-np.log(max_period) * np.arange(half, dtype=np.float64) / half)
+    a = time_factor * float(t) * freqs
+    return np.concatenate([np.cos(a), np.sin(a)])
+
+
+def mlp_embedder(x, w_in, w_out):
+    """MLPEmbedder: Linear, SiLU, Linear (no biases)."""
+    x = np.asarray(x, np.float64)
+    return silu(x @ np.asarray(w_in, np.float64).T) @ np.asarray(w_out, np.float64).T
+
+
+def stream_vectors(t, t_next, cond):
+    """The conditioning vector of each stream [3, D]: the image stream's from
+    timestep t, image_cond's and txt's from timestep 0; with ref_time_in
+    (flow map) every stream adds the embedding of t_next."""
+    vec = np.empty((N_STREAMS, np.asarray(cond["time_in_out"]).shape[0]))
+    v_t = mlp_embedder(timestep_embedding(t), cond["time_in_in"], cond["time_in_out"])
+    v_0 = mlp_embedder(timestep_embedding(0.0), cond["time_in_in"], cond["time_in_out"])
+    vec[STREAM_IMAGE] = v_t
+    vec[STREAM_IMAGE_COND] = v_0
+    vec[STREAM_TXT] = v_0
+    if cond.get("ref_time_in_in") is not None:
+        vec += mlp_embedder(timestep_embedding(t_next), cond["ref_time_in_in"], cond["ref_time_in_out"])
+    return vec
+
+
+def modulation_vectors(vec, lins):
+    """Per stream s: lins[s](SiLU(vec[s])) -> [3, 3D] (shift | scale | gate)."""
+    vec = np.asarray(vec, np.float64)
+    return np.stack([silu(vec[s]) @ np.asarray(lins[s], np.float64).T for s in range(N_STREAMS)])
+
+
+def embed_tokens(inputs, stream_id, cond):
+    """x [T, D]: each token's input row through its stream's embedder
+    (emb_in.image, emb_in.image_cond: 128 latent channels; txt_in: 20480 text
+    features).  inputs[s] holds stream s's rows in sequence order."""
+    stream_id = np.asarray(stream_id)
+    W = {STREAM_IMAGE: cond["emb_in_image"], STREAM_IMAGE_COND: cond["emb_in_image_cond"],
+         STREAM_TXT: cond["txt_in"]}
+    D = np.asarray(W[STREAM_IMAGE]).shape[0]
+    x = np.zeros((len(stream_id), D))
+    for s in range(N_STREAMS):
+        idx = np.nonzero(stream_id == s)[0]
+        if idx.size:
+            x[idx] = np.asarray(inputs[s], np.float64) @ np.asarray(W[s], np.float64).T
+    return x
+
+
+def final_layer(x_img, vec_img, w_adaln, w_linear, eps=EPS_LN):
+    """Image tokens only: (shift, scale) = chunk(adaLN(SiLU(vec)), 2);
+    h = (1 + scale) * LayerNorm(x) + shift; velocity = h @ linear^T."""
+    mod = silu(np.asarray(vec_img, np.float64)) @ np.asarray(w_adaln, np.float64).T
+    D = mod.shape[-1] // 2
+    shift, scale = mod[:D], mod[D:]
+    h = (1.0 + scale) * layer_norm(x_img, eps) + shift
+    return h @ np.asarray(w_linear, np.float64).T
+
+
+def transformer_forward(inputs, stream_id, pos, t, t_next, cond, mode_blocks, joint_blocks):
+    """One call: embed, the per-mode blocks (early modulations), the joint
+    blocks (single-stream modulations), the output layer on the image tokens
+    (in sequence order).  Returns the velocity [T_image, 128]."""
+    stream_id = np.asarray(stream_id)
+    vec = stream_vectors(t, t_next, cond)
+    early = modulation_vectors(vec, cond["early_mod"])
+    single = modulation_vectors(vec, cond["single_mod"])
+    x = embed_tokens(inputs, stream_id, cond)
+    x = mode_blocks_forward(x, mode_blocks, early, stream_id, pos)
+    x = stack_forward(x, joint_blocks, single, stream_id, pos)
+    img = np.nonzero(stream_id == STREAM_IMAGE)[0]
+    return final_layer(x[img], vec[STREAM_IMAGE], cond["final_adaln"], cond["final_linear"])
+
+
+def sigma_schedule(steps, alpha=SHIFT):
+    """sigma_k for t_k = 1 - k/steps, k = 0..steps."""
+    t = np.linspace(1.0, 0.0, steps + 1)
+    return alpha * t / (1.0 + (alpha - 1.0) * t)
+
+
+def euler_step(x, v, sigma, sigma_next):
+    return np.asarray(x, np.float64) + (sigma_next - sigma) * np.asarray(v, np.float64)

@@ -102,6 +102,10 @@ WORKLOADS = {
                         blocks=5, calls=1, wfmt="bf16", stage="modes"),
     "modes5_1024sq_ref1_t8704": dict(spec=[("txt", 512), ("image", (64, 64)), ("image_cond", (64, 64))],
                                      blocks=5, calls=1, wfmt="bf16", stage="modes"),
+    # the 16-step flow-map sampler at 1024x1024 text-to-image: each step one transformer call
+    # (conditioning, embedders, 5 per-mode blocks, 28 joint blocks, output layer) and the Euler update
+    "sample16_1024sq_t4608": dict(spec=[("txt", 512), ("image", (64, 64))], blocks=28, calls=16, wfmt="bf16",
+                                  stage="model", mode_blocks=5),
     # 28-block stack, row-wise FP8 weights, 1024x1024 + one 1024x1024 reference
     "stack28_fp8r_1024sq_ref1_t8704": dict(spec=[("txt", 512), ("image", (64, 64)), ("image_cond", (64, 64))],
                                            blocks=28, calls=1, wfmt="fp8r"),
@@ -157,6 +161,46 @@ def modulation(seed, call=0, device="cpu", hidden=HIDDEN, std=0.1):
     image_cond, txt; columns: shift | scale | gate)."""
     g = _gen(device, _seed(seed, "mod", call))
     return torch.randn((3, 3 * hidden), generator=g, device=device) * std
+
+
+COND_SHAPES = {"time_in_in": (3072, 256), "time_in_out": (3072, 3072), "ref_time_in_in": (3072, 256),
+               "ref_time_in_out": (3072, 3072), "emb_in_image": (3072, 128), "emb_in_image_cond": (3072, 128),
+               "txt_in": (3072, 20480), "final_adaln": (6144, 3072), "final_linear": (128, 3072)}
+
+
+def cond_weights(seed, device="cpu", std=0.02, flow=True):
+    """The non-block weights (time_in, ref_time_in, the six stream modulation
+    linears, the embedders, the image output layer): N(0, std) rounded to
+    bf16, shapes of the checkpoint's tensor list.  Without ``flow`` the
+    ref_time_in weights are None."""
+    w = {}
+    for k, shape in COND_SHAPES.items():
+        if k.startswith("ref_time_in") and not flow:
+            w[k] = None
+            continue
+        g = _gen(device, _seed(seed, "cond", k))
+        w[k] = (torch.randn(shape, generator=g, device=device) * std).to(torch.bfloat16)
+    for grp in ("early_mod", "single_mod"):
+        w[grp] = []
+        for s in range(3):
+            g = _gen(device, _seed(seed, "cond", grp, s))
+            w[grp].append((torch.randn((9216, 3072), generator=g, device=device) * std).to(torch.bfloat16))
+    return w
+
+
+def stream_inputs(seed, lay, device="cpu"):
+    """Per stream the embedder inputs of its tokens in sequence order, bf16
+    N(0, 1): image and image_cond 128 latent channels, txt 20480 features
+    (None for a stream without tokens)."""
+    out = []
+    for s, ch in ((STREAM_IMAGE, 128), (STREAM_IMAGE_COND, 128), (STREAM_TXT, 20480)):
+        n = int((lay.stream_id == s).sum())
+        if n == 0:
+            out.append(None)
+            continue
+        g = _gen(device, _seed(seed, "inputs", s))
+        out.append(torch.randn((n, ch), generator=g, device=device).to(torch.bfloat16))
+    return out
 
 
 def to_f64(t):

@@ -7,6 +7,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 import diffusion_transformer_block_fwd_b300 as F3
@@ -225,3 +226,38 @@ def test_fp8r_sizes_and_validation():
     assert L.flux3_quantize_fp8r(16, 0, 32, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_quantize_fp8r(18, 4, 32, 16, 16, None) == F3.FLUX3_ERR_ALIGNMENT
     assert L.flux3_quantize_fp8r(16, 4, 32, 16, 18, None) == F3.FLUX3_ERR_ALIGNMENT
+
+
+def test_sigma_schedule_host_entry_point_matches_oracle():
+    from oracle import flux3_model as M
+    for steps in (16, 50):
+        got = np.array(F3.flux3_sigma_schedule(steps, 6.93), dtype=np.float32)
+        assert np.array_equal(got, M.sigma_schedule(steps).astype(np.float32))
+    assert F3.lib().flux3_sigma_schedule(0, ctypes.c_double(6.93), (ctypes.c_float * 1)()) == F3.FLUX3_ERR_INVALID_ARG
+
+
+def test_model_entry_points_validation_before_any_launch():
+    L = F3.lib()
+    h = ctypes.c_void_p()
+    w = F3.flux3_cond_weights()
+    assert L.flux3_cond_init(None, ctypes.byref(w), 256, 1 << 40, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_cond_init(ctypes.byref(h), ctypes.byref(w), 256, 1 << 40, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_cond_init(ctypes.byref(h), ctypes.byref(w), 256, 1024, None) == F3.FLUX3_ERR_WORKSPACE
+    w.time_in_in = 4096
+    w.ref_time_in_in = 4096          # ref_time_in_out missing: both or neither
+    assert L.flux3_cond_init(ctypes.byref(h), ctypes.byref(w), 256, 1 << 40, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert h.value is None
+    assert F3.flux3_cond_packed_bytes() > (3072 * 20480 + 6 * 9216 * 3072) * 2
+    assert L.flux3_conditioning(None, ctypes.c_float(0.5), ctypes.c_float(0.4), 16, 16, 16, 16, 1 << 20, None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    segs, n = _segs([(0, 8, 0)])
+    ins = (ctypes.c_void_p * 3)(16, 16, 16)
+    assert L.flux3_embed_tokens(None, ins, 8, segs, n, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_final_layer(None, 16, 8, segs, n, 16, 16, 16, 1 << 20, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_transformer_forward(None, None, 0, None, ins, 8, segs, n, 16, ctypes.c_float(0.5),
+                                       ctypes.c_float(0.4), 16, 16, 1 << 20, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_euler_step(None, 16, 8, ctypes.c_float(1.0), ctypes.c_float(0.9), None) == \
+        F3.FLUX3_ERR_INVALID_ARG
+    cfg = F3.flux3_default_config()
+    assert F3.flux3_transformer_workspace_bytes(cfg, 4608) > F3.flux3_workspace_bytes(cfg, 4608) + 4608 * 3072 * 4
+    assert F3.flux3_transformer_workspace_bytes(cfg, 0) == 0

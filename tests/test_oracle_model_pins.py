@@ -1,0 +1,157 @@
+"""Pins of the oracle's parts around the block stacks (oracle/flux3_model.py):
+the sigma schedule against the figures the pages print, the timestep
+embedding's closed forms, torch.nn.functional restatements of the embedder,
+modulation and output layer, and the stream rules of the conditioning."""
+
+import math
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle as O
+from oracle import flux3_model as M
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------
+# Schedule ("The denoising loop": shift 6.93, 44 of the 50 steps above
+# sigma = 0.5, sigma still 0.97 at step 10; "Sampling": t = linspace(1, 0,
+# steps+1), sigma = alpha t / (1 + (alpha - 1) t))
+# --------------------------------------------------------------------------
+def test_schedule_matches_the_printed_figures():
+    s = M.sigma_schedule(50)
+    assert len(s) == 51 and s[0] == 1.0 and s[-1] == 0.0
+    assert int((s[:50] > 0.5).sum()) == 44
+    assert abs(s[10] - 0.97) < 0.005
+    assert np.all(np.diff(s) < 0)
+
+
+def test_schedule_inverse_map_and_sixteen_steps():
+    # sigma(t) inverts to t = sigma / (alpha - (alpha - 1) sigma)
+    s = M.sigma_schedule(16)
+    t = s / (M.SHIFT - (M.SHIFT - 1.0) * s)
+    np.testing.assert_allclose(t, np.linspace(1, 0, 17), rtol=0, atol=1e-15)
+    # alpha = 1 is the identity schedule
+    np.testing.assert_allclose(M.sigma_schedule(8, alpha=1.0), np.linspace(1, 0, 9), atol=1e-15)
+
+
+def test_euler_steps_telescope():
+    rng = _rng(1)
+    x0, v = rng.standard_normal(10), rng.standard_normal(10)
+    s = M.sigma_schedule(16)
+    x = x0
+    for k in range(16):
+        x = M.euler_step(x, v, s[k], s[k + 1])
+    np.testing.assert_allclose(x, x0 - v, rtol=1e-13, atol=1e-13)   # sum of steps = sigma_16 - sigma_0 = -1
+
+
+# --------------------------------------------------------------------------
+# Timestep embedding ("Structure": [cos, sin] of 1000 * t * freqs, dim 256)
+# --------------------------------------------------------------------------
+def test_timestep_embedding_closed_forms():
+    e0 = M.timestep_embedding(0.0)
+    assert e0.shape == (256,) and np.all(e0[:128] == 1.0) and np.all(e0[128:] == 0.0)
+    for t in (0.03, 0.5, 0.97, 1.0):
+        e = M.timestep_embedding(t)
+        np.testing.assert_allclose(e[:128] ** 2 + e[128:] ** 2, 1.0, rtol=1e-14)     # one (cos, sin) pair per freq
+        assert e[0] == math.cos(1000.0 * t) and e[128] == math.sin(1000.0 * t)      # the first frequency is 1
+    # the ladder runs from 1 down towards 1/max_period
+    a = np.arctan2(M.timestep_embedding(1e-3)[128:], M.timestep_embedding(1e-3)[:128]) / 1.0
+    np.testing.assert_allclose(a, 10000.0 ** (-np.arange(128) / 128), rtol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Embedders, modulation, output layer: torch.nn.functional restatements
+# --------------------------------------------------------------------------
+def _t(a):
+    return torch.from_numpy(np.asarray(a, np.float64))
+
+
+def test_mlp_embedder_and_modulation_match_library():
+    rng = _rng(2)
+    x = rng.standard_normal(16)
+    w_in, w_out = rng.standard_normal((24, 16)) * 0.3, rng.standard_normal((24, 24)) * 0.3
+    ref = F.linear(F.silu(F.linear(_t(x), _t(w_in))), _t(w_out)).numpy()
+    np.testing.assert_allclose(M.mlp_embedder(x, w_in, w_out), ref, rtol=1e-13, atol=1e-14)
+    vec = rng.standard_normal((3, 24))
+    lins = [rng.standard_normal((72, 24)) * 0.2 for _ in range(3)]
+    ref = np.stack([F.linear(F.silu(_t(vec[s])), _t(lins[s])).numpy() for s in range(3)])
+    np.testing.assert_allclose(M.modulation_vectors(vec, lins), ref, rtol=1e-13, atol=1e-14)
+
+
+def test_final_layer_matches_library():
+    rng = _rng(3)
+    D = 32
+    x = rng.standard_normal((7, D))
+    vec = rng.standard_normal(D)
+    w_ada, w_lin = rng.standard_normal((2 * D, D)) * 0.2, rng.standard_normal((8, D)) * 0.2
+    mod = F.linear(F.silu(_t(vec)), _t(w_ada))
+    shift, scale = mod.chunk(2)
+    h = (1 + scale) * F.layer_norm(_t(x), (D,), eps=1e-6) + shift
+    np.testing.assert_allclose(M.final_layer(x, vec, w_ada, w_lin), F.linear(h, _t(w_lin)).numpy(),
+                               rtol=1e-12, atol=1e-13)
+
+
+def _tiny_cond(rng, D=32, flow=True):
+    c = {"time_in_in": rng.standard_normal((D, 256)) * 0.1, "time_in_out": rng.standard_normal((D, D)) * 0.2,
+         "early_mod": [rng.standard_normal((3 * D, D)) * 0.2 for _ in range(3)],
+         "single_mod": [rng.standard_normal((3 * D, D)) * 0.2 for _ in range(3)],
+         "emb_in_image": rng.standard_normal((D, 8)) * 0.3, "emb_in_image_cond": rng.standard_normal((D, 8)) * 0.3,
+         "txt_in": rng.standard_normal((D, 40)) * 0.1, "final_adaln": rng.standard_normal((2 * D, D)) * 0.2,
+         "final_linear": rng.standard_normal((8, D)) * 0.2}
+    if flow:
+        c["ref_time_in_in"] = rng.standard_normal((D, 256)) * 0.1
+        c["ref_time_in_out"] = rng.standard_normal((D, D)) * 0.2
+    return c
+
+
+def test_stream_vectors_follow_the_timestep_rules():
+    rng = _rng(4)
+    c = _tiny_cond(rng)
+    v = M.stream_vectors(0.6, 0.4, c)
+    assert np.array_equal(v[1], v[2])                      # image_cond and txt both at timestep 0
+    assert not np.allclose(v[0], v[1])
+    v0 = M.stream_vectors(0.0, 0.4, c)
+    assert np.array_equal(v0[0], v0[1])                    # at t = 0 the image stream matches them
+    # the flow-map term is the same for every stream
+    d = M.stream_vectors(0.6, 0.4, c) - M.stream_vectors(0.6, 0.1, c)
+    np.testing.assert_allclose(d[0], d[1], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(d[0], d[2], rtol=0, atol=1e-15)
+    assert np.any(d != 0)
+    c.pop("ref_time_in_in"), c.pop("ref_time_in_out")
+    assert np.array_equal(M.stream_vectors(0.6, 0.4, c), M.stream_vectors(0.6, 0.1, c))
+
+
+def test_embed_tokens_routes_each_stream_through_its_embedder():
+    rng = _rng(5)
+    c = _tiny_cond(rng)
+    sid = np.array([2, 2, 0, 0, 0, 1, 1, 0])
+    ins = [rng.standard_normal((4, 8)), rng.standard_normal((2, 8)), rng.standard_normal((2, 40))]
+    x = M.embed_tokens(ins, sid, c)
+    np.testing.assert_allclose(x[[2, 3, 4, 7]], F.linear(_t(ins[0]), _t(c["emb_in_image"])).numpy(), rtol=1e-13)
+    np.testing.assert_allclose(x[[5, 6]], F.linear(_t(ins[1]), _t(c["emb_in_image_cond"])).numpy(), rtol=1e-13)
+    np.testing.assert_allclose(x[[0, 1]], F.linear(_t(ins[2]), _t(c["txt_in"])).numpy(), rtol=1e-13)
+
+
+def test_transformer_output_is_the_image_tokens_only():
+    """Velocity rows = image tokens in sequence order; text and reference
+    inputs reach them only through the joint blocks (zero joint blocks: the
+    image velocity ignores the other streams entirely)."""
+    from test_oracle_pins import _tiny_block
+    rng = _rng(6)
+    c = _tiny_cond(rng)
+    mode_blocks = [[_tiny_block(rng)] for _ in range(3)]
+    joint = [_tiny_block(rng)]
+    sid = np.array([2, 2, 2, 0, 0, 0, 0, 1, 1])
+    pos = np.zeros((9, 4))
+    ins = [rng.standard_normal((4, 8)), rng.standard_normal((2, 8)), rng.standard_normal((3, 40))]
+    v = M.transformer_forward(ins, sid, pos, 0.7, 0.5, c, mode_blocks, joint)
+    assert v.shape == (4, 8)
+    ins2 = [ins[0], ins[1], ins[2] + 1.0]
+    assert not np.allclose(M.transformer_forward(ins2, sid, pos, 0.7, 0.5, c, mode_blocks, joint), v)
+    assert np.array_equal(M.transformer_forward(ins2, sid, pos, 0.7, 0.5, c, mode_blocks, []),
+                          M.transformer_forward(ins, sid, pos, 0.7, 0.5, c, mode_blocks, []))
