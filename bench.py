@@ -277,6 +277,8 @@ def run_ours(args):
         return run_modes(args, rank, world, local, dev)
     if wl.get("stage") == "model":
         return run_model(args, rank, world, local, dev)
+    if wl.get("stage") == "cfg":
+        return run_cfg(args, rank, world, local, dev)
     if wl["blocks"] > 1:
         return run_stack(args, rank, world, local, dev)
     spec = wl["spec"]
@@ -754,6 +756,124 @@ def run_model(args, rank, world, local, dev):
                          "frac": tflops / world / (bf16_sust or bf16_burst), "traffic": None,
                          "peak_source": "measured bf16 sustained (MEASURED_PEAKS.json)"},
             "gpu_launches": per_call_launches * steps * args.steps, "clocks": clocks, "wall_s_timed_region": t_wall}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for b in mb + [joint]:
+        if b is not None:
+            b.close()
+    cond.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_cfg(args, rank, world, local, dev):
+    """The base model's sampler: a step is `calls` sampler steps, each one
+    batched transformer call on the two-sample pack [unconditional,
+    conditional] (flux3_transformer_forward_batch: joint blocks over both
+    samples at once, attention per sample) and the guided Euler update
+    (flux3_cfg_euler_step, guidance 3.5)."""
+    import torch
+    import torch.distributed as dist
+
+    import diffusion_transformer_block_fwd_b300 as F3
+    import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    pack = synth.build_pack(wl["specs"])
+    T, nb, steps, nm = pack.T, wl["blocks"], wl["calls"], wl["mode_blocks"]
+    counts = [[int((lay.stream_id == m).sum()) for m in range(3)] for lay in pack.layouts]
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        cw = synth.cond_weights(1, device=dev, flow=False)
+        stream.synchronize()
+        cond = F3.Flux3Conditioning(cw, stream=stream)
+        del cw
+        mb = []
+        for m in range(3):
+            mx = max(c[m] for c in counts)
+            if mx == 0:
+                mb.append(None)
+                continue
+            ws = [synth.block_weights(10 + m, b, device=dev) for b in range(nm)]
+            stream.synchronize()
+            mb.append(F3.Flux3Blocks(ws, max_tokens=mx, stream=stream))
+            del ws
+        ws = [synth.block_weights(1, b, device=dev) for b in range(nb)]
+        stream.synchronize()
+        joint = F3.Flux3Blocks(ws, max_tokens=T, stream=stream)
+        del ws
+    torch.cuda.synchronize(dev)
+    model = F3.Flux3Transformer(cond, mb, joint)
+    ins = [synth.stream_inputs(1 + b, lay, device=dev) for b, lay in enumerate(pack.layouts)]
+    noise = ins[1][0].float()
+    lat = noise.clone()
+    pos = torch.from_numpy(pack.pos).to(dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        model.sample_cfg(lat, ins[0], ins[1], pack.segments, pack.sample_start, pos, steps=steps, stream=stream)
+        if evs is not None:
+            evs[1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            lat.copy_(noise)
+            step()
+        st = F3.flux3_check_error(sp)
+        assert st == 0, F3.status_string(st)
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(local)
+        sampler.start()
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            lat.copy_(noise)
+            flush.zero_()
+            step(events[i])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+        clocks = sampler.stop()
+    st = F3.flux3_check_error(sp)
+    assert st == 0, F3.status_string(st)
+    assert torch.isfinite(lat).all()
+    value, step_ms = replica_throughput(T * steps, statistics.mean(e[0].elapsed_time(e[1]) for e in events), world,
+                                        dev)
+    # per call: per-sample embedders, per-mode blocks and output layers; joint blocks over the pack
+    per_call = sum(model_call_flops(c, nm, 0) for c in counts) + nb * sum(block_flops(sum(c)) for c in counts)
+    # our kernels per call: per sample ~13 conditioning launches, one embedder GEMM per segment, the per-mode
+    # blocks (2 + 4 per block per present mode), the output layer (LayerNorm + GEMM); the joint blocks
+    # (2 + 4 per block, one more attention launch per block for each further sample); the guided update
+    n_s = len(counts)
+    launches = (sum(13 + len(lay.segments) + sum(2 + 4 * nm for m in range(3) if c[m]) + 2
+                    for c, lay in zip(counts, pack.layouts))
+                + 2 + 4 * nb + nb * (n_s - 1) + 1)
+    flops = steps * per_call
+    hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
+    tflops = world * flops / (step_ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s (two-sample guided calls of the sampler)",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (random-init N(0,0.02) weights, N(0,1) latents and text features)",
+            "config": {"workload": args.workload, "T": T, "sample_start": pack.sample_start,
+                       "tokens_per_mode_per_sample": counts, "sampler_steps": steps, "guidance": 3.5,
+                       "mode_blocks": nm, "joint_blocks": nb, "segments": pack.segments,
+                       "l2": "flushed between timed steps",
+                       "launch": "stream launches through flux3_transformer_forward_batch and flux3_cfg_euler_step"},
+            "ms_per_image": step_ms, "ms_per_call": step_ms / steps,
+            "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
+            "frac_of_bf16_sustained": (tflops / world / bf16_sust) if bf16_sust else None,
+            "roofline": {"kernel": "whole sampler", "bound": "tensor", "achieved": tflops / world,
+                         "peak": bf16_sust or bf16_burst, "unit": "TFLOP/s",
+                         "frac": tflops / world / (bf16_sust or bf16_burst), "traffic": None,
+                         "peak_source": "measured bf16 sustained (MEASURED_PEAKS.json)"},
+            "gpu_launches": launches * steps * args.steps, "clocks": clocks, "wall_s_timed_region": t_wall}
     if rank == 0:
         print(json.dumps(line), flush=True)
     for b in mb + [joint]:

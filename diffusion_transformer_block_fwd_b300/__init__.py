@@ -31,6 +31,7 @@ FLUX3_STREAM_IMAGE_COND = 1
 FLUX3_STREAM_TXT = 2
 FLUX3_MAX_SEGMENTS = 32
 FLUX3_NOALLOC_MAX_TOKENS = 512
+FLUX3_MAX_SAMPLES = 16
 
 EXPORTED = (
     "flux3_default_config", "flux3_packed_weight_bytes", "flux3_workspace_bytes", "flux3_block_init",
@@ -42,6 +43,8 @@ EXPORTED = (
     "flux3_cond_packed_bytes", "flux3_cond_init", "flux3_cond_destroy", "flux3_cond_workspace_bytes",
     "flux3_conditioning", "flux3_embed_tokens", "flux3_final_layer_workspace_bytes", "flux3_final_layer",
     "flux3_transformer_workspace_bytes", "flux3_transformer_forward", "flux3_sigma_schedule", "flux3_euler_step",
+    "flux3_stack_forward_batch", "flux3_transformer_batch_workspace_bytes", "flux3_transformer_forward_batch",
+    "flux3_cfg_euler_step",
 )
 
 
@@ -154,6 +157,12 @@ def lib():
                                               vp, vp, sz, vp]),
             "flux3_sigma_schedule": (i, [i, ctypes.c_double, ctypes.POINTER(ctypes.c_float)]),
             "flux3_euler_step": (i, [vp, vp, sz, f, f, vp]),
+            "flux3_stack_forward_batch": (i, [vp, i, i, vp, i, segp, i, ctypes.POINTER(i), i, vp, vp, vp, sz, vp]),
+            "flux3_transformer_batch_workspace_bytes": (sz, [cfgp, i, i]),
+            "flux3_transformer_forward_batch": (i, [vp, ctypes.POINTER(vp), i, vp, ctypes.POINTER(vp), i, segp, i,
+                                                    ctypes.POINTER(i), i, vp, ctypes.POINTER(f), ctypes.POINTER(f),
+                                                    vp, vp, sz, vp]),
+            "flux3_cfg_euler_step": (i, [vp, vp, vp, sz, f, f, f, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -325,6 +334,44 @@ def flux3_sigma_schedule(steps, alpha=6.93):
 
 def flux3_euler_step(latent, velocity, n, sigma, sigma_next, stream=0):
     _check(lib().flux3_euler_step(latent, velocity, n, sigma, sigma_next, stream), "flux3_euler_step")
+
+
+def _ints(v):
+    return (ctypes.c_int * len(v))(*[int(a) for a in v])
+
+
+def _floats(v):
+    return (ctypes.c_float * len(v))(*[float(a) for a in v])
+
+
+def flux3_stack_forward_batch(h, first_block, n_blocks, x, T, segments, sample_start, pos_ids, mod, workspace,
+                              ws_bytes, stream=0):
+    segs = segments_array(segments)
+    _check(lib().flux3_stack_forward_batch(h, first_block, n_blocks, x, T, segs, len(segments), _ints(sample_start),
+                                           len(sample_start) - 1, pos_ids, mod, workspace, ws_bytes, stream),
+           "flux3_stack_forward_batch")
+
+
+def flux3_transformer_batch_workspace_bytes(cfg, T, n_samples):
+    return int(lib().flux3_transformer_batch_workspace_bytes(ctypes.byref(cfg), int(T), int(n_samples)))
+
+
+def flux3_transformer_forward_batch(c, mode_handles, n_mode_blocks, joint, inputs, T, segments, sample_start,
+                                    pos_ids, t, t_next, velocity, workspace, ws_bytes, stream=0):
+    """inputs: per sample three device pointers (image, image_cond, txt);
+    t, t_next: per-sample timesteps."""
+    flat = [p for per in inputs for p in per]
+    ptrs = (ctypes.c_void_p * len(flat))(*[(int(p) if p else None) for p in flat])
+    segs = segments_array(segments)
+    _check(lib().flux3_transformer_forward_batch(c, _ptr3(mode_handles), n_mode_blocks, joint, ptrs, T, segs,
+                                                 len(segments), _ints(sample_start), len(sample_start) - 1, pos_ids,
+                                                 _floats(t), _floats(t_next), velocity, workspace, ws_bytes, stream),
+           "flux3_transformer_forward_batch")
+
+
+def flux3_cfg_euler_step(latent, v_uncond, v_cond, n, guidance, sigma, sigma_next, stream=0):
+    _check(lib().flux3_cfg_euler_step(latent, v_uncond, v_cond, n, guidance, sigma, sigma_next, stream),
+           "flux3_cfg_euler_step")
 
 
 def flux3_dequantize_block(h, block_idx, w_in, w_out, stream=0):

@@ -12,6 +12,7 @@
 //                          memory)
 //   add_row_kernel         y[m] += r for the flow-map timestep term
 //   euler_kernel           latent += (sigma_next - sigma) * velocity
+//   cfg_euler_kernel       the same with v = v_uncond + g (v_cond - v_uncond)
 
 #pragma once
 
@@ -96,6 +97,14 @@ __global__ void euler_kernel(float *__restrict__ latent, const float *__restrict
     latent[i] = fmaf(dt, v[i], latent[i]);
 }
 
+__global__ void cfg_euler_kernel(float *__restrict__ latent, const float *__restrict__ vu, const float *__restrict__ vc,
+                                 size_t n, float g, float dt) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float u = vu[i];
+    latent[i] = fmaf(dt, fmaf(g, vc[i] - u, u), latent[i]);
+  }
+}
+
 }  // namespace cond_detail
 
 cudaError_t launch_timestep_embed(double t0, double t1, double t2, float *out, cudaStream_t s) {
@@ -129,6 +138,13 @@ cudaError_t launch_add_row(float *y, int ldy, int M, const float *r, int n, cuda
 cudaError_t launch_euler(float *latent, const float *v, size_t n, float dt, cudaStream_t s) {
   const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
   cond_detail::euler_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(latent, v, n, dt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cfg_euler(float *latent, const float *vu, const float *vc, size_t n, float g, float dt,
+                             cudaStream_t s) {
+  const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
+  cond_detail::cfg_euler_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(latent, vu, vc, n, g, dt);
   return cudaGetLastError();
 }
 

@@ -189,20 +189,52 @@ flux3_status run_out_projection(const flux3_handle *h, int b, const __nv_bfloat1
   return cuda_status(launch_gemm(EPI_OUT_RESIDUAL, tmA, h->tm_out[b], T, kHidden, kCatCols, ep, s));
 }
 
+// Sample boundaries of a batched call: 0 = start[0] < ... < start[n] = T,
+// n <= FLUX3_MAX_SAMPLES, every segment inside one sample.  sample_of[i] is
+// segment i's sample.
+flux3_status samples_ok(const int *start, int n, int T, const flux3_segment *segs, int n_segs, int *sample_of) {
+  if (!start || n < 1 || n > FLUX3_MAX_SAMPLES || start[0] != 0 || start[n] != T) return FLUX3_ERR_INVALID_ARG;
+  for (int b = 0; b < n; ++b)
+    if (start[b + 1] <= start[b]) return FLUX3_ERR_INVALID_ARG;
+  for (int i = 0; i < n_segs; ++i) {
+    int b = 0;
+    while (b < n && segs[i].start >= start[b + 1]) ++b;
+    if (b == n || segs[i].start + segs[i].len > start[b + 1]) return FLUX3_ERR_INVALID_ARG;
+    sample_of[i] = b;
+  }
+  return FLUX3_OK;
+}
+
+// The blocks over one sample, or over a batch of samples (sample_start /
+// n_samples): LayerNorm and both GEMMs over all rows, attention per sample,
+// the modulation row of a token = 3 * sample + stream.
 flux3_status forward_common(const flux3_handle *h, int first, int count, float *x, int T, const flux3_segment *segs,
                             int n_segs, const float *pos, const float *mod, void *workspace, size_t ws_bytes,
-                            cudaStream_t s) {
+                            cudaStream_t s, const int *sample_start = nullptr, int n_samples = 1) {
   if (!h || !x || !pos || !mod || !workspace) return FLUX3_ERR_INVALID_ARG;
   if (first < 0 || count < 1 || first + count > h->n_blocks) return FLUX3_ERR_INVALID_ARG;
   if (T < 1 || T > h->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
   F3_TRY(segments_ok(segs, n_segs, T));
+  const int one_sample[2] = {0, T};
+  int sample_of[FLUX3_MAX_SEGMENTS] = {0};
+  if (sample_start) {
+    F3_TRY(samples_ok(sample_start, n_samples, T, segs, n_segs, sample_of));
+  } else {
+    sample_start = one_sample;
+    n_samples = 1;
+  }
+  flux3_segment rows[FLUX3_MAX_SEGMENTS];      // segments with the modulation row as their stream
+  for (int i = 0; i < n_segs; ++i) {
+    rows[i] = segs[i];
+    rows[i].stream = 3 * sample_of[i] + segs[i].stream;
+  }
   if (!aligned16(x) || !aligned16(pos) || !aligned16(mod) || !aligned16(workspace)) return FLUX3_ERR_ALIGNMENT;
   const bool fp4 = lowp(h->cfg.wfmt);
   Workspace ws;
   if (ws_bytes < workspace_layout(T, nullptr, nullptr, fp4)) return FLUX3_ERR_WORKSPACE;
   workspace_layout(T, static_cast<uint8_t *>(workspace), &ws, fp4);
 
-  F3_CUDA(launch_stream_ids(segs, n_segs, T, ws.sid, s));
+  F3_CUDA(launch_stream_ids(rows, n_segs, T, ws.sid, s));
   F3_CUDA(launch_rope_tables(pos, T, h->cfg.rope_theta, ws.cos_tab, ws.sin_tab, s));
   CUtensorMap tmH, tmCat, tmWin, tmWout;
   if (!make_tmap_bf16(&tmH, ws.h, (uint64_t)T, kHidden, kBM)) return FLUX3_ERR_CUDA;
@@ -223,7 +255,11 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     ep.knorm = block_norms(h, b) + kHeadDim;
     ep.eps_rms = h->cfg.eps_rms;
     F3_CUDA(launch_gemm(EPI_IN_PROJ, tmH, fp4 ? tmWin : h->tm_in[b], T, kInRows, kHidden, ep, s));
-    F3_CUDA(launch_attention(ws.qkv, T, ws.cat, s));
+    for (int smp = 0; smp < n_samples; ++smp) {   // attention within each sample
+      const int r0 = sample_start[smp];
+      F3_CUDA(launch_attention(ws.qkv + (size_t)r0 * kQkvCols, sample_start[smp + 1] - r0,
+                               ws.cat + (size_t)r0 * kCatCols, s));
+    }
     EpiParams eo{};
     eo.x = x;
     eo.sid = ws.sid;
@@ -867,7 +903,7 @@ struct ModelWs {
   uint8_t *final_ws, *block_ws;
   size_t block_bytes;
 };
-size_t model_ws_layout(const flux3_config *cfg, int T, uint8_t *base, ModelWs *w) {
+size_t model_ws_layout(const flux3_config *cfg, int T, uint8_t *base, ModelWs *w, int n_samples = 1) {
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -875,9 +911,9 @@ size_t model_ws_layout(const flux3_config *cfg, int T, uint8_t *base, ModelWs *w
     return base ? base + o : nullptr;
   };
   uint8_t *x = take((size_t)T * kHidden * 4);
-  uint8_t *e = take((size_t)3 * kModLen * 4);
-  uint8_t *sg = take((size_t)3 * kModLen * 4);
-  uint8_t *f = take((size_t)kModLen * 4);
+  uint8_t *e = take((size_t)3 * n_samples * kModLen * 4);
+  uint8_t *sg = take((size_t)3 * n_samples * kModLen * 4);
+  uint8_t *f = take((size_t)n_samples * kModLen * 4);
   uint8_t *sc = take(kCondScratchFloats * 4);
   uint8_t *fw = take(final_ws_bytes(T));
   const size_t bb = workspace_layout(T, nullptr, nullptr, lowp(cfg->wfmt));
@@ -1040,6 +1076,100 @@ flux3_status flux3_euler_step(float *latent, const float *velocity, size_t n, fl
   if (!latent || !velocity || n == 0) return FLUX3_ERR_INVALID_ARG;
   const float dt = (float)((double)sigma_next - (double)sigma);
   return cuda_status(launch_euler(latent, velocity, n, dt, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+extern "C" {
+
+flux3_status flux3_stack_forward_batch(const flux3_handle *h, int first_block, int n_blocks, float *x, int T,
+                                       const flux3_segment *segs, int n_segs, const int *sample_start, int n_samples,
+                                       const float *pos_ids, const float *mod, void *workspace, size_t ws_bytes,
+                                       void *stream) {
+  if (!sample_start) return FLUX3_ERR_INVALID_ARG;
+  return forward_common(h, first_block, n_blocks, x, T, segs, n_segs, pos_ids, mod, workspace, ws_bytes,
+                        static_cast<cudaStream_t>(stream), sample_start, n_samples);
+}
+
+size_t flux3_transformer_batch_workspace_bytes(const flux3_config *joint_cfg, int T, int n_samples) {
+  if (!config_ok(joint_cfg) || T < 1 || T > joint_cfg->max_tokens || n_samples < 1 || n_samples > FLUX3_MAX_SAMPLES)
+    return 0;
+  return model_ws_layout(joint_cfg, T, nullptr, nullptr, n_samples);
+}
+
+flux3_status flux3_transformer_forward_batch(const flux3_cond *c, const flux3_handle *const *mode_handles,
+                                             int n_mode_blocks, const flux3_handle *joint, const void *const *inputs,
+                                             int T, const flux3_segment *segs, int n_segs, const int *sample_start,
+                                             int n_samples, const float *pos_ids, const float *t, const float *t_next,
+                                             float *velocity, void *workspace, size_t ws_bytes, void *stream) {
+  if (!c || !joint || !pos_ids || !velocity || !workspace || !t || n_mode_blocks < 0 || !inputs)
+    return FLUX3_ERR_INVALID_ARG;
+  if (n_mode_blocks > 0 && !mode_handles) return FLUX3_ERR_INVALID_ARG;
+  if (c->flow && !t_next) return FLUX3_ERR_INVALID_ARG;
+  if (T < 1 || T > joint->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
+  F3_TRY(segments_ok(segs, n_segs, T));
+  int sample_of[FLUX3_MAX_SEGMENTS] = {0};
+  F3_TRY(samples_ok(sample_start, n_samples, T, segs, n_segs, sample_of));
+  for (int b = 0; b < n_samples; ++b) {
+    if (!(t[b] >= 0.f && t[b] <= 1.f) || (c->flow && !(t_next[b] >= 0.f && t_next[b] <= 1.f)))
+      return FLUX3_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n_segs; ++i) {
+    const void *p = inputs[3 * sample_of[i] + segs[i].stream];
+    if (!p) return FLUX3_ERR_INVALID_ARG;
+    if (!aligned16(p)) return FLUX3_ERR_ALIGNMENT;
+  }
+  if (!aligned16(workspace) || !aligned16(velocity) || !aligned16(pos_ids)) return FLUX3_ERR_ALIGNMENT;
+  if (ws_bytes < model_ws_layout(&joint->cfg, T, nullptr, nullptr, n_samples)) return FLUX3_ERR_WORKSPACE;
+  ModelWs w;
+  model_ws_layout(&joint->cfg, T, static_cast<uint8_t *>(workspace), &w, n_samples);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // per sample: conditioning rows 3b.., embedders, per-mode blocks on the sample's rows
+  for (int b = 0; b < n_samples; ++b) {
+    const int r0 = sample_start[b], tb = sample_start[b + 1] - r0;
+    flux3_segment local[FLUX3_MAX_SEGMENTS], absolute[FLUX3_MAX_SEGMENTS];
+    int n = 0;
+    for (int i = 0; i < n_segs; ++i)
+      if (sample_of[i] == b) {
+        absolute[n] = segs[i];
+        local[n] = segs[i];
+        local[n].start -= r0;
+        ++n;
+      }
+    F3_TRY(run_conditioning(c, t[b], c->flow ? t_next[b] : 0.f, w.early + (size_t)3 * b * kModLen,
+                            w.single + (size_t)3 * b * kModLen, w.fin + (size_t)b * kModLen, w.scratch, s));
+    F3_TRY(run_embed(c, inputs + 3 * b, absolute, n, w.x, s));
+    if (n_mode_blocks > 0)
+      F3_TRY(flux3_mode_blocks_forward(mode_handles, n_mode_blocks, w.x + (size_t)r0 * kHidden, tb, local, n,
+                                       pos_ids + (size_t)r0 * 4, w.early + (size_t)3 * b * kModLen, w.block_ws,
+                                       w.block_bytes, stream));
+  }
+  F3_TRY(forward_common(joint, 0, joint->n_blocks, w.x, T, segs, n_segs, pos_ids, w.single, w.block_ws,
+                        w.block_bytes, s, sample_start, n_samples));
+  int img_rows = 0;
+  for (int b = 0; b < n_samples; ++b) {
+    const int r0 = sample_start[b], tb = sample_start[b + 1] - r0;
+    flux3_segment local[FLUX3_MAX_SEGMENTS];
+    int n = 0, n_img = 0;
+    for (int i = 0; i < n_segs; ++i)
+      if (sample_of[i] == b) {
+        local[n] = segs[i];
+        local[n].start -= r0;
+        if (segs[i].stream == FLUX3_STREAM_IMAGE) n_img += segs[i].len;
+        ++n;
+      }
+    F3_TRY(run_final(c, w.x + (size_t)r0 * kHidden, local, n, tb, w.fin + (size_t)b * kModLen,
+                     velocity + (size_t)img_rows * kLatent, w.final_ws, s));
+    img_rows += n_img;
+  }
+  return FLUX3_OK;
+}
+
+flux3_status flux3_cfg_euler_step(float *latent, const float *v_uncond, const float *v_cond, size_t n,
+                                  float guidance, float sigma, float sigma_next, void *stream) {
+  if (!latent || !v_uncond || !v_cond || n == 0) return FLUX3_ERR_INVALID_ARG;
+  const float dt = (float)((double)sigma_next - (double)sigma);
+  return cuda_status(launch_cfg_euler(latent, v_uncond, v_cond, n, guidance, dt, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -11,7 +11,8 @@ from . import (FLUX3_W_BF16, FLUX3_W_FP8R, FLUX3_W_NVFP4, NVFP4_MATRICES, flux3_
                flux3_stack_forward, flux3_workspace_bytes, flux3_cond_packed_bytes, flux3_cond_init,
                flux3_cond_destroy, flux3_cond_workspace_bytes, flux3_conditioning, flux3_embed_tokens,
                flux3_final_layer_workspace_bytes, flux3_final_layer, flux3_transformer_workspace_bytes,
-               flux3_transformer_forward, flux3_sigma_schedule, flux3_euler_step)
+               flux3_transformer_forward, flux3_sigma_schedule, flux3_euler_step, flux3_stack_forward_batch,
+               flux3_transformer_batch_workspace_bytes, flux3_transformer_forward_batch, flux3_cfg_euler_step)
 
 WEIGHT_KEYS = ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out", "query_norm", "key_norm")
 
@@ -254,6 +255,46 @@ class Flux3Transformer:
                                   pos_ids.data_ptr(), float(t), float(t_next), velocity.data_ptr(),
                                   self._ws.data_ptr(), self._ws.numel(), _stream_ptr(stream))
         return velocity
+
+    def forward_batch(self, inputs, segments, sample_start, pos_ids, t, t_next=None, stream=None, velocity=None):
+        """Several samples through flux3_transformer_forward_batch.  inputs: per
+        sample three bf16 tensors (or None); t, t_next: per-sample timesteps;
+        returns the samples' image-token velocities one after the other."""
+        T = pos_ids.shape[0]
+        n = len(sample_start) - 1
+        need = flux3_transformer_batch_workspace_bytes(self.joint.cfg, T, n)
+        if self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.joint.device)
+        n_img = sum(k for _, k, st in segments if st == 0)
+        if velocity is None:
+            velocity = torch.empty((n_img, 128), dtype=torch.float32, device=self.joint.device)
+        ptrs = [[t_.data_ptr() if t_ is not None else None for t_ in per] for per in inputs]
+        tn = t_next if t_next is not None else [0.0] * n
+        flux3_transformer_forward_batch(self.cond.handle, [b.handle if b is not None else None for b in self.mode_blocks],
+                                        self.n_mode_blocks, self.joint.handle, ptrs, T, segments, sample_start,
+                                        pos_ids.data_ptr(), t, tn, velocity.data_ptr(), self._ws.data_ptr(),
+                                        self._ws.numel(), _stream_ptr(stream))
+        return velocity
+
+    def sample_cfg(self, latents, uncond_inputs, cond_inputs, segments, sample_start, pos_ids, steps=50, alpha=6.93,
+                   guidance=3.5, stream=None):
+        """The base model's sampler: per step one call on the two-sample pack
+        [unconditional, conditional] (both samples carry the current latents as
+        their image input) and the guided Euler update of the latents.
+        segments / sample_start / pos_ids describe the pack."""
+        sig = flux3_sigma_schedule(steps, alpha)
+        n_img = latents.shape[0]
+        v = torch.empty((2 * n_img, 128), dtype=torch.float32, device=latents.device)
+        img = torch.empty(latents.shape, dtype=torch.bfloat16, device=latents.device)
+        u = list(uncond_inputs)
+        c = list(cond_inputs)
+        u[0] = c[0] = img
+        for k in range(steps):
+            img.copy_(latents)
+            self.forward_batch([u, c], segments, sample_start, pos_ids, [sig[k], sig[k]], stream=stream, velocity=v)
+            flux3_cfg_euler_step(latents.data_ptr(), v[:n_img].data_ptr(), v[n_img:].data_ptr(), latents.numel(),
+                                 guidance, sig[k], sig[k + 1], _stream_ptr(stream))
+        return latents
 
     def sample(self, latents, inputs, segments, pos_ids, steps=16, alpha=6.93, flow_map=True, stream=None):
         """The flow-map sampler: for k < steps, v = forward(sigma_k, sigma_{k+1})

@@ -392,6 +392,55 @@ FLUX3_API flux3_status flux3_sigma_schedule(int steps, double alpha, float *sigm
 FLUX3_API flux3_status flux3_euler_step(float *latent, const float *velocity, size_t n, float sigma,
                                         float sigma_next, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Several samples in one call: the base model runs classifier-free guidance
+ * on a two-sample pack [empty prompt, prompt] ("FLUX.3 Image Klein support",
+ * comment "Sampling (sampling.py, pipeline.py)"), and attention stays within
+ * a sample ("Structure": tokens attend to the other tokens of the same
+ * sample).  The samples' tokens are concatenated: sample b owns rows
+ * [sample_start[b], sample_start[b+1]).
+ * ------------------------------------------------------------------------ */
+#define FLUX3_MAX_SAMPLES 16
+
+/* flux3_stack_forward over a batch of samples: LayerNorm and both projection
+ * GEMMs run once over all T rows, attention runs per sample.
+ *   sample_start host int [n_samples + 1], 0 = [0] < [1] < ... < [n] = T
+ *   segs         as flux3_block_forward (stream = the token's mode), each
+ *                segment inside one sample
+ *   mod          device float32 [3 * n_samples, 9216]: row 3 b + stream
+ * The rows of each sample come out as a flux3_stack_forward call on that
+ * sample alone would leave them. */
+FLUX3_API flux3_status flux3_stack_forward_batch(const flux3_handle *h, int first_block, int n_blocks, float *x,
+                                                 int T, const flux3_segment *segs, int n_segs,
+                                                 const int *sample_start, int n_samples, const float *pos_ids,
+                                                 const float *mod, void *workspace, size_t ws_bytes, void *stream);
+
+/* Device workspace of flux3_transformer_forward_batch. */
+FLUX3_API size_t flux3_transformer_batch_workspace_bytes(const flux3_config *joint_cfg, int T, int n_samples);
+
+/* flux3_transformer_forward over a batch of samples: conditioning per sample
+ * (t[b], t_next[b]: host float arrays [n_samples]), embedders, per-mode blocks
+ * per sample, the joint blocks batched (flux3_stack_forward_batch), the
+ * output layer per sample.
+ *   inputs    host array [n_samples * 3] of device bf16 pointers: sample b's
+ *             image, image_cond, txt inputs at 3 b + stream
+ *   velocity  device float32 [sum of the samples' image tokens, 128], the
+ *             samples' image tokens one sample after the other */
+FLUX3_API flux3_status flux3_transformer_forward_batch(const flux3_cond *c, const flux3_handle *const *mode_handles,
+                                                       int n_mode_blocks, const flux3_handle *joint,
+                                                       const void *const *inputs, int T, const flux3_segment *segs,
+                                                       int n_segs, const int *sample_start, int n_samples,
+                                                       const float *pos_ids, const float *t, const float *t_next,
+                                                       float *velocity, void *workspace, size_t ws_bytes,
+                                                       void *stream);
+
+/* The guided update: latent[i] += (sigma_next - sigma) * (v_uncond[i] +
+ * guidance (v_cond[i] - v_uncond[i])), i < n (device float32).  The pages
+ * give the pack and the guidance scale (3.5), not the combination; this is
+ * the classifier-free guidance form. */
+FLUX3_API flux3_status flux3_cfg_euler_step(float *latent, const float *v_uncond, const float *v_cond, size_t n,
+                                            float guidance, float sigma, float sigma_next, void *stream);
+
 /* Largest T flux3_block_forward_noalloc accepts (its scratch is ~25 MB). */
 #define FLUX3_NOALLOC_MAX_TOKENS 512
 

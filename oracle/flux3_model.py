@@ -48,7 +48,8 @@ SHIFT = 6.93
 
 __all__ = ["TIME_DIM", "MAX_PERIOD", "TIME_FACTOR", "LATENT_CH", "TXT_FEAT", "SHIFT",
            "timestep_embedding", "mlp_embedder", "stream_vectors", "modulation_vectors", "embed_tokens",
-           "final_layer", "transformer_forward", "sigma_schedule", "euler_step"]
+           "final_layer", "transformer_forward", "sigma_schedule", "euler_step", "stack_forward_batch",
+           "cfg_velocity", "cfg_euler_step", "transformer_forward_batch"]
 
 
 def timestep_embedding(t, dim=TIME_DIM, max_period=MAX_PERIOD, time_factor=TIME_FACTOR):
@@ -136,3 +137,44 @@ def sigma_schedule(steps, alpha=SHIFT):
 
 def euler_step(x, v, sigma, sigma_next):
     return np.asarray(x, np.float64) + (sigma_next - sigma) * np.asarray(v, np.float64)
+
+
+# --------------------------------------------------------------------------
+# Several samples in one call: the base model's classifier-free guidance on a
+# two-sample pack [empty prompt, prompt] ("Sampling (sampling.py,
+# pipeline.py)"); attention stays within a sample ("Structure": tokens attend
+# to each other per sample).  The guidance combination is a reading: the pages
+# give the pack and the scale (3.5), not the formula; this is the usual
+# classifier-free guidance form.
+# --------------------------------------------------------------------------
+def stack_forward_batch(x, blocks, mods, sample_id, stream_id, pos):
+    """Joint blocks over concatenated samples: each sample's rows run through
+    the blocks as a sequence of their own, a token's modulation row being
+    mods[3 * sample + stream]."""
+    x = np.array(x, dtype=np.float64)
+    sample_id = np.asarray(sample_id)
+    stream_id = np.asarray(stream_id)
+    pos = np.asarray(pos, np.float64)
+    mods = np.asarray(mods, np.float64)
+    blocks = list(blocks)
+    for b in np.unique(sample_id):
+        idx = np.nonzero(sample_id == b)[0]
+        x[idx] = stack_forward(x[idx], blocks, mods[3 * b:3 * b + 3], stream_id[idx], pos[idx])
+    return x
+
+
+def cfg_velocity(v_uncond, v_cond, guidance):
+    v_uncond = np.asarray(v_uncond, np.float64)
+    return v_uncond + guidance * (np.asarray(v_cond, np.float64) - v_uncond)
+
+
+def cfg_euler_step(x, v_uncond, v_cond, guidance, sigma, sigma_next):
+    return euler_step(x, cfg_velocity(v_uncond, v_cond, guidance), sigma, sigma_next)
+
+
+def transformer_forward_batch(samples, t, t_next, cond, mode_blocks, joint_blocks):
+    """samples: per sample (inputs, stream_id, pos); t, t_next per sample.
+    Each sample is one transformer call of its own; the velocities of the
+    samples' image tokens are returned one sample after the other."""
+    return np.concatenate([transformer_forward(ins, sid, pos, t[b], t_next[b], cond, mode_blocks, joint_blocks)
+                           for b, (ins, sid, pos) in enumerate(samples)])

@@ -80,6 +80,35 @@ def build_layout(spec, l_offset=0.0):
     return Layout(segments, pos, sid)
 
 
+@dataclass
+class Pack:
+    """Several samples concatenated: layouts[b] is sample b's own layout;
+    segments, pos, stream_id cover the whole pack; sample_start [n + 1];
+    sample_id [T]."""
+    layouts: list
+    segments: list
+    pos: np.ndarray
+    stream_id: np.ndarray = field(repr=False)
+    sample_id: np.ndarray = field(repr=False)
+    sample_start: list = field(default_factory=list)
+
+    @property
+    def T(self):
+        return int(self.pos.shape[0])
+
+
+def build_pack(specs):
+    """One layout per spec, concatenated sample after sample."""
+    lays = [build_layout(sp) for sp in specs]
+    segments, starts, off = [], [0], 0
+    for lay in lays:
+        segments += [(s0 + off, n, st) for s0, n, st in lay.segments]
+        off += lay.T
+        starts.append(off)
+    return Pack(lays, segments, np.concatenate([l.pos for l in lays]), np.concatenate([l.stream_id for l in lays]),
+                np.concatenate([np.full(l.T, b, np.int64) for b, l in enumerate(lays)]), starts)
+
+
 # The benchmark and parity workloads (text padded to a multiple of 80 by the
 # pipeline is only a sizing rule; these use the stated counts).
 WORKLOADS = {
@@ -106,6 +135,10 @@ WORKLOADS = {
     # (conditioning, embedders, 5 per-mode blocks, 28 joint blocks, output layer) and the Euler update
     "sample16_1024sq_t4608": dict(spec=[("txt", 512), ("image", (64, 64))], blocks=28, calls=16, wfmt="bf16",
                                   stage="model", mode_blocks=5),
+    # the base model's 50-step sampler with guidance on the two-sample pack
+    # [empty prompt (80 padded text tokens) | prompt (160)], both with the 1024x1024 image
+    "cfg50_1024sq_pack2": dict(specs=[[("txt", 80), ("image", (64, 64))], [("txt", 160), ("image", (64, 64))]],
+                               blocks=28, calls=50, wfmt="bf16", stage="cfg", mode_blocks=5),
     # 28-block stack, row-wise FP8 weights, 1024x1024 + one 1024x1024 reference
     "stack28_fp8r_1024sq_ref1_t8704": dict(spec=[("txt", 512), ("image", (64, 64)), ("image_cond", (64, 64))],
                                            blocks=28, calls=1, wfmt="fp8r"),

@@ -1,0 +1,141 @@
+"""Batches of samples: the joint blocks over a concatenated pack with
+attention per sample (flux3_stack_forward_batch), the batched transformer call
+(flux3_transformer_forward_batch) and the guided Euler update
+(flux3_cfg_euler_step), against the oracle (oracle/flux3_model.py) and against
+per-sample calls.  No GPU value ever feeds the oracle."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import diffusion_transformer_block_fwd_b300 as F3
+import oracle as O
+import synth
+from _f3 import DEV, assert_block_output, assert_close, f64, weights_f64
+from oracle import flux3_model as M
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [[("txt", 32), ("image", (8, 8))], [("txt", 37), ("image", (9, 11)), ("image_cond", (5, 7))]]
+T2I_PACK = synth.WORKLOADS["cfg50_1024sq_pack2"]["specs"]
+
+
+def _sync_ok():
+    assert F3.flux3_check_error(torch.cuda.current_stream().cuda_stream) == 0
+
+
+def _batch(blocks, pack, x, mods, first=0, n=None):
+    n = blocks.n_blocks - first if n is None else n
+    ws = blocks.workspace(pack.T)
+    pos = torch.from_numpy(pack.pos).to(DEV)
+    F3.flux3_stack_forward_batch(blocks.handle, first, n, x.data_ptr(), pack.T, pack.segments, pack.sample_start,
+                                 pos.data_ptr(), mods.data_ptr(), ws.data_ptr(), ws.numel(),
+                                 torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.fixture(scope="module")
+def joint3():
+    ws = [synth.block_weights(8100, b, device=DEV) for b in range(3)]
+    return ws, F3.Flux3Blocks(ws, max_tokens=16384)
+
+
+def test_batch_block_against_oracle(joint3):
+    ws, blocks = joint3
+    pack = synth.build_pack(SMALL)
+    x = synth.activations(81, pack.T, device=DEV)
+    mods = torch.cat([synth.modulation(81, call=b, device=DEV) for b in range(2)])   # [6, 9216]
+    y = x.clone()
+    _batch(blocks, pack, y, mods, 0, 1)
+    _sync_ok()
+    m64 = f64(mods)
+    ref = M.stack_forward_batch(f64(x), [weights_f64(ws[0])], m64, pack.sample_id, pack.stream_id,
+                                pack.pos.astype(np.float64))
+    for b in range(2):
+        r = pack.sample_id == b
+        lay = pack.layouts[b]
+        parts = O.single_block_parts(f64(x)[r], weights_f64(ws[0]), m64[3 * b:3 * b + 3], lay.stream_id,
+                                     lay.pos.astype(np.float64))
+        np.testing.assert_allclose(parts["out"], ref[r], rtol=1e-12, atol=1e-12)
+        assert_block_output(f64(y)[r], ref[r], f64(x)[r], m64[3 * b + lay.stream_id, 6144:], parts["y"],
+                            f"sample {b}")
+
+
+def test_batch_equals_per_sample_calls_full_size(joint3):
+    """The text-to-image CFG pack [80 + 64x64 | 160 + 64x64] (8432 tokens):
+    the batched blocks leave each sample's rows exactly as a call on that
+    sample alone."""
+    _, blocks = joint3
+    pack = synth.build_pack(T2I_PACK)
+    x = synth.activations(82, pack.T, device=DEV)
+    mods = torch.cat([synth.modulation(82, call=b, device=DEV) for b in range(2)])
+    a = x.clone()
+    _batch(blocks, pack, a, mods)
+    _sync_ok()
+    for b in range(2):
+        r0, r1 = pack.sample_start[b], pack.sample_start[b + 1]
+        lay = pack.layouts[b]
+        sub = x[r0:r1].clone()
+        blocks.forward(sub, lay.segments, torch.from_numpy(lay.pos).to(DEV), mods[3 * b:3 * b + 3].contiguous())
+        _sync_ok()
+        assert torch.equal(a[r0:r1], sub), f"sample {b}"
+
+
+def test_batch_rejects_bad_sample_tables(joint3):
+    _, blocks = joint3
+    pack = synth.build_pack(SMALL)
+    x = synth.activations(83, pack.T, device=DEV)
+    mods = torch.zeros((6, 9216), device=DEV)
+    pos = torch.from_numpy(pack.pos).to(DEV)
+    ws = blocks.workspace(pack.T)
+    L = F3.lib()
+    segs = F3.segments_array(pack.segments)
+    for starts in ([1, 96, pack.T], [0, 96, pack.T - 1], [0, 0, pack.T], [0, 90, pack.T]):   # last: splits a segment
+        arr = (ctypes.c_int * 3)(*starts)
+        st = L.flux3_stack_forward_batch(blocks.handle, 0, 1, x.data_ptr(), pack.T, segs, len(pack.segments), arr, 2,
+                                         pos.data_ptr(), mods.data_ptr(), ws.data_ptr(), ws.numel(), None)
+        assert st == F3.FLUX3_ERR_INVALID_ARG, starts
+
+
+def test_cfg_euler_step():
+    u = synth.activations(84, 32, device=DEV)[:, :128].contiguous()
+    c = synth.activations(85, 32, device=DEV)[:, :128].contiguous()
+    lat = synth.activations(86, 32, device=DEV)[:, :128].contiguous()
+    sig = F3.flux3_sigma_schedule(50)
+    x = lat.clone()
+    F3.flux3_cfg_euler_step(x.data_ptr(), u.data_ptr(), c.data_ptr(), x.numel(), 3.5, sig[7], sig[8])
+    _sync_ok()
+    ref = M.cfg_euler_step(f64(lat), f64(u), f64(c), 3.5, float(np.float64(sig[7])), float(np.float64(sig[8])))
+    np.testing.assert_allclose(f64(x), ref, rtol=2e-6, atol=2e-6)
+
+
+def test_transformer_batch_against_oracle_and_per_sample():
+    """The base model (no flow-map timestep) on a small two-sample pack: 1
+    per-mode block, 2 joint blocks, against the oracle's per-sample calls; and
+    the batched call equals per-sample calls bit for bit."""
+    w = synth.cond_weights(880, device=DEV, flow=False)
+    c = F3.Flux3Conditioning(w)
+    w64 = {k: (None if v is None else [f64(t) for t in v] if isinstance(v, list) else f64(v)) for k, v in w.items()}
+    pack = synth.build_pack(SMALL)
+    mw = [[synth.block_weights(8800 + m, 0, device=DEV)] for m in range(3)]
+    jw = [synth.block_weights(8900, b, device=DEV) for b in range(2)]
+    mb = [F3.Flux3Blocks(mw[m], max_tokens=512) for m in range(3)]
+    joint = F3.Flux3Blocks(jw, max_tokens=1024)
+    model = F3.Flux3Transformer(c, mb, joint)
+    ins = [synth.stream_inputs(87 + b, lay, device=DEV) for b, lay in enumerate(pack.layouts)]
+    pos = torch.from_numpy(pack.pos).to(DEV)
+    t = [0.62, 0.62]
+    v = model.forward_batch(ins, pack.segments, pack.sample_start, pos, t)
+    _sync_ok()
+    samples = [([f64(i) if i is not None else None for i in ins[b]], lay.stream_id, lay.pos.astype(np.float64))
+               for b, lay in enumerate(pack.layouts)]
+    ref = M.transformer_forward_batch(samples, t, [0.0, 0.0], w64, [[weights_f64(mw[m][0])] for m in range(3)],
+                                      [weights_f64(b) for b in jw])
+    assert_close(f64(v), ref, 2e-2, 0.9995, "pack velocity")
+    rows = 0
+    for b, lay in enumerate(pack.layouts):
+        vb = model.forward(ins[b], lay.segments, torch.from_numpy(lay.pos).to(DEV), t[b])
+        _sync_ok()
+        assert torch.equal(v[rows:rows + vb.shape[0]], vb), f"sample {b}"
+        rows += vb.shape[0]

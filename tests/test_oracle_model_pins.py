@@ -155,3 +155,79 @@ def test_transformer_output_is_the_image_tokens_only():
     assert not np.allclose(M.transformer_forward(ins2, sid, pos, 0.7, 0.5, c, mode_blocks, joint), v)
     assert np.array_equal(M.transformer_forward(ins2, sid, pos, 0.7, 0.5, c, mode_blocks, []),
                           M.transformer_forward(ins, sid, pos, 0.7, 0.5, c, mode_blocks, []))
+
+
+# --------------------------------------------------------------------------
+# Batches of samples (the base model's CFG pack)
+# --------------------------------------------------------------------------
+def _torch_batch_block(x, w, mods, sample_id, sid, pos):
+    """One joint block over concatenated samples in one pass: attention with a
+    block-diagonal boolean mask by sample (scaled_dot_product_attention), each
+    token's modulation row 3 * sample + stream.  fp64 torch."""
+    from test_oracle_pins import _torch_block   # noqa: F401  (same block, restated with a mask below)
+    T, D = x.shape
+    d = len(w["query_norm"])
+    H = D // d
+    tx = _t(x)
+    rows = torch.from_numpy(3 * sample_id + sid).long()
+    tm = _t(mods)[rows]
+    shift, scale, gate = tm[:, :D], tm[:, D:2 * D], tm[:, 2 * D:]
+    h = (1 + scale) * F.layer_norm(tx, (D,), eps=1e-6) + shift
+    W = {k: _t(v) for k, v in w.items()}
+    q, k, v = (F.linear(h, W[n]).view(T, H, d) for n in ("q_proj", "k_proj", "v_proj"))
+
+    def rms(t_, s_):
+        return t_ * torch.rsqrt(t_.pow(2).mean(-1, keepdim=True) + 1e-6) * s_
+
+    n = d // 4
+    freqs = torch.cat([1e4 ** (-torch.arange(0, n, 2, dtype=torch.float64) / n)] * 4)
+    axis = torch.arange(d // 2) // (n // 2)
+    rot = torch.polar(torch.ones(T, d // 2, dtype=torch.float64), _t(pos)[:, axis] * freqs)[:, None, :]
+
+    def rope(t_):
+        return torch.view_as_real(torch.view_as_complex(t_.reshape(T, H, d // 2, 2).contiguous()) * rot).reshape(T, H, d)
+
+    q, k = rope(rms(q, W["query_norm"])), rope(rms(k, W["key_norm"]))
+    smp = torch.from_numpy(sample_id)
+    o = F.scaled_dot_product_attention(q.transpose(0, 1), k.transpose(0, 1), v.transpose(0, 1),
+                                       attn_mask=smp[:, None] == smp[None, :]).transpose(0, 1).reshape(T, D)
+    a, b = F.linear(h, W["mlp_in"]).chunk(2, dim=-1)
+    return (tx + gate * (F.linear(o, W["attn_out"]) + F.linear(F.silu(a) * b, W["mlp_out"]))).numpy()
+
+
+def test_batch_matches_sample_masked_restatement():
+    from test_oracle_pins import _tiny_block, _tiny_inputs
+    rng = _rng(20)
+    ws = [_tiny_block(rng) for _ in range(2)]
+    x, _, sid, pos = _tiny_inputs(rng, T=15)
+    sample_id = np.array([0] * 6 + [1] * 9)
+    mods = 0.3 * rng.standard_normal((6, 96))
+    y = x
+    for w in ws:
+        y = _torch_batch_block(y, w, mods, sample_id, sid, pos)
+    np.testing.assert_allclose(M.stack_forward_batch(x, ws, mods, sample_id, sid, pos), y, rtol=1e-9, atol=1e-10)
+
+
+def test_batch_samples_are_isolated():
+    from test_oracle_pins import _tiny_block, _tiny_inputs
+    rng = _rng(21)
+    ws = [_tiny_block(rng)]
+    x, _, sid, pos = _tiny_inputs(rng, T=12)
+    sample_id = np.array([0] * 5 + [1] * 7)
+    mods = 0.3 * rng.standard_normal((6, 96))
+    out = M.stack_forward_batch(x, ws, mods, sample_id, sid, pos)
+    x2, m2 = x.copy(), mods.copy()
+    x2[:5] += 1.0
+    m2[:3] += 0.5                                            # sample 0's inputs and modulation only
+    out2 = M.stack_forward_batch(x2, ws, m2, sample_id, sid, pos)
+    assert np.array_equal(out[5:], out2[5:])
+    assert np.all(np.any(out[:5] != out2[:5], axis=1))
+
+
+def test_cfg_closed_forms():
+    rng = _rng(22)
+    u, c, x = rng.standard_normal((3, 40))
+    np.testing.assert_allclose(M.cfg_velocity(u, c, 1.0), c, rtol=0, atol=1e-15)
+    assert np.array_equal(M.cfg_velocity(u, c, 0.0), u)
+    np.testing.assert_allclose(M.cfg_velocity(u, c, 3.5), 3.5 * c - 2.5 * u, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(M.cfg_euler_step(x, u, c, 1.0, 0.8, 0.5), x - 0.3 * c, rtol=1e-14, atol=1e-14)
