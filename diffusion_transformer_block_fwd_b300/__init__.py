@@ -44,7 +44,7 @@ EXPORTED = (
     "flux3_conditioning", "flux3_embed_tokens", "flux3_final_layer_workspace_bytes", "flux3_final_layer",
     "flux3_transformer_workspace_bytes", "flux3_transformer_forward", "flux3_sigma_schedule", "flux3_euler_step",
     "flux3_stack_forward_batch", "flux3_transformer_batch_workspace_bytes", "flux3_transformer_forward_batch",
-    "flux3_cfg_euler_step",
+    "flux3_cfg_euler_step", "flux3_latents_to_bf16",
 )
 
 
@@ -156,13 +156,14 @@ def lib():
             "flux3_transformer_forward": (i, [vp, ctypes.POINTER(vp), i, vp, ctypes.POINTER(vp), i, segp, i, vp, f, f,
                                               vp, vp, sz, vp]),
             "flux3_sigma_schedule": (i, [i, ctypes.c_double, ctypes.POINTER(ctypes.c_float)]),
-            "flux3_euler_step": (i, [vp, vp, sz, f, f, vp]),
+            "flux3_euler_step": (i, [vp, vp, sz, f, f, vp, vp]),
+            "flux3_latents_to_bf16": (i, [vp, sz, vp, vp]),
             "flux3_stack_forward_batch": (i, [vp, i, i, vp, i, segp, i, ctypes.POINTER(i), i, vp, vp, vp, sz, vp]),
             "flux3_transformer_batch_workspace_bytes": (sz, [cfgp, i, i]),
             "flux3_transformer_forward_batch": (i, [vp, ctypes.POINTER(vp), i, vp, ctypes.POINTER(vp), i, segp, i,
                                                     ctypes.POINTER(i), i, vp, ctypes.POINTER(f), ctypes.POINTER(f),
                                                     vp, vp, sz, vp]),
-            "flux3_cfg_euler_step": (i, [vp, vp, vp, sz, f, f, f, vp]),
+            "flux3_cfg_euler_step": (i, [vp, vp, vp, sz, f, f, f, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -332,8 +333,12 @@ def flux3_sigma_schedule(steps, alpha=6.93):
     return list(out)
 
 
-def flux3_euler_step(latent, velocity, n, sigma, sigma_next, stream=0):
-    _check(lib().flux3_euler_step(latent, velocity, n, sigma, sigma_next, stream), "flux3_euler_step")
+def flux3_euler_step(latent, velocity, n, sigma, sigma_next, next_input=None, stream=0):
+    _check(lib().flux3_euler_step(latent, velocity, n, sigma, sigma_next, next_input, stream), "flux3_euler_step")
+
+
+def flux3_latents_to_bf16(latent, n, inp, stream=0):
+    _check(lib().flux3_latents_to_bf16(latent, n, inp, stream), "flux3_latents_to_bf16")
 
 
 def _ints(v):
@@ -369,8 +374,8 @@ def flux3_transformer_forward_batch(c, mode_handles, n_mode_blocks, joint, input
            "flux3_transformer_forward_batch")
 
 
-def flux3_cfg_euler_step(latent, v_uncond, v_cond, n, guidance, sigma, sigma_next, stream=0):
-    _check(lib().flux3_cfg_euler_step(latent, v_uncond, v_cond, n, guidance, sigma, sigma_next, stream),
+def flux3_cfg_euler_step(latent, v_uncond, v_cond, n, guidance, sigma, sigma_next, next_input=None, stream=0):
+    _check(lib().flux3_cfg_euler_step(latent, v_uncond, v_cond, n, guidance, sigma, sigma_next, next_input, stream),
            "flux3_cfg_euler_step")
 
 

@@ -11,8 +11,10 @@
 //                          warp per output, the activated rows in shared
 //                          memory)
 //   add_row_kernel         y[m] += r for the flow-map timestep term
-//   euler_kernel           latent += (sigma_next - sigma) * velocity
+//   euler_kernel           latent += (sigma_next - sigma) * velocity, and the
+//                          new latent rounded to bf16 (the next call's input)
 //   cfg_euler_kernel       the same with v = v_uncond + g (v_cond - v_uncond)
+//   to_bf16_kernel         the first call's input from the initial latents
 
 #pragma once
 
@@ -92,17 +94,30 @@ __global__ void add_row_kernel(float *__restrict__ y, int ldy, int M, const floa
   if (i < M * n) y[(size_t)(i / n) * ldy + i % n] += r[i % n];
 }
 
-__global__ void euler_kernel(float *__restrict__ latent, const float *__restrict__ v, size_t n, float dt) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-    latent[i] = fmaf(dt, v[i], latent[i]);
+// The updates also write the new latent's bf16 rounding (the next call's
+// image input) when `next_in` is given.
+__global__ void euler_kernel(float *__restrict__ latent, const float *__restrict__ v, size_t n, float dt,
+                             __nv_bfloat16 *__restrict__ next_in) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float y = fmaf(dt, v[i], latent[i]);
+    latent[i] = y;
+    if (next_in) next_in[i] = __float2bfloat16_rn(y);
+  }
 }
 
 __global__ void cfg_euler_kernel(float *__restrict__ latent, const float *__restrict__ vu, const float *__restrict__ vc,
-                                 size_t n, float g, float dt) {
+                                 size_t n, float g, float dt, __nv_bfloat16 *__restrict__ next_in) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
     const float u = vu[i];
-    latent[i] = fmaf(dt, fmaf(g, vc[i] - u, u), latent[i]);
+    const float y = fmaf(dt, fmaf(g, vc[i] - u, u), latent[i]);
+    latent[i] = y;
+    if (next_in) next_in[i] = __float2bfloat16_rn(y);
   }
+}
+
+__global__ void to_bf16_kernel(const float *__restrict__ src, size_t n, __nv_bfloat16 *__restrict__ dst) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = __float2bfloat16_rn(src[i]);
 }
 
 }  // namespace cond_detail
@@ -135,16 +150,22 @@ cudaError_t launch_add_row(float *y, int ldy, int M, const float *r, int n, cuda
   return cudaGetLastError();
 }
 
-cudaError_t launch_euler(float *latent, const float *v, size_t n, float dt, cudaStream_t s) {
+cudaError_t launch_euler(float *latent, const float *v, size_t n, float dt, __nv_bfloat16 *next_in, cudaStream_t s) {
   const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
-  cond_detail::euler_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(latent, v, n, dt);
+  cond_detail::euler_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(latent, v, n, dt, next_in);
   return cudaGetLastError();
 }
 
 cudaError_t launch_cfg_euler(float *latent, const float *vu, const float *vc, size_t n, float g, float dt,
-                             cudaStream_t s) {
+                             __nv_bfloat16 *next_in, cudaStream_t s) {
   const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
-  cond_detail::cfg_euler_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(latent, vu, vc, n, g, dt);
+  cond_detail::cfg_euler_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(latent, vu, vc, n, g, dt, next_in);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16(const float *src, size_t n, __nv_bfloat16 *dst, cudaStream_t s) {
+  const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8);
+  cond_detail::to_bf16_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(src, n, dst);
   return cudaGetLastError();
 }
 

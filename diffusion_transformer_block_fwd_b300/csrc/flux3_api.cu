@@ -1072,10 +1072,16 @@ flux3_status flux3_sigma_schedule(int steps, double alpha, float *sigmas) {
 }
 
 flux3_status flux3_euler_step(float *latent, const float *velocity, size_t n, float sigma, float sigma_next,
-                              void *stream) {
+                              void *next_input, void *stream) {
   if (!latent || !velocity || n == 0) return FLUX3_ERR_INVALID_ARG;
   const float dt = (float)((double)sigma_next - (double)sigma);
-  return cuda_status(launch_euler(latent, velocity, n, dt, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_euler(latent, velocity, n, dt, static_cast<__nv_bfloat16 *>(next_input),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_latents_to_bf16(const float *latent, size_t n, void *input, void *stream) {
+  if (!latent || !input || n == 0) return FLUX3_ERR_INVALID_ARG;
+  return cuda_status(launch_to_bf16(latent, n, static_cast<__nv_bfloat16 *>(input), static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -1166,10 +1172,11 @@ flux3_status flux3_transformer_forward_batch(const flux3_cond *c, const flux3_ha
 }
 
 flux3_status flux3_cfg_euler_step(float *latent, const float *v_uncond, const float *v_cond, size_t n,
-                                  float guidance, float sigma, float sigma_next, void *stream) {
+                                  float guidance, float sigma, float sigma_next, void *next_input, void *stream) {
   if (!latent || !v_uncond || !v_cond || n == 0) return FLUX3_ERR_INVALID_ARG;
   const float dt = (float)((double)sigma_next - (double)sigma);
-  return cuda_status(launch_cfg_euler(latent, v_uncond, v_cond, n, guidance, dt, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_cfg_euler(latent, v_uncond, v_cond, n, guidance, dt,
+                                      static_cast<__nv_bfloat16 *>(next_input), static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

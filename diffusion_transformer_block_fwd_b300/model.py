@@ -12,7 +12,8 @@ from . import (FLUX3_W_BF16, FLUX3_W_FP8R, FLUX3_W_NVFP4, NVFP4_MATRICES, flux3_
                flux3_cond_destroy, flux3_cond_workspace_bytes, flux3_conditioning, flux3_embed_tokens,
                flux3_final_layer_workspace_bytes, flux3_final_layer, flux3_transformer_workspace_bytes,
                flux3_transformer_forward, flux3_sigma_schedule, flux3_euler_step, flux3_stack_forward_batch,
-               flux3_transformer_batch_workspace_bytes, flux3_transformer_forward_batch, flux3_cfg_euler_step)
+               flux3_transformer_batch_workspace_bytes, flux3_transformer_forward_batch, flux3_cfg_euler_step,
+               flux3_latents_to_bf16)
 
 WEIGHT_KEYS = ("q_proj", "k_proj", "v_proj", "attn_out", "mlp_in", "mlp_out", "query_norm", "key_norm")
 
@@ -284,31 +285,32 @@ class Flux3Transformer:
         segments / sample_start / pos_ids describe the pack."""
         sig = flux3_sigma_schedule(steps, alpha)
         n_img = latents.shape[0]
+        sp = _stream_ptr(stream)
         v = torch.empty((2 * n_img, 128), dtype=torch.float32, device=latents.device)
         img = torch.empty(latents.shape, dtype=torch.bfloat16, device=latents.device)
         u = list(uncond_inputs)
         c = list(cond_inputs)
         u[0] = c[0] = img
+        flux3_latents_to_bf16(latents.data_ptr(), latents.numel(), img.data_ptr(), sp)
         for k in range(steps):
-            img.copy_(latents)
             self.forward_batch([u, c], segments, sample_start, pos_ids, [sig[k], sig[k]], stream=stream, velocity=v)
             flux3_cfg_euler_step(latents.data_ptr(), v[:n_img].data_ptr(), v[n_img:].data_ptr(), latents.numel(),
-                                 guidance, sig[k], sig[k + 1], _stream_ptr(stream))
+                                 guidance, sig[k], sig[k + 1], img.data_ptr(), sp)
         return latents
 
     def sample(self, latents, inputs, segments, pos_ids, steps=16, alpha=6.93, flow_map=True, stream=None):
         """The flow-map sampler: for k < steps, v = forward(sigma_k, sigma_{k+1})
-        on the current latents (bf16 copy as the image input), then
-        latents += (sigma_{k+1} - sigma_k) v.  latents: float32 [T_image, 128],
-        updated in place."""
+        on the current latents (their bf16 rounding, written by the library, is
+        the image input), then latents += (sigma_{k+1} - sigma_k) v.  latents:
+        float32 [T_image, 128], updated in place."""
         sig = flux3_sigma_schedule(steps, alpha)
+        sp = _stream_ptr(stream)
         v = torch.empty_like(latents)
         img = torch.empty(latents.shape, dtype=torch.bfloat16, device=latents.device)
         ins = list(inputs)
         ins[0] = img
+        flux3_latents_to_bf16(latents.data_ptr(), latents.numel(), img.data_ptr(), sp)
         for k in range(steps):
-            img.copy_(latents)
             self.forward(ins, segments, pos_ids, sig[k], sig[k + 1] if flow_map else 0.0, stream=stream, velocity=v)
-            flux3_euler_step(latents.data_ptr(), v.data_ptr(), latents.numel(), sig[k], sig[k + 1],
-                             _stream_ptr(stream))
+            flux3_euler_step(latents.data_ptr(), v.data_ptr(), latents.numel(), sig[k], sig[k + 1], img.data_ptr(), sp)
         return latents

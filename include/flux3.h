@@ -388,9 +388,14 @@ FLUX3_API flux3_status flux3_sigma_schedule(int steps, double alpha, float *sigm
 
 /* latent[i] += (sigma_next - sigma) * velocity[i], i < n (device float32; the
  * difference is taken in double and rounded to float, the update is one fused
- * multiply-add). */
+ * multiply-add).  next_input (device bf16 [n], or NULL): also receives the new
+ * latent rounded to bf16, the image input of the next call. */
 FLUX3_API flux3_status flux3_euler_step(float *latent, const float *velocity, size_t n, float sigma,
-                                        float sigma_next, void *stream);
+                                        float sigma_next, void *next_input, void *stream);
+
+/* input[i] = bf16 rounding (nearest even) of latent[i], i < n: the first call's
+ * image input from the initial latents. */
+FLUX3_API flux3_status flux3_latents_to_bf16(const float *latent, size_t n, void *input, void *stream);
 
 /* ------------------------------------------------------------------------
  * Several samples in one call: the base model runs classifier-free guidance
@@ -437,9 +442,10 @@ FLUX3_API flux3_status flux3_transformer_forward_batch(const flux3_cond *c, cons
 /* The guided update: latent[i] += (sigma_next - sigma) * (v_uncond[i] +
  * guidance (v_cond[i] - v_uncond[i])), i < n (device float32).  The pages
  * give the pack and the guidance scale (3.5), not the combination; this is
- * the classifier-free guidance form. */
+ * the classifier-free guidance form.  next_input as for flux3_euler_step. */
 FLUX3_API flux3_status flux3_cfg_euler_step(float *latent, const float *v_uncond, const float *v_cond, size_t n,
-                                            float guidance, float sigma, float sigma_next, void *stream);
+                                            float guidance, float sigma, float sigma_next, void *next_input,
+                                            void *stream);
 
 /* Largest T flux3_block_forward_noalloc accepts (its scratch is ~25 MB). */
 #define FLUX3_NOALLOC_MAX_TOKENS 512

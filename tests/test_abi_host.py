@@ -256,8 +256,11 @@ def test_model_entry_points_validation_before_any_launch():
     assert L.flux3_final_layer(None, 16, 8, segs, n, 16, 16, 16, 1 << 20, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_transformer_forward(None, None, 0, None, ins, 8, segs, n, 16, ctypes.c_float(0.5),
                                        ctypes.c_float(0.4), 16, 16, 1 << 20, None) == F3.FLUX3_ERR_INVALID_ARG
-    assert L.flux3_euler_step(None, 16, 8, ctypes.c_float(1.0), ctypes.c_float(0.9), None) == \
+    assert L.flux3_euler_step(None, 16, 8, ctypes.c_float(1.0), ctypes.c_float(0.9), None, None) == \
         F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_latents_to_bf16(None, 8, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_cfg_euler_step(16, None, 16, 8, ctypes.c_float(3.5), ctypes.c_float(1.0), ctypes.c_float(0.9),
+                                  None, None) == F3.FLUX3_ERR_INVALID_ARG
     cfg = F3.flux3_default_config()
     assert F3.flux3_transformer_workspace_bytes(cfg, 4608) > F3.flux3_workspace_bytes(cfg, 4608) + 4608 * 3072 * 4
     assert F3.flux3_transformer_workspace_bytes(cfg, 0) == 0

@@ -92,11 +92,17 @@ def test_euler_step():
     v = synth.activations(74, 64, device=DEV)[:, :128].contiguous()
     sig = F3.flux3_sigma_schedule(16)
     x = lat.clone()
-    F3.flux3_euler_step(x.data_ptr(), v.data_ptr(), x.numel(), sig[3], sig[4])
+    nxt = torch.empty(x.shape, dtype=torch.bfloat16, device=DEV)
+    F3.flux3_euler_step(x.data_ptr(), v.data_ptr(), x.numel(), sig[3], sig[4], nxt.data_ptr())
     _sync_ok()
     dt = np.float32(np.float64(sig[4]) - np.float64(sig[3]))
     want = (f64(lat) + np.float64(dt) * f64(v)).astype(np.float32)     # one rounding: fused multiply-add
     assert np.array_equal(x.cpu().numpy(), want)
+    assert torch.equal(nxt.cpu(), torch.from_numpy(want).to(torch.bfloat16))   # the next input: nearest-even bf16
+    first = torch.empty(x.shape, dtype=torch.bfloat16, device=DEV)
+    F3.flux3_latents_to_bf16(lat.data_ptr(), lat.numel(), first.data_ptr())
+    _sync_ok()
+    assert torch.equal(first.cpu(), lat.cpu().to(torch.bfloat16))
 
 
 def test_transformer_small_against_oracle(cond):
