@@ -153,7 +153,8 @@ def test_attention(T, q_scale):
     assert torch.isnan(cat[:, 3072:].float()).all(), "SwiGLU columns must be left untouched"
 
 
-@pytest.mark.parametrize("T", [4608, 8704, 16384])
+# 4256 = 160 text + 64x64 image tokens, the pages' text-to-image count per call (a ragged last key tile)
+@pytest.mark.parametrize("T", [4256, 4608, 8704, 16384])
 def test_attention_full_size_sampled_rows(T):
     qkv = _qkv_inputs(T, 31, 3.0)
     cat = torch.empty((T, 12288), dtype=torch.bfloat16, device=DEV)
