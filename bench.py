@@ -196,7 +196,8 @@ def run_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return
     import synth
-    spec = synth.WORKLOADS[args.workload]["spec"]
+    wl = synth.WORKLOADS[args.workload]
+    spec = wl["spec"] if "spec" in wl else wl["specs"][-1]   # a pack: the conditional sample's layout
     s = OracleSample(spec)
     for _ in range(args.warmup):
         s.run()
