@@ -15,6 +15,13 @@
  * dit.py)" and its tensor list; "Welcome FLUX.3 Image Klein in Diffusers",
  * sections "Inside one block", "Two stages" and "Positions in four dimensions".
  *
+ * Around the joint blocks the library also runs the 5 per-mode blocks (each
+ * mode through its own weights, attention within the mode), weights stored
+ * in NVFP4 or row-wise FP8, one whole transformer call (timestep
+ * conditioning, embedders, both block stages, the image output layer), the
+ * sampler updates, and batches of samples with attention per sample (the base
+ * model's guided two-sample pack).  Each declaration below cites its passage.
+ *
  * Conventions for every entry point:
  *   - Device pointers are CUDA device addresses on the current device; host
  *     pointers are ordinary process memory.  Each argument says which.
@@ -22,8 +29,9 @@
  *     Every call is asynchronous on it; nothing synchronises except
  *     flux3_check_error().
  *   - All device memory (weights, packed weights, activations, workspace) is
- *     owned by the caller.  Weights are borrowed by flux3_block_init only for
- *     the packing copy it enqueues; the packed buffer must outlive the handle.
+ *     owned by the caller.  Weights are borrowed by the *_init calls only for
+ *     the packing copies they enqueue; the packed buffer must outlive the
+ *     handle.  Handles are freed by flux3_destroy / flux3_cond_destroy.
  *   - Layouts are row-major, token-major: a [T, C] tensor has element (t, c) at
  *     offset t*C + c.  bf16 is IEEE bfloat16 stored in 16 bits.
  *   - Errors are returned as flux3_status codes, never by aborting.  Argument
