@@ -7,9 +7,9 @@
 //                          in float64 (256 values per row)
 //   rows_linear_kernel     y[m] (+)= W act(x[m]) for a few rows m (M <= 4):
 //                          the MLPEmbedders, the modulation and adaLN linears.
-//                          HBM-bound on W (bf16 [N, K], 16-byte loads, one
-//                          warp per output, the activated rows in shared
-//                          memory)
+//                          HBM-bound on W (bf16 [N, K], four independent
+//                          16-byte loads in flight per lane, one warp per
+//                          output, the activated rows in shared memory)
 //   add_row_kernel         y[m] += r for the flow-map timestep term
 //   euler_kernel           latent += (sigma_next - sigma) * velocity, and the
 //                          new latent rounded to bf16 (the next call's input)
@@ -27,6 +27,7 @@ namespace cond_detail {
 
 constexpr int kTimeDim = 256;
 constexpr int kMaxRows = 4;
+constexpr int kLoads = 4;     // 16-byte weight loads each lane has in flight
 
 __global__ void timestep_embed_kernel(double t0, double t1, double t2, float *out) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -57,22 +58,32 @@ __global__ void __launch_bounds__(256) rows_linear_kernel(const __nv_bfloat16 *_
   for (int n = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; n < N; n += warps) {
     float acc[kMaxRows] = {0.f, 0.f, 0.f, 0.f};
     const uint4 *wr = reinterpret_cast<const uint4 *>(W + (size_t)n * K);
-    for (int k8 = lane; k8 < K / 8; k8 += 32) {
-      const uint4 wv = __ldcs(wr + k8);
-      const uint32_t u[4] = {wv.x, wv.y, wv.z, wv.w};
-      float w[8];
+    for (int k0 = lane; k0 < K / 8; k0 += 32 * kLoads) {
+      uint4 wv[kLoads];   // several independent 16-byte loads in flight per lane
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        w[2 * q] = __uint_as_float(u[q] << 16);
-        w[2 * q + 1] = __uint_as_float(u[q] & 0xFFFF0000u);
+      for (int l = 0; l < kLoads; ++l) {
+        const int k8 = k0 + 32 * l;
+        wv[l] = k8 < K / 8 ? __ldcs(wr + k8) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int m = 0; m < kMaxRows; ++m) {
-        if (m < M) {
-          const float4 a = *reinterpret_cast<const float4 *>(xs + m * K + 8 * k8);
-          const float4 b = *reinterpret_cast<const float4 *>(xs + m * K + 8 * k8 + 4);
-          acc[m] = fmaf(w[0], a.x, fmaf(w[1], a.y, fmaf(w[2], a.z, fmaf(w[3], a.w,
-                   fmaf(w[4], b.x, fmaf(w[5], b.y, fmaf(w[6], b.z, fmaf(w[7], b.w, acc[m]))))))));
+      for (int l = 0; l < kLoads; ++l) {
+        const int k8 = k0 + 32 * l;
+        if (k8 >= K / 8) break;
+        const uint32_t u[4] = {wv[l].x, wv[l].y, wv[l].z, wv[l].w};
+        float w[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          w[2 * q] = __uint_as_float(u[q] << 16);
+          w[2 * q + 1] = __uint_as_float(u[q] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int m = 0; m < kMaxRows; ++m) {
+          if (m < M) {
+            const float4 a = *reinterpret_cast<const float4 *>(xs + m * K + 8 * k8);
+            const float4 b = *reinterpret_cast<const float4 *>(xs + m * K + 8 * k8 + 4);
+            acc[m] = fmaf(w[0], a.x, fmaf(w[1], a.y, fmaf(w[2], a.z, fmaf(w[3], a.w,
+                     fmaf(w[4], b.x, fmaf(w[5], b.y, fmaf(w[6], b.z, fmaf(w[7], b.w, acc[m]))))))));
+          }
         }
       }
     }
