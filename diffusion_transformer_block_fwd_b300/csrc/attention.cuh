@@ -336,17 +336,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s) {
   using namespace attn_tc;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<bool> attr_set[kMaxDevices];
+  const int slot = device_slot();
+  if (slot < 0 || !attr_set[slot].load(std::memory_order_acquire)) {
     // the warpgroup register split assumes exactly kLaunchRegs per thread at launch
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attention_kernel);
+    const cudaError_t e = cudaFuncGetAttributes(&fa, attention_kernel);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
   }
+  const cudaError_t e = set_smem_once(attention_kernel, (int)kSmem, attr_set);
+  if (e != cudaSuccess) return e;
   CUtensorMap tm;
   if (!make_tmap_bf16(&tm, qkv, (uint64_t)T, kQkvCols, kRows)) return cudaErrorInvalidValue;
   dim3 grid((T + 2 * kRows - 1) / (2 * kRows), kHeads);

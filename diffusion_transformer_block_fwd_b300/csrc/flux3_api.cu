@@ -278,7 +278,6 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
 constexpr size_t kNoAllocScratchBytes = workspace_total(FLUX3_NOALLOC_MAX_TOKENS);
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[kMaxDevices] = {nullptr};
 
@@ -323,17 +322,24 @@ bool make_tmap_f32_box32(CUtensorMap *tm, const void *base, uint64_t rows, uint6
   return r == CUDA_SUCCESS;
 }
 
+int device_slot() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
 int num_sms() {
-  static int n[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (n[dev] == 0) {
-    int v = 0;
+  static std::atomic<int> n[kMaxDevices];
+  const int slot = device_slot();
+  int v = slot >= 0 ? n[slot].load(std::memory_order_relaxed) : 0;
+  if (v == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    n[dev] = v > 0 ? v : 1;
+    if (v <= 0) v = 1;
+    if (slot >= 0) n[slot].store(v, std::memory_order_relaxed);
   }
-  return n[dev];
+  return v;
 }
 
 }  // namespace flux3

@@ -1,6 +1,7 @@
 // Internal launchers shared by the C-ABI layer and the kernel files.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -55,7 +56,26 @@ bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t c
 // {32 cols, 32 rows} box and 128-byte swizzle.  Returns false on failure.
 bool make_tmap_f32_box32(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols);
 
+// Multiprocessor count of the current device.
 int num_sms();
+
+// The current device as an index into per-device state, or -1 when it has
+// none (no current device, or an ordinal past kMaxDevices: the state is then
+// set up on every call).  Function attributes and device properties belong to
+// a device's context, so a process that drives several GPUs sets them up on
+// each.
+constexpr int kMaxDevices = 64;
+int device_slot();
+
+// Sets a kernel's dynamic shared-memory limit once per device.
+template <typename Kernel>
+cudaError_t set_smem_once(Kernel kernel, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
+  const int slot = device_slot();
+  if (slot >= 0 && done[slot].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && slot >= 0) done[slot].store(true, std::memory_order_release);
+  return e;
+}
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K,
                         const EpiParams &ep, cudaStream_t s);

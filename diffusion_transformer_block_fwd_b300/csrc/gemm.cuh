@@ -465,15 +465,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
+// ---------------------------------------------------------------- host launchers
 template <int EPI>
 cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K, const EpiParams &ep,
                         cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevices];
+  const cudaError_t e = set_smem_once(gemm_kernel<EPI>, (int)kSmemBytes, attr_set);
+  if (e != cudaSuccess) return e;
   // output boxes of 32 rows x 64 columns for the bf16 epilogues
   CUtensorMap tmO0 = tmA, tmO1 = tmA;
   if (EPI == EPI_STORE && !make_tmap_bf16(&tmO0, ep.C, (uint64_t)M, (uint64_t)ep.ldc, 32)) return cudaErrorInvalidValue;
