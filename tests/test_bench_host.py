@@ -1,0 +1,87 @@
+"""Host-side pieces of bench.py that need no GPU: the reference arm's JSON
+line (the CPU oracle timed on a bounded sample, in the unit of the workload's
+own line) and the rule that keys a captured DRAM traffic figure to a kernel's
+device code."""
+
+import importlib.util
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _reference_line(workload, steps=2, warmup=3):
+    env = dict(os.environ, RANK="0")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          workload, "--steps", str(steps), "--warmup", str(warmup)],
+                         capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    return json.loads(lines[0])
+
+
+@pytest.mark.parametrize("workload", ["block_t96", "modes5_t112"])
+def test_reference_line_keeps_the_contract_and_the_workloads_unit(workload):
+    b = _bench()
+    tokens, flops, unit = b.workload_call(workload)
+    d = _reference_line(workload)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "impl"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["unit"] == unit and d["config"]["workload"] == workload and d["config"]["T"] == tokens
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    # value = tokens of one call / seconds of one call
+    assert d["value"] == pytest.approx(tokens / (d["ms_per_step"] * 1e-3), rel=1e-9)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["unit"] == unit and cb["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_is_silent_on_other_ranks():
+    env = dict(os.environ, RANK="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "block_t96", "--steps", "1", "--warmup", "3"],
+                         capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
+    assert out.returncode == 0 and not out.stdout.strip()
+
+
+def test_workload_calls_scale_with_their_blocks():
+    b = _bench()
+    T, f1, u1 = b.workload_call("block_1024sq_ref1_t8704")
+    T28, f28, u28 = b.workload_call("stack28_1024sq_ref1_t8704")
+    assert T == T28 == 8704 and f28 == 28 * f1 and u1 == b.UNIT and u28 == b.UNIT_STACK
+    # the block formula: 245,366,784 T + 12,288 T^2
+    assert f1 == 245_366_784 * T + 12_288 * T * T
+    # per-mode blocks: the formula at each mode's own count (512 txt, 4096 image, 4096 reference)
+    _, fm, um = b.workload_call("modes5_1024sq_ref1_t8704")
+    assert fm == 5 * (b.block_flops(512) + 2 * b.block_flops(4096)) and um == b.UNIT_MODES
+    # the guided pack: joint attention within each sample, so less than one joint sequence of both
+    Tp, fc, uc = b.workload_call("cfg50_1024sq_pack2")
+    assert Tp == 80 + 4096 + 160 + 4096 and uc == b.UNIT_CFG
+    assert fc < b.model_call_flops([8192, 0, 240], 5, 28)
+
+
+def test_traffic_key_covers_device_code_only():
+    b = _bench()
+    dev = b"__global__ void k() {}\n"
+    host = b"cudaError_t launch() { return cudaSuccess; }\n"
+    assert b.device_part(dev + b.HOST_MARKER + host) == dev
+    assert b.device_part(dev + b.HOST_MARKER + host + b"// edited\n") == dev
+    assert b.device_part(dev + host) == dev + host          # no marker: the whole file
+    # every kernel source a traffic figure is keyed to has the marker once
+    for tr in b.TRAFFIC.values():
+        with open(os.path.join(ROOT, tr["src"]), "rb") as f:
+            assert f.read().count(b.HOST_MARKER) == 1, tr["src"]
