@@ -99,8 +99,21 @@ def load_peaks():
     return 6400.0, 1800.0, 1400.0, "fallback"
 
 
+def smi_target(dev_index):
+    """The nvidia-smi id of CUDA device `dev_index`: its PCI bus id (nvidia-smi
+    numbers GPUs in PCI order and ignores CUDA_VISIBLE_DEVICES), else the
+    ordinal."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev_index)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return str(dev_index)
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """nvidia-smi clock / throttle samples while the timed region runs, on the
+    GPU the CUDA device maps to."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -108,6 +121,7 @@ class ClockSampler:
 
     def __init__(self, index):
         self.index = index
+        self.target = None
         self.proc = None
         self.path = None
 
@@ -115,10 +129,15 @@ class ClockSampler:
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            for target in dict.fromkeys((smi_target(self.index), str(self.index))):
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", target, f"--query-gpu={self.FIELDS}",
+                                              "--format=csv,noheader,nounits", "-lms", "50"],
+                                             stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                time.sleep(0.3)
+                if self.proc.poll() is None:     # still sampling: the id was accepted
+                    self.target = target
+                    break
+                self.proc = None
         except Exception:
             self.proc = None
 
@@ -148,7 +167,8 @@ class ClockSampler:
                         reasons.add(n)
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons),
+                "gpu": self.target}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
