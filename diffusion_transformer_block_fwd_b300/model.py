@@ -134,6 +134,21 @@ class Flux3Blocks:
                                 mod.data_ptr(), ws.data_ptr(), ws.numel(), sp)
         return x
 
+    def forward_batch(self, x, segments, sample_start, pos_ids, mod, first_block=0, n_blocks=None, stream=None):
+        """The blocks over several samples concatenated in x (sample b owns
+        rows sample_start[b] .. sample_start[b + 1] - 1): LayerNorm and the
+        projections over all rows, attention within each sample, in place.
+        mod: float32 [3 * n_samples, 9216], row 3 b + stream."""
+        T = x.shape[0]
+        n = self.n_blocks - first_block if n_blocks is None else n_blocks
+        for t in (x, pos_ids, mod):
+            assert t.dtype == torch.float32 and t.is_contiguous() and t.device == self.device
+        assert sample_start[0] == 0 and sample_start[-1] == T
+        ws = self.workspace(T)
+        flux3_stack_forward_batch(self.handle, first_block, n, x.data_ptr(), T, segments, list(sample_start),
+                                  pos_ids.data_ptr(), mod.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+        return x
+
     def close(self):
         if getattr(self, "handle", None):
             flux3_destroy(self.handle)

@@ -27,12 +27,8 @@ def _sync_ok():
 
 
 def _batch(blocks, pack, x, mods, first=0, n=None):
-    n = blocks.n_blocks - first if n is None else n
-    ws = blocks.workspace(pack.T)
     pos = torch.from_numpy(pack.pos).to(DEV)
-    F3.flux3_stack_forward_batch(blocks.handle, first, n, x.data_ptr(), pack.T, pack.segments, pack.sample_start,
-                                 pos.data_ptr(), mods.data_ptr(), ws.data_ptr(), ws.numel(),
-                                 torch.cuda.current_stream().cuda_stream)
+    blocks.forward_batch(x, pack.segments, pack.sample_start, pos, mods, first_block=first, n_blocks=n)
 
 
 @pytest.fixture(scope="module")

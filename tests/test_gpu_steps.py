@@ -1,8 +1,6 @@
 """Parity of each step of the block (through the C ABI) against the CPU
 oracle, on seeded inputs that span several tiles and a ragged tail."""
 
-import math
-
 import numpy as np
 import pytest
 import torch

@@ -164,7 +164,6 @@ def _torch_batch_block(x, w, mods, sample_id, sid, pos):
     """One joint block over concatenated samples in one pass: attention with a
     block-diagonal boolean mask by sample (scaled_dot_product_attention), each
     token's modulation row 3 * sample + stream.  fp64 torch."""
-    from test_oracle_pins import _torch_block   # noqa: F401  (same block, restated with a mask below)
     T, D = x.shape
     d = len(w["query_norm"])
     H = D // d

@@ -5,7 +5,6 @@ scratch is a fixed array inside the library, so its output must match the
 ordinary entry point (caller-provided workspace) on the same inputs, call
 after call.  This file is collected last on purpose."""
 
-import ctypes
 
 import numpy as np
 import pytest
