@@ -1,0 +1,156 @@
+"""A model of the tcgen05 GEMM's synchronisation protocol, run on the CPU.
+
+The persistent GEMM has three roles per CTA pair: a TMA producer filling a
+6-stage operand ring (full / empty barriers), one MMA-issuing thread that
+accumulates each tile into one of two TMEM accumulators (acc = local tile
+index & 1) and commits the stage back and, after the tile's last k-block,
+the accumulator to the epilogue (tmem_full), and the epilogue warps, which
+drain an accumulator and hand it back (tmem_empty).  The roles are replayed
+as coroutines under random interleavings with mbarrier semantics (counts,
+transaction bytes, phase parity) and an in-order tensor pipe.  The model
+checks that every interleaving finishes, that each MMA reads the stage
+holding its (tile, k-block), that an accumulator is not restarted before the
+epilogue has drained its previous tile, and that the epilogue reads complete
+sums.  Planted mistakes (a stage released before its MMAs, a wrong
+accumulator phase) must be caught.
+"""
+
+import random
+
+import pytest
+
+from test_attention_protocol import Barrier
+
+STAGES = 6
+
+
+class Gemm:
+    def __init__(self, tiles, num_kb, seed, plant=None):
+        self.tiles, self.num_kb, self.plant = tiles, num_kb, plant
+        self.rng = random.Random(seed)
+        self.full = [Barrier(f"full{s}", 1) for s in range(STAGES)]
+        self.empty = [Barrier(f"empty{s}", 1) for s in range(STAGES)]
+        self.tmem_full = [Barrier(f"tmem_full{a}", 1) for a in range(2)]
+        self.tmem_empty = [Barrier(f"tmem_empty{a}", 1) for a in range(2)]   # the epilogue's arrivals, as one
+        self.drain = Barrier("drain", 1)
+        self.pipe, self.copies = [], []
+        self.stage_holds = [None] * STAGES
+        self.acc = [None, None]            # (tile, k-blocks accumulated)
+        self.drained = [set(), set()]      # tiles whose accumulator the epilogue has read out
+        self.finished = set()
+
+    @staticmethod
+    def wait(bar, parity):
+        while not bar.passed(parity):
+            yield (bar, parity)
+
+    def producer(self):
+        stage = phase = 0
+        for t in self.tiles:
+            for kb in range(self.num_kb):
+                yield from self.wait(self.empty[stage], phase ^ 1)
+                self.full[stage].expect_tx(1)
+                self.full[stage].arrive()
+                self.copies.append((stage, (t, kb)))
+                stage += 1
+                if stage == STAGES:
+                    stage, phase = 0, phase ^ 1
+
+    def issuer(self):
+        stage = phase = 0
+        for local, t in enumerate(self.tiles):
+            a = local & 1
+            acc_phase = (local >> 1) & 1
+            if self.plant == "wrong_acc_phase":
+                acc_phase ^= 1
+            yield from self.wait(self.tmem_empty[a], acc_phase ^ 1)
+            for kb in range(self.num_kb):
+                yield from self.wait(self.full[stage], phase)
+                if self.plant == "stage_released_early":
+                    self.pipe.append(("commit", self.empty[stage]))
+                self.pipe.append(("mma", a, stage, (t, kb)))
+                if self.plant != "stage_released_early":
+                    self.pipe.append(("commit", self.empty[stage]))
+                stage += 1
+                if stage == STAGES:
+                    stage, phase = 0, phase ^ 1
+            self.pipe.append(("commit", self.tmem_full[a]))
+        self.pipe.append(("commit", self.drain))
+        yield from self.wait(self.drain, 0)
+
+    def epilogue(self):
+        for local, t in enumerate(self.tiles):
+            a = local & 1
+            yield from self.wait(self.tmem_full[a], (local >> 1) & 1)
+            assert self.acc[a] == (t, self.num_kb), f"epilogue of tile {t} read {self.acc[a]}"
+            yield None                       # reading the accumulator out
+            self.drained[a].add(t)
+            self.tmem_empty[a].arrive()
+
+    def tensor_step(self):
+        op = self.pipe.pop(0)
+        if op[0] == "commit":
+            op[1].arrive()
+            return
+        _, a, stage, (t, kb) = op
+        assert self.stage_holds[stage] == (t, kb), f"MMA ({t}, {kb}) read stage {stage} = {self.stage_holds[stage]}"
+        if kb == 0:
+            prev = self.acc[a]
+            assert prev is None or prev[0] in self.drained[a], f"tile {t} restarted accumulator {a} over {prev}"
+            self.acc[a] = (t, 1)
+        else:
+            assert self.acc[a] == (t, kb), f"accumulator {a} holds {self.acc[a]}, MMA ({t}, {kb})"
+            self.acc[a] = (t, kb + 1)
+
+    def copy_step(self, i):
+        stage, tag = self.copies.pop(i)
+        self.stage_holds[stage] = tag
+        self.full[stage].tx_done(1)
+
+    def run(self):
+        roles = {"tma": self.producer(), "mma": self.issuer(), "epi": self.epilogue()}
+        blocked = {}
+        for _ in range(400_000):
+            choices = [("role", r) for r in roles
+                       if r not in self.finished and (r not in blocked or blocked[r][0].passed(blocked[r][1]))]
+            if self.pipe:
+                choices.append(("pipe", None))
+            choices += [("copy", i) for i in range(len(self.copies))]
+            if not choices:
+                assert len(self.finished) == 3, "deadlock: " + ", ".join(
+                    f"{r} on {b.name}/{p}" for r, (b, p) in blocked.items())
+                return
+            kind, arg = self.rng.choice(choices)
+            if kind == "pipe":
+                self.tensor_step()
+            elif kind == "copy":
+                self.copy_step(arg)
+            else:
+                try:
+                    y = next(roles[arg])
+                    if y is None:
+                        blocked.pop(arg, None)
+                    else:
+                        blocked[arg] = y
+                except StopIteration:
+                    self.finished.add(arg)
+                    blocked.pop(arg, None)
+        raise AssertionError("step limit")
+
+
+@pytest.mark.parametrize("n_tiles,num_kb", [(1, 1), (1, 7), (2, 3), (3, 5), (5, 2), (6, 13)])
+def test_protocol_finishes_and_reads_the_right_stages(n_tiles, num_kb):
+    for seed in range(40):
+        Gemm(list(range(10, 10 + n_tiles)), num_kb, seed * 31 + n_tiles).run()
+
+
+@pytest.mark.parametrize("plant", ["stage_released_early", "wrong_acc_phase"])
+def test_planted_mistakes_are_caught(plant):
+    caught = 0
+    for n_tiles, num_kb in ((3, 4), (4, 7), (2, 9)):
+        for seed in range(40):
+            try:
+                Gemm(list(range(n_tiles)), num_kb, seed, plant).run()
+            except AssertionError:
+                caught += 1
+    assert caught > 0, f"the model missed the planted mistake {plant}"
