@@ -271,11 +271,11 @@ FLUX3_API flux3_status flux3_stack_forward(const flux3_handle *h, int first_bloc
                                            void *workspace, size_t ws_bytes, void *stream);
 
 /* The per-mode blocks that precede the joint stack ("FLUX.3 Image Klein
- * support", comment "Structure (from dit.py)": the first 5 blocks are per
- * mode, each mode runs through its own weights, attends only to its own
- * tokens of the same sample, and takes its modulation from the mode's
- * early_stream_modulations; tensor names content_mode_blocks.{image,
- * image_cond}.{0..4} and txt_mode_blocks.{0..4}).  Each mode's tokens run
+ * support", comment "Structure (from dit.py)"): five blocks per mode with
+ * that mode's own weights; attention limited to the tokens of the same mode
+ * in the same sample; modulation from the mode's early_stream_modulations
+ * (tensor names content_mode_blocks.{image, image_cond}.{0..4} and
+ * txt_mode_blocks.{0..4}).  Each mode's tokens run
  * through blocks 0 .. n_blocks-1 of that mode's handle as a sequence of their
  * own (attention block-diagonal by mode); x is updated in place.
  *   mode_handles  host array [3] indexed by flux3_stream: the handle holding
@@ -406,11 +406,11 @@ FLUX3_API flux3_status flux3_euler_step(float *latent, const float *velocity, si
 FLUX3_API flux3_status flux3_latents_to_bf16(const float *latent, size_t n, void *input, void *stream);
 
 /* ------------------------------------------------------------------------
- * Several samples in one call: the base model runs classifier-free guidance
- * on a two-sample pack [empty prompt, prompt] ("FLUX.3 Image Klein support",
- * comment "Sampling (sampling.py, pipeline.py)"), and attention stays within
- * a sample ("Structure": tokens attend to the other tokens of the same
- * sample).  The samples' tokens are concatenated: sample b owns rows
+ * Several samples in one call: the base model guides its sampler with a
+ * pack of two samples, the empty prompt's and the prompt's ("FLUX.3 Image
+ * Klein support", comment "Sampling (sampling.py, pipeline.py)"), and a
+ * token attends only within its own sample (comment "Structure (from
+ * dit.py)").  The samples' tokens are concatenated: sample b owns rows
  * [sample_start[b], sample_start[b+1]).
  * ------------------------------------------------------------------------ */
 #define FLUX3_MAX_SAMPLES 16

@@ -8,15 +8,18 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Sources:
 * "FLUX.3 Image Klein support" (stable-diffusion.cpp issue #2142), comment
-  "Structure (from dit.py)": timestep_embedding(t) = [cos, sin] of
-  1000 * t * freqs (dim 256, max_period 10000) into an MLPEmbedder (Linear,
-  SiLU, Linear); image tokens carry the current t, the other modes 0; for the
-  flow-map checkpoint vec += ref_time_in(timestep_embedding(t_next)) for every
-  mode; output on the image tokens only: LayerNorm with shift/scale from
-  adaLN_modulation (SiLU, Linear to 2 x 3072), then a linear to 128 channels.
-  Comment "Sampling (sampling.py, pipeline.py)": t = linspace(1, 0, steps+1),
-  sigma = alpha t / (1 + (alpha - 1) t), alpha = 6.93; the flow map is called
-  with (sigma_k, sigma_{k+1}) and updates x += (sigma_{k+1} - sigma_k) v.
+  "Structure (from dit.py)": the time conditioning is a 256-wide sinusoidal
+  embedding (cosines and sines of 1000 t times a frequency ladder with period
+  scale 10000) fed to an MLPEmbedder (Linear, SiLU, Linear); the image mode is
+  conditioned on the current t and the other two modes on 0; the flow-map
+  checkpoint adds the ref_time_in embedding of t_next to the vector of every
+  mode; only image tokens reach the output, a LayerNorm modulated by a shift
+  and scale from adaLN_modulation (SiLU, then a Linear to 2 x 3072) followed
+  by a linear to 128 channels.  Comment "Sampling (sampling.py,
+  pipeline.py)": the sigma schedule alpha t / (1 + (alpha - 1) t) over t
+  evenly spaced from 1 to 0 in `steps` intervals, alpha 6.93; the flow map
+  takes (sigma_k, sigma_{k+1}) and the latents move by
+  (sigma_{k+1} - sigma_k) times the velocity.
   Tensor list: emb_in.{image,image_cond} [3072,128], txt_in [3072,20480],
   time_in / ref_time_in in_layer [3072,256] and out_layer [3072,3072], the
   modulation linears [9216,3072], final_layer adaLN [6144,3072] and linear
@@ -30,7 +33,7 @@ Sources:
 Readings (the pages are silent): the frequency ladder freqs_i =
 max_period^(-i/128), i = 0..127; the modulation vectors are Linear(SiLU(vec))
 like the output layer's adaLN (the pages name only the linear); the output
-LayerNorm is the blocks' one (no affine, eps 1e-6); adaLN chunk order shift,
+LayerNorm is the blocks' one (no learned parameters, epsilon 1e-6); adaLN chunk order shift,
 scale; the embedders, like every matrix of the checkpoint, have no bias.
 """
 
@@ -140,10 +143,10 @@ def euler_step(x, v, sigma, sigma_next):
 
 
 # --------------------------------------------------------------------------
-# Several samples in one call: the base model's classifier-free guidance on a
-# two-sample pack [empty prompt, prompt] ("Sampling (sampling.py,
-# pipeline.py)"); attention stays within a sample ("Structure": tokens attend
-# to each other per sample).  The guidance combination is a reading: the pages
+# Several samples in one call: the base model guides its sampler with a pack
+# of two samples, the empty prompt's and the prompt's (comment "Sampling
+# (sampling.py, pipeline.py)"); a token attends only within its own sample
+# (comment "Structure (from dit.py)").  The guidance combination is a reading: the pages
 # give the pack and the scale (3.5), not the formula; this is the usual
 # classifier-free guidance form.
 # --------------------------------------------------------------------------

@@ -120,9 +120,10 @@ def split_modulation(mod_row, hidden=HIDDEN):
 
 
 def layer_norm(x, eps=EPS_LN):
-    """LayerNorm over the last axis without affine parameters (eps 1e-6),
-    biased variance ("FLUX.3 Image Klein support", "Structure": "LayerNorm(x)
-    ... (no affine, eps 1e-6)")."""
+    """LayerNorm over the last axis with no learned scale or bias, epsilon
+    1e-6 and the biased variance ("FLUX.3 Image Klein support", comment
+    "Structure (from dit.py)", the block's x_mod line; the variance form is a
+    reading)."""
     x = np.asarray(x, dtype=np.float64)
     mu = x.mean(axis=-1, keepdims=True)
     var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
@@ -131,17 +132,20 @@ def layer_norm(x, eps=EPS_LN):
 
 def modulate(x, mods, stream_id, eps=EPS_LN):
     """x_mod = (1 + scale) * LayerNorm(x) + shift, with each token's shift and
-    scale taken from its own stream's modulation vector ("Structure": "each
-    token's shift/scale/gate comes from single_stream_modulations of its mode";
-    "Inside one block" pseudocode lines 2-3)."""
+    scale taken from the modulation vector of the token's own mode ("FLUX.3
+    Image Klein support", comment "Structure (from dit.py)", on the shared
+    blocks; "Welcome FLUX.3 Image Klein in Diffusers", section "Inside one
+    block")."""
     x = np.asarray(x, np.float64)
     shift, scale, _ = split_modulation(np.asarray(mods)[np.asarray(stream_id)], x.shape[-1])
     return (1.0 + scale) * layer_norm(x, eps) + shift
 
 
 def rms_norm(x, scale, eps=EPS_RMS):
-    """Per-head RMSNorm over head_dim: x / sqrt(mean(x^2) + eps) * scale
-    ("Structure": "per-head RMSNorm (eps 1e-6, scale over head_dim 128)")."""
+    """RMSNorm of each head's 128 values: x / sqrt(mean(x^2) + eps) * scale,
+    with epsilon 1e-6 and a learned scale of length 128 shared by the heads
+    ("FLUX.3 Image Klein support", comment "Structure (from dit.py)", applied
+    to q and k before RoPE)."""
     x = np.asarray(x, dtype=np.float64)
     return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps) * np.asarray(scale, np.float64)
 
@@ -214,9 +218,9 @@ def silu(x):
 
 
 def swiglu(ab, mlp_hidden=None):
-    """a, b = chunk(2) of the mlp_in output (a = first half); returns
-    silu(a) * b ("Structure": "mlp_out(silu(a) * b) with a, b =
-    mlp_in(x_mod).chunk(2)")."""
+    """SwiGLU of the mlp_in output: with a its first half and b its second,
+    returns silu(a) * b ("FLUX.3 Image Klein support", comment "Structure
+    (from dit.py)", the block line; which half gates is a reading)."""
     ab = np.asarray(ab, np.float64)
     if mlp_hidden is None:
         mlp_hidden = ab.shape[-1] // 2
@@ -244,12 +248,14 @@ def qkv_heads(h, w, pos, rows=None):
 def single_block_parts(x, w, mods, stream_id, pos, rows=None):
     """The block step by step; returns a dict of intermediates and the output.
 
-    Follows "Structure" (the block line) and the "Inside one block" pseudocode:
+    Follows "FLUX.3 Image Klein support", comment "Structure (from dit.py)"
+    (the block line), and "Welcome FLUX.3 Image Klein in Diffusers", section
+    "Inside one block":
       h      = (1 + scale) * LayerNorm(x) + shift          (per token's stream)
       q, k, v = separate projections of h
       q, k   = RoPE(RMSNorm(q)), RoPE(RMSNorm(k))          (per head)
       attn   = attention(q, k, v)                          (all tokens)
-      g      = silu(a) * b,  a, b = mlp_in(h).chunk(2)
+      g      = silu(a) * b,  [a | b] = h mlp_in^T (halves of 9216)
       x'     = x + gate * (attn_out(attn) + mlp_out(g))    (per token's stream)
     ``rows`` restricts the outputs (and q, attention, MLP) to those tokens;
     keys and values always cover all T tokens.  Sizes are taken from the
@@ -291,11 +297,12 @@ def stack_forward(x, blocks, mods, stream_id, pos):
 
 def mode_blocks_forward(x, mode_blocks, early_mods, stream_id, pos):
     """The per-mode blocks that come before the joint ones ("FLUX.3 Image
-    Klein support", comment "Structure (from dit.py)": the first 5 blocks are
-    per mode; each mode runs through its own weights and attends only to its
-    own tokens of the same sample; its modulation is the mode's
-    early_stream_modulations; names content_mode_blocks.{image,image_cond}.*
-    and txt_mode_blocks.* in "Tensor names (distilled checkpoint)").
+    Klein support", comment "Structure (from dit.py)"): five blocks for each
+    mode, with weights of that mode alone; a token's attention is limited to
+    tokens of its own mode within its sample; the modulation comes from the
+    mode's early_stream_modulations linear (weight names
+    content_mode_blocks.{image,image_cond}.* and txt_mode_blocks.* in the
+    comment's tensor list).
 
     mode_blocks: for each stream id (image, image_cond, txt) the list of that
     mode's block weights, in order.  early_mods: [3, 3D].  The tokens of each

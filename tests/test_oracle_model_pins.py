@@ -18,9 +18,10 @@ def _rng(seed):
 
 
 # --------------------------------------------------------------------------
-# Schedule ("The denoising loop": shift 6.93, 44 of the 50 steps above
-# sigma = 0.5, sigma still 0.97 at step 10; "Sampling": t = linspace(1, 0,
-# steps+1), sigma = alpha t / (1 + (alpha - 1) t))
+# Schedule ("Welcome FLUX.3 Image Klein in Diffusers", section "The denoising
+# loop": the shift 6.93, 44 of 50 steps above sigma 0.5, sigma near 0.97 at
+# step 10; "FLUX.3 Image Klein support", comment "Sampling (sampling.py,
+# pipeline.py)": the shifted map of evenly spaced t from 1 to 0)
 # --------------------------------------------------------------------------
 def test_schedule_matches_the_printed_figures():
     s = M.sigma_schedule(50)
@@ -50,7 +51,8 @@ def test_euler_steps_telescope():
 
 
 # --------------------------------------------------------------------------
-# Timestep embedding ("Structure": [cos, sin] of 1000 * t * freqs, dim 256)
+# Timestep embedding (comment "Structure (from dit.py)": a 256-wide embedding
+# of cosines then sines of 1000 t times the frequencies)
 # --------------------------------------------------------------------------
 def test_timestep_embedding_closed_forms():
     e0 = M.timestep_embedding(0.0)
