@@ -133,8 +133,11 @@ class ClockSampler:
                 self.proc = subprocess.Popen(["nvidia-smi", "-i", target, f"--query-gpu={self.FIELDS}",
                                               "--format=csv,noheader,nounits", "-lms", "50"],
                                              stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-                time.sleep(0.3)
-                if self.proc.poll() is None:     # still sampling: the id was accepted
+                # accepted once a sample line arrives; an id nvidia-smi rejects ends the process
+                t_end = time.time() + 2.0
+                while time.time() < t_end and self.proc.poll() is None and os.path.getsize(self.path) == 0:
+                    time.sleep(0.05)
+                if self.proc.poll() is None:
                     self.target = target
                     break
                 self.proc = None
