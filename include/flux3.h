@@ -330,6 +330,9 @@ FLUX3_API size_t flux3_cond_packed_bytes(void);
  * source weights may be freed once the stream has passed the copies. */
 FLUX3_API flux3_status flux3_cond_init(flux3_cond **out, const flux3_cond_weights *w, void *packed,
                                        size_t packed_bytes, void *stream);
+
+/* Frees the conditioning handle's host state (NULL is allowed); the packed
+ * weight buffer stays the caller's. */
 FLUX3_API void flux3_cond_destroy(flux3_cond *c);
 
 /* Device workspace of flux3_conditioning (a few tens of KB). */

@@ -264,3 +264,19 @@ def test_model_entry_points_validation_before_any_launch():
     cfg = F3.flux3_default_config()
     assert F3.flux3_transformer_workspace_bytes(cfg, 4608) > F3.flux3_workspace_bytes(cfg, 4608) + 4608 * 3072 * 4
     assert F3.flux3_transformer_workspace_bytes(cfg, 0) == 0
+
+
+def test_every_entry_point_is_documented_in_the_header():
+    """Each FLUX3_API declaration of include/flux3.h follows its own comment
+    block (the operation, its arguments, layouts and errors)."""
+    lines = open(os.path.join(ROOT, "include", "flux3.h")).read().split("\n")
+    undocumented = []
+    for i, line in enumerate(lines):
+        if not line.startswith("FLUX3_API"):
+            continue
+        j = i - 1
+        while j >= 0 and not lines[j].strip():
+            j -= 1
+        if not lines[j].rstrip().endswith("*/"):
+            undocumented.append(line.split("(")[0].split()[-1])
+    assert not undocumented, undocumented
