@@ -492,6 +492,8 @@ FLUX3_API flux3_status flux3_block_forward_noalloc(const flux3_handle *h, int bl
  * Returns FLUX3_OK, FLUX3_ERR_TIMEOUT, FLUX3_ERR_DEVICE or FLUX3_ERR_CUDA. */
 FLUX3_API flux3_status flux3_check_error(void *stream);
 
+/* A static, NUL-terminated English name of a status code (never NULL; unknown
+ * codes give a generic string).  The caller does not free it. */
 FLUX3_API const char *flux3_status_string(flux3_status s);
 
 /* Frees the handle's host state.  Does not touch caller-owned device memory. */
