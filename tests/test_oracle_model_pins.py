@@ -232,3 +232,94 @@ def test_cfg_closed_forms():
     assert np.array_equal(M.cfg_velocity(u, c, 0.0), u)
     np.testing.assert_allclose(M.cfg_velocity(u, c, 3.5), 3.5 * c - 2.5 * u, rtol=1e-14, atol=1e-14)
     np.testing.assert_allclose(M.cfg_euler_step(x, u, c, 1.0, 0.8, 0.5), x - 0.3 * c, rtol=1e-14, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# One whole transformer call against a torch.nn.functional restatement
+# (comment "Structure (from dit.py)": embedders, time_in / ref_time_in, the
+# per-mode blocks under the early modulations, the joint blocks under the
+# single-stream modulations, the image output layer)
+# --------------------------------------------------------------------------
+def _torch_transformer_call(ins, sid, pos, t, t_next, c, mode_blocks, joint):
+    """The call restated in fp64 torch, written apart from the oracle: the
+    timestep embedding from its definition, each MLPEmbedder and modulation
+    linear with F.linear / F.silu, the per-mode blocks as block-diagonal
+    masked passes over the whole sequence, the joint blocks as full passes,
+    the output layer with F.layer_norm."""
+    from test_oracle_pins import _torch_block, _torch_mode_block
+
+    def temb(tt):
+        i = torch.arange(128, dtype=torch.float64)
+        a = 1000.0 * tt * torch.exp(-math.log(10000.0) * i / 128.0)
+        return torch.cat([torch.cos(a), torch.sin(a)])
+
+    def embedder(e, w_in, w_out):
+        return F.linear(F.silu(F.linear(e, _t(w_in))), _t(w_out))
+
+    v_img = embedder(temb(t), c["time_in_in"], c["time_in_out"])
+    v_rest = embedder(temb(0.0), c["time_in_in"], c["time_in_out"])
+    vec = torch.stack([v_img, v_rest, v_rest])          # rows: image, image_cond, txt
+    if "ref_time_in_in" in c:
+        vec = vec + embedder(temb(t_next), c["ref_time_in_in"], c["ref_time_in_out"])[None, :]
+    early = torch.stack([F.linear(F.silu(vec[s]), _t(c["early_mod"][s])) for s in range(3)]).numpy()
+    single = torch.stack([F.linear(F.silu(vec[s]), _t(c["single_mod"][s])) for s in range(3)]).numpy()
+    emb = [c["emb_in_image"], c["emb_in_image_cond"], c["txt_in"]]
+    T, D = len(sid), vec.shape[1]
+    x = torch.zeros((T, D), dtype=torch.float64)
+    for s in range(3):
+        x[torch.from_numpy(sid == s)] = F.linear(_t(ins[s]), _t(emb[s]))
+    x = x.numpy()
+    for b in range(len(mode_blocks[0])):
+        x = _torch_mode_block(x, [mode_blocks[m][b] for m in range(3)], early, sid, pos)
+    for w in joint:
+        x = _torch_block(x, w, single, sid, pos)
+    ada = F.linear(F.silu(vec[0]), _t(c["final_adaln"]))
+    shift, scale = ada[:D], ada[D:]
+    img = _t(x)[torch.from_numpy(sid == 0)]
+    h = (1.0 + scale) * F.layer_norm(img, (D,), eps=1e-6) + shift
+    return F.linear(h, _t(c["final_linear"])).numpy()
+
+
+def _tiny_call(seed):
+    from test_oracle_pins import _tiny_block
+    rng = _rng(seed)
+    c = _tiny_cond(rng)
+    mode_blocks = [[_tiny_block(rng) for _ in range(2)] for _ in range(3)]
+    joint = [_tiny_block(rng) for _ in range(2)]
+    sid = np.array([2, 2, 2, 0, 0, 0, 0, 0, 0, 1, 1, 1, 1])
+    pos = np.zeros((13, 4))
+    pos[:3, 3] = np.arange(3)
+    pos[3:9, 1], pos[3:9, 2] = np.repeat(np.arange(2), 3) * 0.5, np.tile(np.arange(3), 2) * 0.5
+    pos[9:, 1], pos[9:, 2], pos[9:, 3] = np.repeat(np.arange(2), 2) * 0.5, np.tile(np.arange(2), 2) * 0.5, -1.0
+    ins = [rng.standard_normal((6, 8)), rng.standard_normal((4, 8)), rng.standard_normal((3, 40))]
+    return ins, sid, pos, c, mode_blocks, joint
+
+
+def test_transformer_call_matches_library_restatement():
+    ins, sid, pos, c, mode_blocks, joint = _tiny_call(40)
+    for t, t_next in ((0.8, 0.6), (1.0, 0.75)):
+        got = M.transformer_forward(ins, sid, pos, t, t_next, c, mode_blocks, joint)
+        ref = _torch_transformer_call(ins, sid, pos, t, t_next, c, mode_blocks, joint)
+        assert got.shape == (6, 8)
+        np.testing.assert_allclose(got, ref, rtol=1e-9, atol=1e-11)
+
+
+def test_transformer_call_restatement_catches_planted_wiring_mistakes():
+    """Mistakes planted in the oracle's wiring (on the CPU, in copies of its
+    inputs) must break the agreement above: the early and single modulation
+    sets swapped, the image stream conditioned on t_next instead of t, the
+    per-mode and joint blocks run in the other order."""
+    ins, sid, pos, c, mode_blocks, joint = _tiny_call(41)
+    ref = _torch_transformer_call(ins, sid, pos, 0.8, 0.6, c, mode_blocks, joint)
+    scale = float(np.sqrt(np.mean(ref ** 2)))
+    swapped = dict(c, early_mod=c["single_mod"], single_mod=c["early_mod"])
+    planted = [M.transformer_forward(ins, sid, pos, 0.8, 0.6, swapped, mode_blocks, joint),
+               M.transformer_forward(ins, sid, pos, 0.6, 0.6, c, mode_blocks, joint)]
+    # blocks in the other order: the joint blocks first, then the per-mode ones
+    vec = M.stream_vectors(0.8, 0.6, c)
+    x = M.embed_tokens(ins, sid, c)
+    x = O.stack_forward(x, joint, M.modulation_vectors(vec, c["single_mod"]), sid, pos)
+    x = O.mode_blocks_forward(x, mode_blocks, M.modulation_vectors(vec, c["early_mod"]), sid, pos)
+    planted.append(M.final_layer(x[sid == 0], vec[0], c["final_adaln"], c["final_linear"]))
+    for p in planted:
+        assert np.abs(p - ref).max() > 1e-3 * scale
