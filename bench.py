@@ -45,6 +45,7 @@ UNIT_STACK = "tokens/s (per stack call)"
 UNIT_MODES = "tokens/s (per-mode blocks)"
 UNIT_MODEL = "tokens/s (transformer calls of the sampler)"
 UNIT_CFG = "tokens/s (two-sample guided calls of the sampler)"
+UNIT_ONE_BLOCK = "tokens/s (one joint block over the workload's token layout)"
 
 # Algorithmic FLOPs of one block over T tokens: 2 x (MACs of the six
 # projections) + QK^T + PV = 245,366,784 T + 12,288 T^2.
@@ -124,15 +125,22 @@ class ClockSampler:
         self.target = None
         self.proc = None
         self.path = None
+        self.out = None
+
+    def _close_out(self):
+        if self.out is not None:
+            self.out.close()
+            self.out = None
 
     def start(self):
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             for target in dict.fromkeys((smi_target(self.index), str(self.index))):
+                self.out = open(self.path, "w")
                 self.proc = subprocess.Popen(["nvidia-smi", "-i", target, f"--query-gpu={self.FIELDS}",
                                               "--format=csv,noheader,nounits", "-lms", "50"],
-                                             stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                                             stdout=self.out, stderr=subprocess.DEVNULL)
                 # accepted once a sample line arrives; an id nvidia-smi rejects ends the process
                 t_end = time.time() + 2.0
                 while time.time() < t_end and self.proc.poll() is None and os.path.getsize(self.path) == 0:
@@ -141,17 +149,22 @@ class ClockSampler:
                     self.target = target
                     break
                 self.proc = None
+                self._close_out()
         except Exception:
             self.proc = None
+            self._close_out()
 
     def stop(self):
         if self.proc is None:
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+        self._close_out()
         sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
@@ -175,11 +188,12 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-class OracleSample:
-    """The CPU oracle on a bounded sample of the workload: the block output for
-    `rows_n` query tokens (keys and values over all T tokens).  A sample's time
-    is scaled to a whole block by the ratio of algorithmic FLOPs (full block /
-    the sample's)."""
+class OracleBlock:
+    """The CPU oracle running one joint block over a workload's token layout
+    (seeded inputs, float64).  `run()` times the whole block: every output
+    row, keys and values over all T tokens.  `run_sampled()` times the block
+    output for `rows_n` query tokens only (keys and values still over all
+    tokens), for warm-up and for a labelled FLOP-scaled estimate."""
 
     def __init__(self, spec, rows_n=128):
         import oracle as O
@@ -195,18 +209,40 @@ class OracleSample:
         self.rows = np.linspace(0, T - 1, rows_n).astype(np.int64)
         D, F = 3072, 9216
         sample_flops = 4 * T * D * D + rows_n * (2 * D * D + 4 * D * F + 2 * (D + F) * D + 4 * T * D)
-        self.scale = block_flops(T) / sample_flops
+        self.sample_scale = block_flops(T) / sample_flops
         self.rows_n = rows_n
 
     def run(self):
-        """Seconds of one whole block, extrapolated from one timed sample."""
+        """Seconds of one whole block (measured)."""
+        t0 = time.perf_counter()
+        self.O.single_block(self.x, self.wf, self.mods, self.lay.stream_id, self.pos)
+        return time.perf_counter() - t0
+
+    def run_sampled(self):
+        """Seconds of the sampled block (measured, not scaled)."""
         t0 = time.perf_counter()
         self.O.single_block(self.x, self.wf, self.mods, self.lay.stream_id, self.pos, rows=self.rows)
-        return (time.perf_counter() - t0) * self.scale
+        return time.perf_counter() - t0
 
     def describe(self, reps):
+        return (f"fp64 NumPy oracle: one whole block over the workload's {self.T} tokens (every output row), "
+                f"{reps} measured rep(s)")
+
+    def describe_sampled(self, reps):
         return (f"fp64 NumPy oracle: block output for {self.rows_n} of {self.T} query tokens (keys/values over all "
-                f"tokens), {reps} rep(s), time scaled to a whole block by algorithmic FLOPs x{self.scale:.2f}")
+                f"tokens), {reps} rep(s), time scaled to a whole block by algorithmic FLOPs x{self.sample_scale:.2f}")
+
+
+def pin_blas_threads():
+    """Pins the BLAS thread pool to the cores this process may run on and
+    returns that count (the core count the oracle's time is quoted for)."""
+    cores = len(os.sched_getaffinity(0))
+    try:
+        from threadpoolctl import threadpool_limits
+        threadpool_limits(limits=cores, user_api="blas")
+    except Exception:
+        pass
+    return cores
 
 
 def host_cores():
@@ -222,43 +258,64 @@ def host_cores():
 
 
 def oracle_baseline(spec, seconds):
-    s = OracleSample(spec)
+    """The oracle timed in full on this host: whole blocks until `seconds` have
+    passed (at least one); the 128-row FLOP-scaled estimate is reported beside
+    it under its own key."""
+    pin_blas_threads()
+    s = OracleBlock(spec)
+    s.run_sampled()                                    # warm-up (BLAS threads, page faults)
+    est = s.run_sampled() * s.sample_scale
     times = []
     t_end = time.perf_counter() + seconds
-    while not times or (time.perf_counter() < t_end and len(times) < 50):
+    while not times or time.perf_counter() < t_end:
         times.append(s.run())
     t_block = statistics.mean(times)
     return {"value": s.T / t_block, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-            "sample": s.describe(len(times))}
+            "sample": s.describe(len(times)), "ms_per_block": 1e3 * t_block,
+            "sampled_extrapolation": {"value": s.T / est, "unit": UNIT, "ms_per_block": 1e3 * est,
+                                      "sample": s.describe_sampled(1)}}
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on the host cores.  A
+    timed step is one whole joint block over the workload's token layout,
+    measured (no scaling).  For a single-block workload that is the call our
+    arm's step repeats, so the line has our line's unit; for the multi-block
+    workloads (stacks, samplers, per-mode blocks) the line's unit is one
+    block, and the call-scaled figure is reported under its own key.
+    Warm-up steps run the sampled block (the same code on 128 query rows) so
+    that the whole run ends within a few minutes."""
     if int(os.environ.get("RANK", "0")) != 0:
         return
     import synth
+    cores = pin_blas_threads()
     wl = synth.WORKLOADS[args.workload]
     spec = wl["spec"] if "spec" in wl else wl["specs"][-1]   # a pack: the conditional sample's layout
     tokens, call_flops, unit = workload_call(args.workload)
-    s = OracleSample(spec)
-    # one sampled block's time, scaled from that block's FLOPs to the workload's call
-    call_scale = call_flops / block_flops(s.T)
+    s = OracleBlock(spec)
     for _ in range(args.warmup):
-        s.run()
+        s.run_sampled()
     t0 = time.perf_counter()
-    times = [s.run() * call_scale for _ in range(args.steps)]
+    times = [s.run() for _ in range(args.steps)]
     wall = time.perf_counter() - t0
-    value = tokens / statistics.mean(times)
-    sample = s.describe(args.steps)
-    if call_scale != 1.0:
-        sample += f", then to one call of the workload by its algorithmic FLOPs x{call_scale:.2f}"
-    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+    t_step = statistics.mean(times)
+    single = call_flops == block_flops(s.T) and tokens == s.T
+    line_unit = unit if single else UNIT_ONE_BLOCK
+    value = s.T / t_step
+    sample = s.describe(args.steps) + f"; warm-up: {args.warmup} sampled block(s) ({s.rows_n} query rows)"
+    line = {"metric": METRIC, "value": value, "unit": line_unit, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": args.workload, "T": tokens},
-            "cpu_baseline": {"value": value, "unit": unit, "cores": host_cores(), "kind": "oracle",
+            "config": {"workload": args.workload, "T": s.T, "unit_of_work": "one joint block, measured in full"},
+            "cpu_baseline": {"value": value, "unit": line_unit, "cores": cores, "kind": "oracle",
                              "sample": sample},
-            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "e2e": {"value": value, "unit": line_unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s_timed_region": wall}
+    if not single:
+        call_s = t_step * call_flops / block_flops(s.T)
+        line["call_extrapolation"] = {"value": tokens / call_s, "unit": unit, "ms_per_call": 1e3 * call_s,
+                                      "how": f"the measured block scaled to one call of the workload by "
+                                             f"algorithmic FLOPs x{call_flops / block_flops(s.T):.2f}"}
     print(json.dumps(line), flush=True)
 
 
@@ -498,28 +555,33 @@ def run_ours(args):
                            "(copy streams, three device buffers)"},
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
             "wall_s_timed_region": t_wall}
+    blocks.close()
+    if not args.no_stack_target:
+        line["stack28_1024sq_ref1_t8704"] = stack_target(dev, local, world)
     if world > 1:
         dist.barrier()
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_baseline(spec, args.cpu_seconds)
         print(json.dumps(line), flush=True)
-    blocks.close()
     if world > 1:
         dist.destroy_process_group()
 
 
-def run_stack(args, rank, world, local, dev):
-    """A 28-block stack workload: a step is `calls` stack calls (one per
+def measure_stack(name, steps, warmup, dev, local, world):
+    """Times a 28-block stack workload: a step is `calls` stack calls (one per
     sampler step, each with its own modulation vectors) over the whole token
-    sequence, bf16 or NVFP4 weights (quantised on the device)."""
+    sequence, bf16 or NVFP4 / fp8r weights (quantised on the device); L2 is
+    flushed between steps; CUDA events on the launching stream; nvidia-smi
+    clock samples over the timed region.  Returns the figures of the
+    workload's line."""
     import torch
     import torch.distributed as dist
 
     import diffusion_transformer_block_fwd_b300 as F3
     import synth
 
-    wl = synth.WORKLOADS[args.workload]
+    wl = synth.WORKLOADS[name]
     lay = synth.build_layout(wl["spec"])
     T, nb, calls = lay.T, wl["blocks"], wl["calls"]
     fp4, fp8 = wl["wfmt"] == "nvfp4", wl["wfmt"] == "fp8r"
@@ -556,19 +618,19 @@ def run_stack(args, rank, world, local, dev):
 
     per_call_launches = 2 + nb * (4 + (1 if fp4 or fp8 else 0))
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             x.copy_(x0)
             step()
         st = F3.flux3_check_error(sp)
         assert st == 0, F3.status_string(st)
-        events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
         sampler = ClockSampler(local)
         sampler.start()
         t_wall0 = time.perf_counter()
-        for i in range(args.steps):
+        for i in range(steps):
             x.copy_(x0)
             flush.zero_()
             step(events[i])
@@ -577,20 +639,34 @@ def run_stack(args, rank, world, local, dev):
         clocks = sampler.stop()
     st = F3.flux3_check_error(sp)
     assert st == 0, F3.status_string(st)
+    blocks.close()
     value, step_ms = replica_throughput(T * calls, statistics.mean(e[0].elapsed_time(e[1]) for e in events), world,
                                         dev)
     flops = calls * nb * block_flops(T)
     hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
     tflops = world * flops / (step_ms * 1e-3) / 1e12
-    line = {"metric": METRIC, "value": value, "unit": UNIT_STACK,
+    return {"T": T, "blocks": nb, "calls": calls, "segments": lay.segments, "fp4": fp4, "fp8": fp8,
+            "value": value, "ms_per_step": step_ms, "tflops": tflops, "bf16_burst": bf16_burst,
+            "bf16_sust": bf16_sust, "launches": per_call_launches * calls * steps, "clocks": clocks,
+            "wall_s_timed_region": t_wall}
+
+
+def run_stack(args, rank, world, local, dev):
+    """A 28-block stack workload's line (see measure_stack)."""
+    import torch.distributed as dist
+
+    m = measure_stack(args.workload, args.steps, args.warmup, dev, local, world)
+    fp4, fp8, tflops, calls, nb = m["fp4"], m["fp8"], m["tflops"], m["calls"], m["blocks"]
+    bf16_burst, bf16_sust, step_ms = m["bf16_burst"], m["bf16_sust"], m["ms_per_step"]
+    line = {"metric": METRIC, "value": m["value"], "unit": UNIT_STACK,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" + (" (NVFP4 weights dequantised per block)" if fp4 else
                                " (fp8r weights expanded per block)" if fp8 else ""),
             "data": "synthetic (random-init N(0,0.02) weights" + (", NVFP4-quantised on the device)" if fp4 else
                                                                     ", fp8r-quantised on the device)" if fp8 else ")"),
-            "config": {"workload": args.workload, "T": T, "blocks": nb, "calls_per_step": calls,
-                       "segments": lay.segments, "l2": "flushed between timed steps",
+            "config": {"workload": args.workload, "T": m["T"], "blocks": nb, "calls_per_step": calls,
+                       "segments": m["segments"], "l2": "flushed between timed steps",
                        "launch": "stream launches through flux3_stack_forward"},
             "ms_per_stack_call": step_ms / calls, "ms_per_block": step_ms / calls / nb,
             "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
@@ -600,12 +676,28 @@ def run_stack(args, rank, world, local, dev):
                          "peak": bf16_sust or bf16_burst, "unit": "TFLOP/s",
                          "frac": tflops / world / (bf16_sust or bf16_burst), "traffic": None,
                          "peak_source": "measured bf16 sustained (MEASURED_PEAKS.json)"},
-            "gpu_launches": per_call_launches * calls * args.steps, "clocks": clocks, "wall_s_timed_region": t_wall}
+            "gpu_launches": m["launches"], "clocks": m["clocks"], "wall_s_timed_region": m["wall_s_timed_region"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    blocks.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+def stack_target(dev, local, world, steps=5, warmup=2):
+    """The 28-block stack at 1024x1024 + one 1024x1024 reference (8704 tokens),
+    timed on its own (own events and clock record) for the line of the
+    single-block workload: ms per stack call and TFLOP/s against the dense
+    bf16 spec (2.25 PFLOP/s) and the measured burst and sustained peaks."""
+    name = "stack28_1024sq_ref1_t8704"
+    m = measure_stack(name, steps, warmup, dev, local, world)
+    t = m["tflops"] / world
+    return {"workload": name, "T": m["T"], "blocks": m["blocks"], "steps": steps, "warmup": warmup,
+            "ms_per_stack_call": m["ms_per_step"] / m["calls"], "ms_per_block": m["ms_per_step"] / m["calls"] / m["blocks"],
+            "tokens_per_s": m["value"], "tflops": t, "frac_of_bf16_spec_2250": t / 2250.0,
+            "frac_of_bf16_peak": t / m["bf16_burst"],
+            "frac_of_bf16_sustained": (t / m["bf16_sust"]) if m["bf16_sust"] else None,
+            "gpu_launches": m["launches"], "clocks": m["clocks"],
+            "timing": "CUDA events around each stack call (flux3_stack_forward), L2 flushed between calls"}
 
 
 def run_modes(args, rank, world, local, dev):
@@ -972,6 +1064,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack-target", action="store_true",
+                    help="skip the 28-block 8704-token stack timed beside the single-block workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

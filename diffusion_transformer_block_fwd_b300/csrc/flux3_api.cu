@@ -273,25 +273,20 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
 // Scratch for flux3_block_forward_noalloc: a file-scope device array sized for
 // FLUX3_NOALLOC_MAX_TOKENS tokens.  Every device that loads the library holds
 // it until the process exits.  Host code only ever sees a host-side stand-in
-// for the symbol, so the device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached.
+// for the symbol, so the device address is looked up with cudaGetSymbolAddress
+// in the current context.  The lookup runs on every call rather than being
+// cached: the address belongs to a CUDA context, and a context can be replaced
+// on the same device ordinal (cudaDeviceReset, or a host that drives the call
+// under a context of its own).  Once the module is loaded the lookup is a
+// host-side query that allocates nothing.
 constexpr size_t kNoAllocScratchBytes = workspace_total(FLUX3_NOALLOC_MAX_TOKENS);
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch array on the current device, or nullptr.
+// Device address of the scratch array in the current context, or nullptr.
 void *noalloc_scratch() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
-    g_noalloc_ptr[dev] = p;
-  }
-  return g_noalloc_ptr[dev];
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
 
 }  // namespace
@@ -786,6 +781,9 @@ flux3_status flux3_block_forward_noalloc(const flux3_handle *h, int block_idx, f
   if (T > FLUX3_NOALLOC_MAX_TOKENS) return FLUX3_ERR_WORKSPACE;
   if (!h || T < 1) return FLUX3_ERR_INVALID_ARG;
   if (h->cfg.wfmt != FLUX3_W_BF16) return FLUX3_ERR_UNSUPPORTED;
+  // the array is sized by workspace_total; the carving is workspace_layout's
+  if (workspace_layout(FLUX3_NOALLOC_MAX_TOKENS, nullptr, nullptr, false) > kNoAllocScratchBytes)
+    return FLUX3_ERR_WORKSPACE;
   void *scratch = noalloc_scratch();
   if (!scratch) return FLUX3_ERR_CUDA;
   return forward_common(h, block_idx, 1, x, T, segs, n_segs, pos_ids, mod, scratch, kNoAllocScratchBytes,

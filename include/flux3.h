@@ -477,8 +477,10 @@ FLUX3_API flux3_status flux3_cfg_euler_step(float *latent, const float *v_uncond
  *   - T > FLUX3_NOALLOC_MAX_TOKENS returns FLUX3_ERR_WORKSPACE; a handle with
  *     NVFP4 or fp8r weights returns FLUX3_ERR_UNSUPPORTED (its expanded weights
  *     would not fit); other errors as flux3_block_forward.
- *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any
+ *   - Every call looks up the array's device address in the current CUDA
+ *     context (cudaGetSymbolAddress; an address belongs to a context, which a
+ *     device reset or a host's own context replaces).  The first call on a
+ *     device may load the library's device code, so make it before any
  *     stream capture.
  *   - All calls share the one array and it keeps the last call's contents.
  *     Nothing in it needs to start at zero: every call writes each scratch

@@ -1,7 +1,6 @@
 """Host-side pieces of bench.py that need no GPU: the reference arm's JSON
-line (the CPU oracle timed on a bounded sample, in the unit of the workload's
-own line) and the rule that keys a captured DRAM traffic figure to a kernel's
-device code."""
+line (the CPU oracle timed on whole blocks), the CPU baseline of our line, and
+the rule that keys a captured DRAM traffic figure to a kernel's device code."""
 
 import importlib.util
 import json
@@ -34,6 +33,11 @@ def _reference_line(workload, steps=2, warmup=3):
 
 @pytest.mark.parametrize("workload", ["block_t96", "modes5_t112"])
 def test_reference_line_keeps_the_contract_and_the_workloads_unit(workload):
+    """The reference line states a measured time: each timed step is one whole
+    block over the workload's layout.  A single-block workload's step is the
+    call our line repeats, so the units agree; for a multi-block workload the
+    line is per block and the call-scaled figure sits under its own key, in
+    the unit of our line."""
     b = _bench()
     tokens, flops, unit = b.workload_call(workload)
     d = _reference_line(workload)
@@ -41,13 +45,33 @@ def test_reference_line_keeps_the_contract_and_the_workloads_unit(workload):
               "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "impl"):
         assert k in d, k
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
-    assert d["unit"] == unit and d["config"]["workload"] == workload and d["config"]["T"] == tokens
+    assert d["config"]["workload"] == workload and d["config"]["T"] == tokens
     assert d["value"] > 0 and d["higher_is_better"] is True
-    # value = tokens of one call / seconds of one call
+    # value = tokens of one block / measured seconds of one block
     assert d["value"] == pytest.approx(tokens / (d["ms_per_step"] * 1e-3), rel=1e-9)
+    # the timed region holds the steps it reports
+    assert d["wall_s_timed_region"] >= d["steps"] * d["ms_per_step"] * 1e-3 * 0.999
+    single = flops == b.block_flops(tokens)
+    assert d["unit"] == (unit if single else b.UNIT_ONE_BLOCK)
+    assert ("call_extrapolation" in d) != single
+    if not single:
+        ce = d["call_extrapolation"]
+        assert ce["unit"] == unit
+        assert ce["value"] == pytest.approx(tokens / (ce["ms_per_call"] * 1e-3), rel=1e-9)
+        assert ce["ms_per_call"] == pytest.approx(d["ms_per_step"] * flops / b.block_flops(tokens), rel=1e-9)
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["unit"] == unit and cb["cores"] >= 1
-    assert d["e2e"] == {"value": d["value"], "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["unit"] == d["unit"] and cb["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_is_measured_whole_blocks():
+    b = _bench()
+    cb = b.oracle_baseline([("txt", 8), ("image", (4, 4))], 0.0)
+    assert cb["kind"] == "oracle" and cb["unit"] == b.UNIT and cb["cores"] >= 1
+    assert cb["value"] == pytest.approx(24 / (cb["ms_per_block"] * 1e-3), rel=1e-9)
+    assert "whole block" in cb["sample"] and "1 measured rep" in cb["sample"]
+    ex = cb["sampled_extrapolation"]
+    assert ex["unit"] == b.UNIT and "scaled" in ex["sample"]
 
 
 def test_reference_arm_is_silent_on_other_ranks():

@@ -230,3 +230,49 @@ def test_nvfp4_handle_rejects_bf16_only_calls(fp4_block):
     st = F3.lib().flux3_block_forward_noalloc(blocks.handle, 0, x.data_ptr(), T, segs, 1, buf.data_ptr(),
                                               buf.data_ptr(), sp)
     assert st == F3.FLUX3_ERR_UNSUPPORTED
+
+
+@pytest.mark.slow
+def test_nvfp4_stack28_t14848_every_block_sampled_rows():
+    """Every block of a 28-block NVFP4 stack at the 14848-token layout
+    (1024x1024 + ten 512x512 references).  The oracle quantises each block's
+    seeded weights itself (worker processes) and the GPU handle is built from
+    the oracle's codes; each block gets a seeded input of its own (made on the
+    CPU), and its output rows (segment ends, the ragged tail, random rows)
+    are checked against the oracle run on the exactly dequantised weights:
+    5e-2 RMS / cosine 0.998 on x', plus the bf16 path's update criterion."""
+    import multiprocessing as mp
+
+    import _oracle_pool
+
+    with mp.get_context("spawn").Pool(6) as pool:
+        qs = pool.map(_oracle_pool.quantize_block, [(1357, b) for b in range(28)])
+    dev = []
+    for q in qs:
+        d = {k: (torch.from_numpy(q[k][0]).to(DEV), torch.from_numpy(q[k][1]).to(DEV),
+                 torch.tensor([q[k][2]], dtype=torch.float32, device=DEV)) for k in MATS}
+        d.update({k: torch.from_numpy(q[k].astype(np.float32)).to(DEV) for k in ("query_norm", "key_norm")})
+        dev.append(d)
+    blocks = F3.Flux3Blocks(dev, max_tokens=14848, wfmt="nvfp4")
+    del dev
+    lay = synth.build_layout(synth.WORKLOADS["stack28_nvfp4_1024sq_10ref512_t14848"]["spec"])
+    assert lay.T == 14848
+    pos, _ = layout_tensors(lay)
+    pos64 = lay.pos.astype(np.float64)
+    rows = sample_rows(lay.T, lay.segments, n_random=8)
+    mods = synth.modulation(1358, device=DEV)
+    m64 = f64(mods)
+    for b in range(28):
+        wdq = {k: Q.dequantize(*qs[b][k]) for k in MATS}
+        wdq.update({k: qs[b][k] for k in ("query_norm", "key_norm")})
+        x_in = synth.activations(1400 + b, lay.T, device=DEV)
+        xg = x_in.clone()
+        blocks.forward(xg, lay.segments, pos, mods, first_block=b, n_blocks=1)
+        x64 = f64(x_in)
+        parts = O.single_block_parts(x64, wdq, m64, lay.stream_id, pos64, rows=rows)
+        assert F3.flux3_check_error(_stream()) == 0
+        got = f64(xg)[rows]
+        assert_close(got, parts["out"], 5e-2, 0.998, f"t14848 block {b} x' (NVFP4 criterion)")
+        assert_block_output(got, parts["out"], x64[rows], m64[lay.stream_id[rows], 6144:], parts["y"],
+                            f"t14848 block {b}")
+    blocks.close()
