@@ -7,7 +7,8 @@ the 1024x1024 workload: 512 text + 64x64 image tokens = 4608): stream ids,
 RoPE tables, LayerNorm + modulation, the fused in-projection GEMM (q/k/v with
 QK-RMSNorm + RoPE, SwiGLU), attention, and the out-projection GEMM with the
 gated residual.  Inputs are resident in HBM when the timed region starts;
-L2 is flushed (a 256 MiB write) between timed steps, outside the per-step
+L2 is flushed (a 256 MiB write, then a 256 MiB read of another buffer, which
+drains the write's dirty lines) between timed steps, outside the per-step
 events.  For N > 1 (torchrun) every rank runs an independent replica (the
 path needs no exchange): the value is the tokens of all ranks over the
 slowest rank's time.
@@ -61,6 +62,23 @@ def kernel_flops(T):
             "out_projection": 2 * T * 12288 * 3072}
 
 
+def out_proj_splits(T, sms):
+    """K ranges of the out-projection's trailing tiles at T tokens on `sms`
+    SMs (1: no split), the plan the library takes: the last, partial round of
+    256 x 256 tiles on the CTA pairs is split by the largest of 8, 6, 4, 3, 2
+    that divides the 192 k-blocks into ranges of >= 16 and keeps the units
+    within the pairs and 96 partial tiles.  A split adds one merge launch."""
+    pairs = sms // 2
+    tiles = -(-T // 256) * 12
+    rem = tiles % pairs if tiles >= pairs else tiles
+    if rem == 0:
+        return 1
+    for S in (8, 6, 4, 3, 2):
+        if 192 % S == 0 and 192 // S >= 16 and rem * S <= pairs and rem * S <= 96:
+            return S
+    return 1
+
+
 def kernel_bytes(T):
     """Algorithmic HBM bytes per launch of the memory-bound kernels."""
     return {"ln_modulate": T * (3072 * 4 + 3072 * 2), "rope_tables": T * (16 + 2 * 64 * 4), "stream_ids": T}
@@ -89,6 +107,25 @@ def device_part(text):
 def src_sha(path):
     with open(os.path.join(ROOT, path), "rb") as f:
         return hashlib.sha256(device_part(f.read())).hexdigest()[:16]
+
+
+class L2Flush:
+    """Evicts the step's data from L2 between timed steps: a 256 MiB write
+    (larger than the 126 MB L2), then a 256 MiB read of a second buffer, so
+    that the write's dirty lines are written back before the next step starts
+    instead of during its first kernels.  Runs outside the step's events."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+L2_NOTE = "flushed between timed steps (256 MiB write, then a 256 MiB read of another buffer), outside the events"
 
 
 def load_peaks():
@@ -399,7 +436,8 @@ def run_ours(args):
     h = torch.empty((T, 3072), dtype=torch.bfloat16, device=dev)
     qkv = torch.empty((T, 9216), dtype=torch.bfloat16, device=dev)
     cat = torch.empty((T, 12288), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MiB > L2
+    split = torch.empty(F3.FLUX3_SPLIT_BYTES // 4, dtype=torch.float32, device=dev)   # out-projection K split
+    flush = L2Flush(dev)
     stream = torch.cuda.Stream(dev)
     sp = stream.cuda_stream
     cfg = blocks.cfg
@@ -425,11 +463,12 @@ def run_ours(args):
         if evs is not None:
             evs[4].record(stream)
         F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), x.data_ptr(),
-                                sp)
+                                sp, split.data_ptr(), F3.FLUX3_SPLIT_BYTES)
         if evs is not None:
             evs[5].record(stream)
 
-    launches_per_step = 6
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    launches_per_step = 6 + (1 if out_proj_splits(T, sms) > 1 else 0)
     torch.cuda.synchronize(dev)          # inputs were made on the default stream
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -543,7 +582,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init N(0,0.02) bf16 weights)",
             "config": {"workload": args.workload, "T": T, "segments": lay.segments,
-                       "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+                       "l2": L2_NOTE,
                        "launch": "one CUDA graph replay per step (event-record nodes around each kernel)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
@@ -605,7 +644,7 @@ def measure_stack(name, steps, warmup, dev, local, world):
     x = x0.clone()
     mods = [synth.modulation(1, call=c, device=dev) for c in range(calls)]
     pos = torch.from_numpy(lay.pos).to(dev)
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     torch.cuda.synchronize(dev)
 
     def step(evs=None):
@@ -616,7 +655,8 @@ def measure_stack(name, steps, warmup, dev, local, world):
         if evs is not None:
             evs[1].record(stream)
 
-    per_call_launches = 2 + nb * (4 + (1 if fp4 or fp8 else 0))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    per_call_launches = 2 + nb * (4 + (1 if fp4 or fp8 else 0) + (1 if out_proj_splits(T, sms) > 1 else 0))
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             x.copy_(x0)
@@ -666,7 +706,7 @@ def run_stack(args, rank, world, local, dev):
             "data": "synthetic (random-init N(0,0.02) weights" + (", NVFP4-quantised on the device)" if fp4 else
                                                                     ", fp8r-quantised on the device)" if fp8 else ")"),
             "config": {"workload": args.workload, "T": m["T"], "blocks": nb, "calls_per_step": calls,
-                       "segments": m["segments"], "l2": "flushed between timed steps",
+                       "segments": m["segments"], "l2": L2_NOTE,
                        "launch": "stream launches through flux3_stack_forward"},
             "ms_per_stack_call": step_ms / calls, "ms_per_block": step_ms / calls / nb,
             "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
@@ -730,7 +770,7 @@ def run_modes(args, rank, world, local, dev):
     x = x0.clone()
     mods = synth.modulation(1, device=dev)
     pos = torch.from_numpy(lay.pos).to(dev)
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     torch.cuda.synchronize(dev)
 
     def step(evs=None):
@@ -740,7 +780,8 @@ def run_modes(args, rank, world, local, dev):
         if evs is not None:
             evs[1].record(stream)
 
-    launches = sum(2 + nb * 4 for c in counts if c)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    launches = sum(2 + nb * (4 + (out_proj_splits(c, sms) > 1)) for c in counts if c)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             x.copy_(x0)
@@ -772,7 +813,7 @@ def run_modes(args, rank, world, local, dev):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (random-init N(0,0.02) weights, one set per mode)",
             "config": {"workload": args.workload, "T": T, "tokens_per_mode": counts, "blocks_per_mode": nb,
-                       "segments": lay.segments, "l2": "flushed between timed steps",
+                       "segments": lay.segments, "l2": L2_NOTE,
                        "launch": "stream launches through flux3_mode_blocks_forward"},
             "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
             "frac_of_bf16_sustained": (tflops / world / bf16_sust) if bf16_sust else None,
@@ -871,7 +912,7 @@ def run_model(args, rank, world, local, dev):
     noise = ins[0].float()
     lat = noise.clone()
     pos = torch.from_numpy(lay.pos).to(dev)
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     torch.cuda.synchronize(dev)
 
     def step(evs=None):
@@ -909,7 +950,9 @@ def run_model(args, rank, world, local, dev):
     flops = steps * model_call_flops(counts, nm, nb)
     hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
     tflops = world * flops / (step_ms * 1e-3) / 1e12
-    per_call_launches = (15 + sum(1 for c in counts if c) * (2 + 4 * nm) + 2 + 4 * nb + 1
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    per_call_launches = (15 + sum(2 + nm * (4 + (out_proj_splits(c, sms) > 1)) for c in counts if c)
+                         + 2 + nb * (4 + (out_proj_splits(T, sms) > 1)) + 1
                          + sum(1 for s_ in lay.segments) + 2 + 1)
     line = {"metric": METRIC, "value": value, "unit": UNIT_MODEL,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -917,7 +960,7 @@ def run_model(args, rank, world, local, dev):
             "data": "synthetic (random-init N(0,0.02) weights, N(0,1) latents and text features)",
             "config": {"workload": args.workload, "T": T, "tokens_per_mode": counts, "sampler_steps": steps,
                        "mode_blocks": nm, "joint_blocks": nb, "segments": lay.segments,
-                       "l2": "flushed between timed steps",
+                       "l2": L2_NOTE,
                        "launch": "stream launches through flux3_transformer_forward and flux3_euler_step"},
             "ms_per_image": step_ms, "ms_per_call": step_ms / steps,
             "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,
@@ -981,7 +1024,7 @@ def run_cfg(args, rank, world, local, dev):
     noise = ins[1][0].float()
     lat = noise.clone()
     pos = torch.from_numpy(pack.pos).to(dev)
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     torch.cuda.synchronize(dev)
 
     def step(evs=None):
@@ -1022,9 +1065,11 @@ def run_cfg(args, rank, world, local, dev):
     # blocks (2 + 4 per block per present mode), the output layer (LayerNorm + GEMM); the joint blocks
     # (2 + 4 per block, one more attention launch per block for each further sample); the guided update
     n_s = len(counts)
-    launches = (sum(13 + len(lay.segments) + sum(2 + 4 * nm for m in range(3) if c[m]) + 2
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    launches = (sum(13 + len(lay.segments) + sum(2 + nm * (4 + (out_proj_splits(c[m], sms) > 1))
+                                                  for m in range(3) if c[m]) + 2
                     for c, lay in zip(counts, pack.layouts))
-                + 2 + 4 * nb + nb * (n_s - 1) + 1)
+                + 2 + nb * (4 + (out_proj_splits(pack.T, sms) > 1)) + nb * (n_s - 1) + 1)
     flops = steps * per_call
     hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
     tflops = world * flops / (step_ms * 1e-3) / 1e12
@@ -1035,7 +1080,7 @@ def run_cfg(args, rank, world, local, dev):
             "config": {"workload": args.workload, "T": T, "sample_start": pack.sample_start,
                        "tokens_per_mode_per_sample": counts, "sampler_steps": steps, "guidance": 3.5,
                        "mode_blocks": nm, "joint_blocks": nb, "segments": pack.segments,
-                       "l2": "flushed between timed steps",
+                       "l2": L2_NOTE,
                        "launch": "stream launches through flux3_transformer_forward_batch and flux3_cfg_euler_step"},
             "ms_per_image": step_ms, "ms_per_call": step_ms / steps,
             "tflops": tflops, "frac_of_bf16_peak": tflops / world / bf16_burst,

@@ -132,7 +132,7 @@ def lib():
             "flux3_ln_modulate": (i, [vp, i, vp, vp, f, vp, vp]),
             "flux3_in_projection": (i, [vp, i, vp, i, vp, vp, vp, vp, vp]),
             "flux3_attention": (i, [vp, i, vp, vp]),
-            "flux3_out_projection": (i, [vp, i, vp, i, vp, vp, vp, vp]),
+            "flux3_out_projection": (i, [vp, i, vp, i, vp, vp, vp, vp, sz, vp]),
             "flux3_gemm_bf16": (i, [vp, vp, vp, i, i, i, vp]),
             "flux3_selftest_wait_timeout": (i, [i, vp]),
             "flux3_block_forward_noalloc": (i, [vp, i, vp, i, segp, i, vp, vp, vp]),
@@ -435,8 +435,12 @@ def flux3_attention(qkv, T, cat, stream=0):
     _check(lib().flux3_attention(qkv, T, cat, stream), "flux3_attention")
 
 
-def flux3_out_projection(h, block_idx, cat, T, stream_id, mod, x, stream=0):
-    _check(lib().flux3_out_projection(h, block_idx, cat, T, stream_id, mod, x, stream), "flux3_out_projection")
+FLUX3_SPLIT_BYTES = 96 * 256 * 256 * 4
+
+
+def flux3_out_projection(h, block_idx, cat, T, stream_id, mod, x, stream=0, split_buf=None, split_bytes=0):
+    _check(lib().flux3_out_projection(h, block_idx, cat, T, stream_id, mod, x, split_buf, split_bytes, stream),
+           "flux3_out_projection")
 
 
 def flux3_gemm_bf16(A, B, C, M, N, K, stream=0):

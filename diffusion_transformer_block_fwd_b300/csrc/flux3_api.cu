@@ -79,9 +79,15 @@ bool config_ok(const flux3_config *c) {
 // Bytes of the workspace for T tokens (each sub-buffer rounded up to 256 B);
 // the order and sizes match workspace_layout below.
 constexpr size_t ws_round(size_t v) { return (v + 255) / 256 * 256; }
+// The out-projection's split partials reuse h and qkv (both dead once
+// attention has run) when those hold kSplitBytes; below that size of T they
+// get a region of their own.
+constexpr bool split_in_place(size_t T) {
+  return ws_round(T * kHidden * 2) + ws_round(T * kQkvCols * 2) >= kSplitBytes;
+}
 constexpr size_t workspace_total(size_t T) {
   return ws_round(T) + 2 * ws_round(T * kRopePairs * 4) + ws_round(T * kHidden * 2) + ws_round(T * kQkvCols * 2) +
-         ws_round(T * kCatCols * 2);
+         ws_round(T * kCatCols * 2) + (split_in_place(T) ? 0 : kSplitBytes);
 }
 
 // NVFP4 packed block: in-projection codes and scales, out-projection codes and
@@ -109,6 +115,7 @@ struct Workspace {
   uint8_t *sid;
   float *cos_tab, *sin_tab;
   __nv_bfloat16 *h, *qkv, *cat;
+  float *part;                   // the out-projection's split partials (kSplitBytes)
   __nv_bfloat16 *w_in, *w_out;   // NVFP4 / fp8r handles: the running block's weights in bf16
 };
 
@@ -125,6 +132,7 @@ size_t workspace_layout(int T, uint8_t *base, Workspace *ws, bool fp4_weights = 
   uint8_t *h = take((size_t)T * kHidden * 2);
   uint8_t *qkv = take((size_t)T * kQkvCols * 2);
   uint8_t *cat = take((size_t)T * kCatCols * 2);
+  uint8_t *part = split_in_place((size_t)T) ? h : take(kSplitBytes);
   uint8_t *w_in = fp4_weights ? take(kWInElems * 2) : nullptr;
   uint8_t *w_out = fp4_weights ? take(kWOutElems * 2) : nullptr;
   if (ws) {
@@ -134,6 +142,7 @@ size_t workspace_layout(int T, uint8_t *base, Workspace *ws, bool fp4_weights = 
     ws->h = reinterpret_cast<__nv_bfloat16 *>(h);
     ws->qkv = reinterpret_cast<__nv_bfloat16 *>(qkv);
     ws->cat = reinterpret_cast<__nv_bfloat16 *>(cat);
+    ws->part = reinterpret_cast<float *>(part);
     ws->w_in = reinterpret_cast<__nv_bfloat16 *>(w_in);
     ws->w_out = reinterpret_cast<__nv_bfloat16 *>(w_out);
   }
@@ -179,13 +188,15 @@ flux3_status run_in_projection(const flux3_handle *h, int b, const __nv_bfloat16
 }
 
 flux3_status run_out_projection(const flux3_handle *h, int b, const __nv_bfloat16 *cat, int T, const uint8_t *sid,
-                                const float *mod, float *x, cudaStream_t s) {
+                                const float *mod, float *x, float *part, size_t part_bytes, cudaStream_t s) {
   CUtensorMap tmA;
   if (!make_tmap_bf16(&tmA, cat, (uint64_t)T, kCatCols, kBM)) return FLUX3_ERR_CUDA;
   EpiParams ep{};
   ep.x = x;
   ep.sid = sid;
   ep.mod = mod;
+  ep.part = part;
+  ep.part_bytes = part_bytes;
   return cuda_status(launch_gemm(EPI_OUT_RESIDUAL, tmA, h->tm_out[b], T, kHidden, kCatCols, ep, s));
 }
 
@@ -264,6 +275,8 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     eo.x = x;
     eo.sid = ws.sid;
     eo.mod = mod;
+    eo.part = ws.part;
+    eo.part_bytes = kSplitBytes;
     F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, fp4 ? tmWout : h->tm_out[b], T, kHidden, kCatCols, eo, s));
   }
   return FLUX3_OK;
@@ -753,12 +766,15 @@ flux3_status flux3_attention(const void *qkv, int T, void *cat, void *stream) {
 }
 
 flux3_status flux3_out_projection(const flux3_handle *h, int block_idx, const void *cat, int T,
-                                  const uint8_t *stream_id, const float *mod, float *x, void *stream) {
+                                  const uint8_t *stream_id, const float *mod, float *x, void *split_buf,
+                                  size_t split_bytes, void *stream) {
   if (!h || !cat || !stream_id || !mod || !x) return FLUX3_ERR_INVALID_ARG;
   if (block_idx < 0 || block_idx >= h->n_blocks || T < 1 || T > h->cfg.max_tokens) return FLUX3_ERR_INVALID_ARG;
   if (h->cfg.wfmt != FLUX3_W_BF16) return FLUX3_ERR_UNSUPPORTED;
   if (!aligned16(cat) || !aligned16(mod) || !aligned16(x)) return FLUX3_ERR_ALIGNMENT;
+  if (split_buf && !aligned16(split_buf)) return FLUX3_ERR_ALIGNMENT;
   return run_out_projection(h, block_idx, static_cast<const __nv_bfloat16 *>(cat), T, stream_id, mod, x,
+                            static_cast<float *>(split_buf), split_buf ? split_bytes : 0,
                             static_cast<cudaStream_t>(stream));
 }
 

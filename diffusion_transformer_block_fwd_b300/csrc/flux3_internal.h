@@ -46,7 +46,17 @@ struct EpiParams {
   float *x;             // [M, 3072] (EPI_STORE_F32: the float32 output [M, ldc])
   const uint8_t *sid;   // [M]
   const float *mod;     // [3, 9216]
+  // EPI_OUT_RESIDUAL with a K split of the trailing tiles: float32 partial
+  // tiles (256 x 256 per split unit); null / too small: no split
+  float *part;
+  size_t part_bytes;
 };
+
+// Most split units one GEMM launch uses (their partial tiles: 256 KB each).
+constexpr int kMaxSplitUnits = 96;
+constexpr size_t kSplitUnitBytes = 256 * 256 * 4;
+constexpr size_t kSplitBytes = kMaxSplitUnits * kSplitUnitBytes;
+static_assert(kSplitBytes == FLUX3_SPLIT_BYTES, "split scratch size of the header");
 
 // Encodes a 2-D bf16 tensor map over a row-major [rows, cols] matrix with a
 // {64 cols, box_rows} box and 128-byte swizzle.  Returns false on failure.

@@ -24,6 +24,13 @@
 // accumulator through tcgen05.ld (one output row and one 128-column half per
 // thread) and run the epilogue, so the epilogue of tile i overlaps the MMAs
 // of tile i+1.
+// Units: the pairs take units round robin.  Whole tiles fill complete
+// rounds; when the last round would leave pairs idle, its tiles are split
+// along K into ranges (out-projection only): each range stores its float32
+// partial tile, and split_merge_residual_kernel sums a tile's ranges in a fixed
+// order (deterministic) and applies the gated residual.
+// L2: the operand that every round re-reads is loaded with evict_last, the
+// streamed one with evict_first.
 // Every wait is bounded (see mbar_wait); on a timeout the CTA drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 
@@ -286,11 +293,56 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, bool n_
   }
 }
 
+// The pair schedule over units: units 0 .. n_full-1 are whole tiles (every
+// k-block); each later tile is `splits` units, unit ks of it covering k-blocks
+// [ks * num_kb / splits, (ks + 1) * num_kb / splits).  slot = -1 for a whole
+// tile, else the unit's index among the split units (its partial buffer).
+struct Unit {
+  int m_blk, n_blk, kb0, kb1, slot;
+};
+__device__ __forceinline__ Unit unit_of(int u, int n_full, int splits, int num_m, int num_n, bool n_fast,
+                                        int num_kb) {
+  Unit r;
+  int tile;
+  if (u < n_full) {
+    tile = u;
+    r.kb0 = 0;
+    r.kb1 = num_kb;
+    r.slot = -1;
+  } else {
+    const int v = u - n_full, ks = v % splits;
+    tile = n_full + v / splits;
+    r.kb0 = ks * num_kb / splits;
+    r.kb1 = (ks + 1) * num_kb / splits;
+    r.slot = v;
+  }
+  tile_coords(tile, num_m, num_n, n_fast, r.m_blk, r.n_blk);
+  return r;
+}
+
+// A split unit's fp32 accumulator rows go to its partial buffer (256 x 256
+// float32 per unit, row = row in the tile) as four 32 x 32 boxes per half.
+__device__ __forceinline__ void store_partial_half(uint32_t taddr, int slot, int row_box0, int rows_valid, int half,
+                                                   const BoxWriter &bw, const CUtensorMap *tmP) {
+  if (row_box0 >= rows_valid) return;   // the merge reads no row past M
+  uint32_t r[32];
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    bw.begin();
+    tmem_ld32(taddr + half * 128 + c * 32, r);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4 *>(bw.buf + bw.lane * 128 + ((q ^ (bw.lane & 7)) * 16)) =
+          make_float4(f32(r[4 * q]), f32(r[4 * q + 1]), f32(r[4 * q + 2]), f32(r[4 * q + 3]));
+    bw.store(tmP, half * 128 + c * 32, slot * kTileM + row_box0);
+  }
+}
+
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
-                int K, EpiParams ep) {
+                int K, int n_full, int splits, EpiParams ep) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *smA = smem;
@@ -306,6 +358,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int num_m = (M + kTileM - 1) / kTileM;
   const int num_n = N / kBN;
   const int num_tiles = num_m * num_n;
+  const int num_units = n_full + (num_tiles - n_full) * splits;
   const int num_kb = K / kBK;
   // Tile order: consecutive pairs share the operand with more rows, so that
   // it is read from DRAM about once and the smaller one is re-read from L2.
@@ -342,26 +395,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer (both CTAs): this CTA's 128 A rows and
-      // 128 B rows of each stage, completing on the leader's full barrier
+      // 128 B rows of each stage, completing on the leader's full barrier.
+      // The operand the tile order re-reads in every round of tiles (B when
+      // consecutive pairs sweep the columns, else A) is kept in L2 with
+      // evict_last; the other one streams with evict_first.
+      const uint64_t keep = l2_policy_evict_last(), stream_once = l2_policy_evict_first();
+      const uint64_t pol_a = n_fast ? stream_once : keep, pol_b = n_fast ? keep : stream_once;
       int last_phase[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-        int m_blk, n_blk;
-        tile_coords(tile, num_m, num_n, n_fast, m_blk, n_blk);
-        const int a_row = m_blk * kTileM + (int)rank * kRowsPerCta;
-        const int b_row = n_blk * kBN + (int)rank * kRowsPerCta;
-        for (int kb = 0; kb < num_kb; ++kb) {
+      for (int u = pair; u < num_units && ok; u += num_pairs) {
+        const Unit un = unit_of(u, n_full, splits, num_m, num_n, n_fast, num_kb);
+        const int a_row = un.m_blk * kTileM + (int)rank * kRowsPerCta;
+        const int b_row = un.n_blk * kBN + (int)rank * kRowsPerCta;
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) {
             ok = false;
             break;
           }
           const uint32_t full_leader = map_to_cta(smem_addr(&ctl->full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&ctl->full[stage], kPairStageBytes);
-          tma_load_2d_pair(smA + stage * kABytes, &tmA, full_leader, kb * kBK, a_row);
-          tma_load_2d_pair(smB + stage * kBBytes, &tmB, full_leader, kb * kBK, b_row);
+          tma_load_2d_pair_hint(smA + stage * kABytes, &tmA, full_leader, kb * kBK, a_row, pol_a);
+          tma_load_2d_pair_hint(smB + stage * kBBytes, &tmB, full_leader, kb * kBK, b_row, pol_b);
           last_phase[stage] = (int)phase;
           if (++stage == kStages) {
             stage = 0;
@@ -384,13 +441,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs, ++local) {
+      for (int u = pair; u < num_units && ok; u += num_pairs, ++local) {
+        const Unit un = unit_of(u, n_full, splits, num_m, num_n, n_fast, num_kb);
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait(&ctl->tmem_empty[acc], acc_phase ^ 1, abort)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!mbar_wait(&ctl->full[stage], phase, abort)) {
             ok = false;
             break;
@@ -399,7 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)
             mma_bf16_ss_pair_at(d_tmem, da, stage * kABytes + k * 32, db, stage * kBBytes + k * 32, idesc,
-                                (kb | k) != 0);
+                                (kb != un.kb0 || k != 0) ? 1u : 0u);
           mma_commit_pair_mc(&ctl->empty[stage], 0x3);
           if (++stage == kStages) {
             stage = 0;
@@ -429,25 +487,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t empty_leader0 = map_to_cta(smem_addr(&ctl->tmem_empty[0]), 0);
     const uint32_t empty_leader1 = map_to_cta(smem_addr(&ctl->tmem_empty[1]), 0);
     int local = 0;
-    for (int tile = pair; tile < num_tiles; tile += num_pairs, ++local) {
-      int m_blk, n_blk;
-      tile_coords(tile, num_m, num_n, n_fast, m_blk, n_blk);
+    for (int u = pair; u < num_units; u += num_pairs, ++local) {
+      const Unit un = unit_of(u, n_full, splits, num_m, num_n, n_fast, num_kb);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if constexpr (EPI == EPI_OUT_RESIDUAL) {
         // the residual does not depend on the accumulator: its first box is
         // loaded while the MMAs of this tile still run
-        bw.begin();
-        load_x_box(bw, &tmO0, xbar, n_blk * kBN + half * 128, m_blk * kTileM + row_in_tile - lane);
+        if (un.slot < 0) {
+          bw.begin();
+          load_x_box(bw, &tmO0, xbar, un.n_blk * kBN + half * 128, un.m_blk * kTileM + row_in_tile - lane);
+        }
       }
       if (!mbar_wait(&ctl->tmem_full[acc], acc_phase, abort)) {
-        x_in_flight = EPI == EPI_OUT_RESIDUAL;
+        x_in_flight = EPI == EPI_OUT_RESIDUAL && un.slot < 0;
         break;
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kBN;
-      if (!epilogue_half<EPI>(taddr, m_blk * kTileM + row_in_tile, m_blk * kTileM + row_in_tile - lane, M, n_blk,
-                              half, ep, bw, &tmO0, &tmO1, xbar, xphase, abort)) {
+      if (un.slot >= 0) {
+        store_partial_half(taddr, un.slot, row_in_tile - lane, M - un.m_blk * kTileM, half, bw, &tmO1);
+      } else if (!epilogue_half<EPI>(taddr, un.m_blk * kTileM + row_in_tile, un.m_blk * kTileM + row_in_tile - lane,
+                                     M, un.n_blk, half, ep, bw, &tmO0, &tmO1, xbar, xphase, abort)) {
         x_in_flight = true;   // only the residual box wait can fail
         break;
       }
@@ -465,13 +526,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
+// Sums the split units of each trailing tile in a fixed order (unit 0 first)
+// and applies the out-projection's epilogue: x[row, col] += gate[stream(row)]
+// [col] * sum.  One thread per 4 columns of a row; tile i of the trailing
+// tiles is tile n_full + i of the schedule.
+__global__ void split_merge_residual_kernel(const float *__restrict__ part, int n_full, int splits, int num_m,
+                                            int num_n, int n_fast, int M, float *__restrict__ x,
+                                            const uint8_t *__restrict__ sid, const float *__restrict__ mod) {
+  const int i = blockIdx.y;                                 // trailing tile
+  const int r = blockIdx.x * 4 + threadIdx.x / 64;          // row in the tile
+  const int c = (threadIdx.x % 64) * 4;                     // column in the tile
+  int m_blk, n_blk;
+  tile_coords(n_full + i, num_m, num_n, n_fast != 0, m_blk, n_blk);
+  const int row = m_blk * kTileM + r;
+  if (row >= M) return;
+  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int ks = 0; ks < splits; ++ks) {
+    const float4 p = __ldcs(reinterpret_cast<const float4 *>(part + ((size_t)(i * splits + ks) * kTileM + r) * kBN + c));
+    y.x += p.x;
+    y.y += p.y;
+    y.z += p.z;
+    y.w += p.w;
+  }
+  const int col = n_blk * kBN + c;
+  const float4 g = __ldg(reinterpret_cast<const float4 *>(mod + (size_t)sid[row] * kModLen + 2 * kHidden + col));
+  float4 *xp = reinterpret_cast<float4 *>(x + (size_t)row * kHidden + col);
+  float4 xv = *xp;
+  xv.x = fmaf(g.x, y.x, xv.x);
+  xv.y = fmaf(g.y, y.y, xv.y);
+  xv.z = fmaf(g.z, y.z, xv.z);
+  xv.w = fmaf(g.w, y.w, xv.w);
+  *xp = xv;
+}
+
 // ---------------------------------------------------------------- host launchers
+// Split plan of a launch: whole tiles fill complete rounds of the pairs; the
+// tiles of the last, partial round are split along K into `splits` ranges
+// (a divisor of the k-block count leaving at least 16 k-blocks per range) so
+// that their units fill that round.  Only the out-projection splits (its
+// epilogue is linear in the product, so partial sums merge exactly as a sum);
+// no split when there is no partial buffer, the round is full, or no divisor
+// fits.
+void split_plan(int EPI, int M, int N, int K, int pairs, size_t part_bytes, int &n_full, int &splits) {
+  const int tiles = ((M + kTileM - 1) / kTileM) * (N / kBN);
+  const int num_kb = K / kBK;
+  n_full = tiles;
+  splits = 1;
+  if (EPI != EPI_OUT_RESIDUAL || pairs < 2) return;
+  const int full = tiles / pairs * pairs, rem = tiles - full;
+  if (rem == 0) return;
+  const int cand[5] = {8, 6, 4, 3, 2};
+  for (int S : cand) {
+    const int units = rem * S;
+    if (num_kb % S != 0 || num_kb / S < 16 || units > pairs || units > kMaxSplitUnits) continue;
+    if ((size_t)units * kSplitUnitBytes > part_bytes) continue;
+    n_full = full;
+    splits = S;
+    return;
+  }
+}
+
 template <int EPI>
 cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K, const EpiParams &ep,
                         cudaStream_t s) {
   static std::atomic<bool> attr_set[kMaxDevices];
   const cudaError_t e = set_smem_once(gemm_kernel<EPI>, (int)kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
+  const int tiles = ((M + kTileM - 1) / kTileM) * (N / kBN);
+  const int pairs = num_sms() / 2;
+  int n_full, splits;
+  split_plan(EPI, M, N, K, pairs, ep.part ? ep.part_bytes : 0, n_full, splits);
+  const int split_units = (tiles - n_full) * splits;
   // output boxes of 32 rows x 64 columns for the bf16 epilogues
   CUtensorMap tmO0 = tmA, tmO1 = tmA;
   if (EPI == EPI_STORE && !make_tmap_bf16(&tmO0, ep.C, (uint64_t)M, (uint64_t)ep.ldc, 32)) return cudaErrorInvalidValue;
@@ -479,12 +604,19 @@ cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, i
                              !make_tmap_bf16(&tmO1, ep.cat, (uint64_t)M, kCatCols, 32)))
     return cudaErrorInvalidValue;
   if (EPI == EPI_OUT_RESIDUAL && !make_tmap_f32_box32(&tmO0, ep.x, (uint64_t)M, kHidden)) return cudaErrorInvalidValue;
+  if (EPI == EPI_OUT_RESIDUAL && splits > 1 &&
+      !make_tmap_f32_box32(&tmO1, ep.part, (uint64_t)split_units * kTileM, kBN))
+    return cudaErrorInvalidValue;
   if (EPI == EPI_STORE_F32 && !make_tmap_f32_box32(&tmO0, ep.x, (uint64_t)M, (uint64_t)ep.ldc))
     return cudaErrorInvalidValue;
-  const int tiles = ((M + kTileM - 1) / kTileM) * (N / kBN);
-  const int pairs = num_sms() / 2;
-  const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmO0, tmO1, M, N, K, ep);
+  const int units = n_full + split_units;
+  const int grid = 2 * (units < pairs ? units : pairs);
+  gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
+  cudaError_t le = cudaGetLastError();
+  if (le != cudaSuccess || splits == 1) return le;
+  const int num_m = (M + kTileM - 1) / kTileM, num_n = N / kBN;
+  split_merge_residual_kernel<<<dim3(kTileM / 4, tiles - n_full), 256, 0, s>>>(
+      ep.part, n_full, splits, num_m, num_n, M > N ? 1 : 0, M, ep.x, ep.sid, ep.mod);
   return cudaGetLastError();
 }
 

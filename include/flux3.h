@@ -458,7 +458,7 @@ FLUX3_API flux3_status flux3_cfg_euler_step(float *latent, const float *v_uncond
                                             float guidance, float sigma, float sigma_next, void *next_input,
                                             void *stream);
 
-/* Largest T flux3_block_forward_noalloc accepts (its scratch is ~25 MB). */
+/* Largest T flux3_block_forward_noalloc accepts (its scratch is ~51 MB). */
 #define FLUX3_NOALLOC_MAX_TOKENS 512
 
 /* flux3_block_forward for callers that must not allocate device memory.
@@ -550,14 +550,25 @@ FLUX3_API flux3_status flux3_in_projection(const flux3_handle *h, int block_idx,
  *   (only columns 0..3071 are written). */
 FLUX3_API flux3_status flux3_attention(const void *qkv, int T, void *cat, void *stream);
 
+/* Bytes of scratch the out-projection's K split can use (96 partial tiles of
+ * 256 x 256 float32); the block workspace already holds it. */
+#define FLUX3_SPLIT_BYTES ((size_t)96 * 256 * 256 * 4)
+
 /* Output projection and gated residual (one GEMM with K = 3072 + 9216 over
  * cat = [attention | SwiGLU] against [Wattn_out | Wmlp_out]):
  *   x[t] += gate[s(t)] * (cat[t] [Wattn_out | Wmlp_out]^T)
  *   cat device bf16 [T, 12288]; stream_id device uint8 [T];
- *   mod device float32 [3, 9216]; x device float32 [T, 3072] (in place). */
+ *   mod device float32 [3, 9216]; x device float32 [T, 3072] (in place).
+ * split_buf: optional device scratch (16-byte aligned, split_bytes long, at
+ * most FLUX3_SPLIT_BYTES used; NULL for none).  With it, when the output
+ * tiles leave SMs idle in the GEMM's last round of tiles, those tiles are
+ * split along K, their float32 partial sums stored there and summed in a fixed
+ * order (deterministic) before the gated residual; the block forward calls do
+ * the same with their workspace.  Without it no tile is split. */
 FLUX3_API flux3_status flux3_out_projection(const flux3_handle *h, int block_idx, const void *cat,
                                             int T, const uint8_t *stream_id, const float *mod,
-                                            float *x, void *stream);
+                                            float *x, void *split_buf, size_t split_bytes,
+                                            void *stream);
 
 /* Plain tensor-core GEMM C = A B^T (fp32 accumulation, bf16 result), the core
  * the projections are built on.  A device bf16 [M, K], B device bf16 [N, K],

@@ -60,8 +60,15 @@ def test_batch_block_against_oracle(joint3):
 
 def test_batch_equals_per_sample_calls_full_size(joint3):
     """The text-to-image CFG pack [80 + 64x64 | 160 + 64x64] (8432 tokens):
-    the batched blocks leave each sample's rows exactly as a call on that
-    sample alone."""
+    the batched blocks leave each sample's rows as a call on that sample
+    alone.  The pack's out-projection has 396 output tiles, so on 74 CTA pairs
+    its last 26 tiles (rows of the second sample) are split along K; the
+    per-sample calls (204 tiles each) split nothing.  The only difference is
+    then the float32 summation order of those tiles and the bf16 roundings it
+    flips downstream (a flip moves one value by up to 2^-8 of itself; three
+    blocks measured 3.7e-3 of RMS), held to half the block criterion: max|err|
+    <= 1e-2 RMS, cosine >= 0.999999.  The first sample's rows lie in tiles no
+    split touches and are equal bit for bit."""
     _, blocks = joint3
     pack = synth.build_pack(T2I_PACK)
     x = synth.activations(82, pack.T, device=DEV)
@@ -75,7 +82,17 @@ def test_batch_equals_per_sample_calls_full_size(joint3):
         sub = x[r0:r1].clone()
         blocks.forward(sub, lay.segments, torch.from_numpy(lay.pos).to(DEV), mods[3 * b:3 * b + 3].contiguous())
         _sync_ok()
-        assert torch.equal(a[r0:r1], sub), f"sample {b}"
+        assert_close(f64(a[r0:r1]), f64(sub), 1e-2, 0.999999, f"sample {b}")
+    # the first sample's rows lie in whole tiles of the pack (rows < 4176 < 7680)
+    assert torch.equal(a[:pack.sample_start[1]], _first_alone(blocks, pack, x, mods))
+
+
+def _first_alone(blocks, pack, x, mods):
+    lay = pack.layouts[0]
+    sub = x[:pack.sample_start[1]].clone()
+    blocks.forward(sub, lay.segments, torch.from_numpy(lay.pos).to(DEV), mods[0:3].contiguous())
+    _sync_ok()
+    return sub
 
 
 def test_batch_rejects_bad_sample_tables(joint3):
@@ -109,7 +126,11 @@ def test_cfg_euler_step():
 def test_transformer_batch_against_oracle_and_per_sample():
     """The base model (no flow-map timestep) on a small two-sample pack: 1
     per-mode block, 2 joint blocks, against the oracle's per-sample calls; and
-    the batched call equals per-sample calls bit for bit."""
+    the batched call against per-sample calls.  The pack (267 tokens, 24
+    out-projection tiles) splits its out-projection's K in 3 ranges, the
+    per-sample calls (96 and 171 tokens, 12 tiles) in 6: the float32 sums are
+    grouped differently, so the two agree to summation order and the bf16
+    roundings it flips (1e-2 of RMS, cosine 0.999999), not bit for bit."""
     w = synth.cond_weights(880, device=DEV, flow=False)
     c = F3.Flux3Conditioning(w)
     w64 = {k: (None if v is None else [f64(t) for t in v] if isinstance(v, list) else f64(v)) for k, v in w.items()}
@@ -133,5 +154,5 @@ def test_transformer_batch_against_oracle_and_per_sample():
     for b, lay in enumerate(pack.layouts):
         vb = model.forward(ins[b], lay.segments, torch.from_numpy(lay.pos).to(DEV), t[b])
         _sync_ok()
-        assert torch.equal(v[rows:rows + vb.shape[0]], vb), f"sample {b}"
+        assert_close(f64(v[rows:rows + vb.shape[0]]), f64(vb), 1e-2, 0.999999, f"sample {b}")
         rows += vb.shape[0]

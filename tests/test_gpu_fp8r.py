@@ -172,7 +172,7 @@ def test_fp8r_handle_rejects_bf16_only_calls(fp8_block):
     p = buf.data_ptr()
     assert L.flux3_in_projection(blocks.handle, 0, p, T, p, p, p, p, sp) == F3.FLUX3_ERR_UNSUPPORTED
     x = torch.zeros((T, 3072), device=DEV)
-    assert L.flux3_out_projection(blocks.handle, 0, p, T, p, p, x.data_ptr(), sp) == F3.FLUX3_ERR_UNSUPPORTED
+    assert L.flux3_out_projection(blocks.handle, 0, p, T, p, p, x.data_ptr(), None, 0, sp) == F3.FLUX3_ERR_UNSUPPORTED
     segs = F3.segments_array([(0, T, 0)])
     assert L.flux3_block_forward_noalloc(blocks.handle, 0, x.data_ptr(), T, segs, 1, p, p, sp) == \
         F3.FLUX3_ERR_UNSUPPORTED

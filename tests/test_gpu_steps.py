@@ -165,27 +165,75 @@ def test_attention_full_size_sampled_rows(T):
     check_attention(f64(cat)[rows, :3072], ref, ref_abs, f"attention T={T}")
 
 
-@pytest.mark.parametrize("T", [96, 171, 4608])
-def test_out_projection(block1, T):
+OUT_LAYOUTS = {96: "block_t96", 4608: "block_1024sq_t4608", 6656: "stack28_1024sq_2ref512_t6656"}
+
+
+@pytest.mark.parametrize("T,split", [(96, False), (96, True), (171, False), (171, True), (512, True),
+                                     (4608, True), (6656, False), (6656, True)])
+def test_out_projection(block1, T, split):
+    """With a split buffer, the tiles of the GEMM's last, partial round of
+    tiles are split along K (all 12 tiles at 96 and 171 tokens, 24 at 512,
+    the 16 trailing tiles at 6656; none at 4608, whose last round is nearly
+    full); without it no tile is split.  Both against the float64 product."""
     w, blocks = block1
-    lay = synth.build_layout(RAGGED if T == 171 else synth.WORKLOADS[
-        "block_t96" if T == 96 else "block_1024sq_t4608"]["spec"])
+    spec = RAGGED if T == 171 else ([("txt", 160), ("image", (16, 20)), ("image_cond", (4, 8))] if T == 512
+                                    else synth.WORKLOADS[OUT_LAYOUTS[T]]["spec"])
+    lay = synth.build_layout(spec)
+    assert lay.T == T
     _, sid = layout_tensors(lay)
     cat = synth.bf16_matrix(9, T, 12288, device=DEV)
     x = synth.activations(9, T, device=DEV)
     x0 = x.clone()
     mods = synth.modulation(9, device=DEV)
+    buf = torch.empty(F3.FLUX3_SPLIT_BYTES // 4, dtype=torch.float32, device=DEV) if split else None
     F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), x.data_ptr(),
-                            _stream())
+                            _stream(), buf.data_ptr() if split else None, F3.FLUX3_SPLIT_BYTES if split else 0)
     assert F3.flux3_check_error(_stream()) == 0
     wf = weights_f64(w)
-    rows = np.arange(T) if T <= 200 else sample_rows(T, lay.segments)
+    rows = np.arange(T) if T <= 600 else sample_rows(T, lay.segments)
+    if T == 6656:   # every row of the trailing tiles (row blocks 24 and 25)
+        rows = np.union1d(rows, np.arange(6144, 6656, 7))
     c = f64(cat)[rows]
     y = c[:, :3072] @ wf["attn_out"].T + c[:, 3072:] @ wf["mlp_out"].T
     gate = f64(mods)[lay.stream_id[rows], 6144:]
     ref_delta = gate * y
     got_delta = f64(x)[rows] - f64(x0)[rows]
-    assert_close(got_delta, ref_delta, 1e-3, 0.999999, f"out_projection T={T}")
+    assert_close(got_delta, ref_delta, 1e-3, 0.999999, f"out_projection T={T} split={split}")
+
+
+def test_out_projection_split_matches_unsplit_up_to_summation_order(block1):
+    """The split changes only the order of the float32 sums of the trailing
+    tiles: the two results agree to float32 rounding, and rows outside the
+    trailing tiles are equal bit for bit."""
+    _, blocks = block1
+    lay = synth.build_layout(synth.WORKLOADS["stack28_1024sq_2ref512_t6656"]["spec"])
+    _, sid = layout_tensors(lay)
+    T = lay.T
+    cat = synth.bf16_matrix(10, T, 12288, device=DEV)
+    x = synth.activations(10, T, device=DEV)
+    mods = synth.modulation(10, device=DEV)
+    buf = torch.empty(F3.FLUX3_SPLIT_BYTES // 4, dtype=torch.float32, device=DEV)
+    a, b = x.clone(), x.clone()
+    F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), a.data_ptr(),
+                            _stream())
+    F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), b.data_ptr(),
+                            _stream(), buf.data_ptr(), F3.FLUX3_SPLIT_BYTES)
+    assert F3.flux3_check_error(_stream()) == 0
+    assert torch.equal(a[:6144], b[:6144])
+    da, db = f64(a[6144:]) - f64(x[6144:]), f64(b[6144:]) - f64(x[6144:])
+    assert not np.array_equal(da, db)
+    # float32 sums of 12288 products in another grouping: ~1e-5 of RMS per
+    # element, its maximum over 1.5 M elements a few times that; both bounds
+    # are far inside the 1e-3 the oracle comparison above allows
+    rms = np.sqrt(np.mean(da * da))
+    assert np.abs(da - db).max() <= 5e-4 * rms
+    assert np.sqrt(np.mean((da - db) ** 2)) <= 5e-5 * rms
+    # and twice the same split call: bit for bit (fixed merge order)
+    c = x.clone()
+    F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), c.data_ptr(),
+                            _stream(), buf.data_ptr(), F3.FLUX3_SPLIT_BYTES)
+    assert F3.flux3_check_error(_stream()) == 0
+    assert torch.equal(b, c)
 
 
 def test_timeout_path_reports_and_context_survives():
