@@ -36,7 +36,7 @@ FLUX3_MAX_SAMPLES = 16
 EXPORTED = (
     "flux3_default_config", "flux3_packed_weight_bytes", "flux3_workspace_bytes", "flux3_block_init",
     "flux3_block_forward", "flux3_stack_forward", "flux3_check_error", "flux3_status_string", "flux3_destroy",
-    "flux3_stream_ids", "flux3_rope_tables", "flux3_ln_modulate", "flux3_in_projection", "flux3_attention",
+    "flux3_stream_ids", "flux3_rope_tables", "flux3_prepare", "flux3_ln_modulate", "flux3_in_projection", "flux3_attention",
     "flux3_out_projection", "flux3_gemm_bf16", "flux3_selftest_wait_timeout", "flux3_block_forward_noalloc",
     "flux3_block_init_nvfp4", "flux3_quantize_nvfp4", "flux3_dequantize_block", "flux3_mode_blocks_forward",
     "flux3_block_init_fp8r", "flux3_quantize_fp8r",
@@ -129,6 +129,7 @@ def lib():
             "flux3_destroy": (None, [vp]),
             "flux3_stream_ids": (i, [segp, i, i, vp, vp]),
             "flux3_rope_tables": (i, [vp, i, f, vp, vp, vp]),
+            "flux3_prepare": (i, [segp, i, i, vp, f, vp, vp, vp, vp]),
             "flux3_ln_modulate": (i, [vp, i, vp, vp, f, vp, vp]),
             "flux3_in_projection": (i, [vp, i, vp, i, vp, vp, vp, vp, vp]),
             "flux3_attention": (i, [vp, i, vp, vp]),
@@ -420,6 +421,13 @@ def flux3_stream_ids(segments, T, stream_id, stream=0):
 
 def flux3_rope_tables(pos_ids, T, theta, cos_tab, sin_tab, stream=0):
     _check(lib().flux3_rope_tables(pos_ids, T, theta, cos_tab, sin_tab, stream), "flux3_rope_tables")
+
+
+def flux3_prepare(segments, T, pos_ids, theta, stream_id, cos_tab, sin_tab, stream=0):
+    """flux3_stream_ids and flux3_rope_tables in one launch."""
+    segs = segments_array(segments)
+    _check(lib().flux3_prepare(segs, len(segments), T, pos_ids, theta, stream_id, cos_tab, sin_tab, stream),
+           "flux3_prepare")
 
 
 def flux3_ln_modulate(x, T, stream_id, mod, eps, h, stream=0):

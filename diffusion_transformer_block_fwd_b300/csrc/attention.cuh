@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
+  // set-up above overlaps the previous kernel when launched as its programmatic dependent
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp >= kWarpTma) {
     // third warpgroup: one register share for all four of its warps (the
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace attn_tc
 
-cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s) {
+cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s, bool pdl) {
   using namespace attn_tc;
   static std::atomic<bool> attr_set[kMaxDevices];
   const int slot = device_slot();
@@ -350,8 +353,7 @@ cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat
   CUtensorMap tm;
   if (!make_tmap_bf16(&tm, qkv, (uint64_t)T, kQkvCols, kRows)) return cudaErrorInvalidValue;
   dim3 grid((T + 2 * kRows - 1) / (2 * kRows), kHeads);
-  attention_kernel<<<grid, kThreads, kSmem, s>>>(tm, T, cat);
-  return cudaGetLastError();
+  return launch_kernel(attention_kernel, grid, dim3(kThreads), kSmem, s, pdl, tm, T, cat);
 }
 
 }  // namespace flux3

@@ -2,6 +2,7 @@
 //
 //   stream_ids   segment table -> uint8 stream id per token
 //   rope_tables  pos ids [T, 4] -> cos / sin [T, 64] (pair p = 16 a + j of axis a)
+//   prepare      both in one launch (the forward calls)
 //   ln_modulate  x fp32 [T, 3072] -> h = (1 + scale[s]) * LN(x) + shift[s], bf16
 //
 // ln_modulate is HBM-bound: 12 KB read + 6 KB written per token.  One warp per
@@ -24,18 +25,6 @@ struct SegTable {
   int n;
 };
 
-__global__ void stream_ids_kernel(SegTable tab, int T, uint8_t *sid) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= T) return;
-  int s = -1;
-  for (int i = 0; i < tab.n; ++i)
-    if (t >= tab.start[i] && t < tab.start[i] + tab.len[i]) s = tab.stream[i];
-  if (s < 0) {  // the host validated coverage; keep the kernel honest anyway
-    record_error(DEVERR_BOUNDS);
-    s = 0;
-  }
-  sid[t] = (uint8_t)s;
-}
 
 // Angles are carried in turns (angle / 2 pi) as an unevaluated float pair
 // hi + lo: hi = pos * fh (rounded), lo = its exact rounding error (fma) plus
@@ -48,9 +37,8 @@ struct RopeFreqs {
   float hi[16], lo[16];
 };
 
-__global__ void rope_tables_kernel(const float *pos, int T, RopeFreqs fr, float *cos_tab, float *sin_tab) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= T * kRopePairs) return;
+__device__ __forceinline__ void rope_entry(const float *pos, const RopeFreqs &fr, int i, float *cos_tab,
+                                           float *sin_tab) {
   const int t = i / kRopePairs, p = i % kRopePairs;
   const int axis = p / 16, j = p % 16;
   const float x = __ldg(pos + (size_t)t * 4 + axis);
@@ -63,12 +51,49 @@ __global__ void rope_tables_kernel(const float *pos, int T, RopeFreqs fr, float 
   sin_tab[i] = sn;
 }
 
+__global__ void rope_tables_kernel(const float *pos, int T, RopeFreqs fr, float *cos_tab, float *sin_tab) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * kRopePairs) return;
+  rope_entry(pos, fr, i, cos_tab, sin_tab);
+}
+
+__device__ __forceinline__ int stream_of(const SegTable &tab, int t) {
+  int s = -1;
+  for (int i = 0; i < tab.n; ++i)
+    if (t >= tab.start[i] && t < tab.start[i] + tab.len[i]) s = tab.stream[i];
+  if (s < 0) {  // the host validated coverage; keep the kernel honest anyway
+    record_error(DEVERR_BOUNDS);
+    s = 0;
+  }
+  return s;
+}
+
+__global__ void stream_ids_kernel(SegTable tab, int T, uint8_t *sid) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  sid[t] = (uint8_t)stream_of(tab, t);
+}
+
+// The per-call preparation in one launch: thread i writes RoPE pair i % 64 of
+// token i / 64, and the token's first thread its stream id.
+__global__ void prepare_kernel(SegTable tab, const float *pos, int T, RopeFreqs fr, uint8_t *sid, float *cos_tab,
+                               float *sin_tab) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T * kRopePairs) return;
+  rope_entry(pos, fr, i, cos_tab, sin_tab);
+  if (i % kRopePairs == 0) sid[i / kRopePairs] = (uint8_t)stream_of(tab, i / kRopePairs);
+}
+
 constexpr int kLnWarps = 8;
 
 __global__ void __launch_bounds__(kLnWarps * 32, 2)
     ln_modulate_kernel(const float *__restrict__ x, int T, const uint8_t *__restrict__ sid,
                        const float *__restrict__ mod, float eps, __nv_bfloat16 *__restrict__ h) {
   constexpr int kVec = kHidden / (32 * 4);  // 24 float4 per lane
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * kLnWarps + warp;
   if (t >= T) return;
@@ -125,8 +150,9 @@ __global__ void selftest_wait_kernel(unsigned long long timeout_ns) {
 
 }  // namespace ew_detail
 
-cudaError_t launch_stream_ids(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, cudaStream_t s) {
-  using namespace ew_detail;
+namespace ew_detail {
+
+SegTable seg_table(const flux3_segment *segs, int n_segs) {
   SegTable tab{};
   tab.n = n_segs;
   for (int i = 0; i < n_segs; ++i) {
@@ -134,14 +160,10 @@ cudaError_t launch_stream_ids(const flux3_segment *segs, int n_segs, int T, uint
     tab.len[i] = segs[i].len;
     tab.stream[i] = segs[i].stream;
   }
-  stream_ids_kernel<<<(T + 255) / 256, 256, 0, s>>>(tab, T, sid);
-  return cudaGetLastError();
+  return tab;
 }
 
-cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_tab, float *sin_tab,
-                               cudaStream_t s) {
-  using namespace ew_detail;
-  const int n = T * kRopePairs;
+RopeFreqs rope_freqs(float theta) {
   RopeFreqs fr;
   const double inv_two_pi = 0.15915494309189535;
   for (int j = 0; j < 16; ++j) {
@@ -149,15 +171,39 @@ cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_
     fr.hi[j] = (float)turns;
     fr.lo[j] = (float)(turns - (double)fr.hi[j]);
   }
-  rope_tables_kernel<<<(n + 255) / 256, 256, 0, s>>>(pos, T, fr, cos_tab, sin_tab);
+  return fr;
+}
+
+}  // namespace ew_detail
+
+cudaError_t launch_stream_ids(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, cudaStream_t s) {
+  using namespace ew_detail;
+  stream_ids_kernel<<<(T + 255) / 256, 256, 0, s>>>(seg_table(segs, n_segs), T, sid);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_tab, float *sin_tab,
+                               cudaStream_t s) {
+  using namespace ew_detail;
+  const int n = T * kRopePairs;
+  rope_tables_kernel<<<(n + 255) / 256, 256, 0, s>>>(pos, T, rope_freqs(theta), cos_tab, sin_tab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, const float *pos, float theta,
+                           float *cos_tab, float *sin_tab, cudaStream_t s) {
+  using namespace ew_detail;
+  const int n = T * kRopePairs;
+  prepare_kernel<<<(n + 255) / 256, 256, 0, s>>>(seg_table(segs, n_segs), pos, T, rope_freqs(theta), sid, cos_tab,
+                                                 sin_tab);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ln_modulate(const float *x, int T, const uint8_t *sid, const float *mod, float eps,
-                               __nv_bfloat16 *h, cudaStream_t s) {
+                               __nv_bfloat16 *h, cudaStream_t s, bool pdl) {
   using namespace ew_detail;
-  ln_modulate_kernel<<<(T + kLnWarps - 1) / kLnWarps, kLnWarps * 32, 0, s>>>(x, T, sid, mod, eps, h);
-  return cudaGetLastError();
+  return launch_kernel(ln_modulate_kernel, dim3((T + kLnWarps - 1) / kLnWarps), dim3(kLnWarps * 32), 0, s, pdl, x,
+                       T, sid, mod, eps, h);
 }
 
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, cudaStream_t s) {

@@ -245,8 +245,10 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
   if (ws_bytes < workspace_layout(T, nullptr, nullptr, fp4)) return FLUX3_ERR_WORKSPACE;
   workspace_layout(T, static_cast<uint8_t *>(workspace), &ws, fp4);
 
-  F3_CUDA(launch_stream_ids(rows, n_segs, T, ws.sid, s));
-  F3_CUDA(launch_rope_tables(pos, T, h->cfg.rope_theta, ws.cos_tab, ws.sin_tab, s));
+  // the first launch waits for everything before it on the stream; each later
+  // one is a programmatic dependent of the kernel before it (its set-up runs
+  // while that kernel finishes)
+  F3_CUDA(launch_prepare(rows, n_segs, T, ws.sid, pos, h->cfg.rope_theta, ws.cos_tab, ws.sin_tab, s));
   CUtensorMap tmH, tmCat, tmWin, tmWout;
   if (!make_tmap_bf16(&tmH, ws.h, (uint64_t)T, kHidden, kBM)) return FLUX3_ERR_CUDA;
   if (!make_tmap_bf16(&tmCat, ws.cat, (uint64_t)T, kCatCols, kBM)) return FLUX3_ERR_CUDA;
@@ -254,9 +256,9 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
               !make_tmap_bf16(&tmWout, ws.w_out, kHidden, kCatCols, kBoxB)))
     return FLUX3_ERR_CUDA;
   for (int b = first; b < first + count; ++b) {
-    if (h->cfg.wfmt == FLUX3_W_NVFP4) F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s));
-    if (h->cfg.wfmt == FLUX3_W_FP8R) F3_CUDA(launch_dequantize_fp8r_block(h->fp8[b], ws.w_in, ws.w_out, s));
-    F3_CUDA(launch_ln_modulate(x, T, ws.sid, mod, h->cfg.eps_ln, ws.h, s));
+    if (h->cfg.wfmt == FLUX3_W_NVFP4) F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s, true));
+    if (h->cfg.wfmt == FLUX3_W_FP8R) F3_CUDA(launch_dequantize_fp8r_block(h->fp8[b], ws.w_in, ws.w_out, s, true));
+    F3_CUDA(launch_ln_modulate(x, T, ws.sid, mod, h->cfg.eps_ln, ws.h, s, true));
     EpiParams ep{};
     ep.qkv = ws.qkv;
     ep.cat = ws.cat;
@@ -265,11 +267,11 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     ep.qnorm = block_norms(h, b);
     ep.knorm = block_norms(h, b) + kHeadDim;
     ep.eps_rms = h->cfg.eps_rms;
-    F3_CUDA(launch_gemm(EPI_IN_PROJ, tmH, fp4 ? tmWin : h->tm_in[b], T, kInRows, kHidden, ep, s));
+    F3_CUDA(launch_gemm(EPI_IN_PROJ, tmH, fp4 ? tmWin : h->tm_in[b], T, kInRows, kHidden, ep, s, true));
     for (int smp = 0; smp < n_samples; ++smp) {   // attention within each sample
       const int r0 = sample_start[smp];
       F3_CUDA(launch_attention(ws.qkv + (size_t)r0 * kQkvCols, sample_start[smp + 1] - r0,
-                               ws.cat + (size_t)r0 * kCatCols, s));
+                               ws.cat + (size_t)r0 * kCatCols, s, true));
     }
     EpiParams eo{};
     eo.x = x;
@@ -277,7 +279,7 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     eo.mod = mod;
     eo.part = ws.part;
     eo.part_bytes = kSplitBytes;
-    F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, fp4 ? tmWout : h->tm_out[b], T, kHidden, kCatCols, eo, s));
+    F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, fp4 ? tmWout : h->tm_out[b], T, kHidden, kCatCols, eo, s, true));
   }
   return FLUX3_OK;
 }
@@ -736,6 +738,15 @@ flux3_status flux3_rope_tables(const float *pos_ids, int T, float theta, float *
                                void *stream) {
   if (!pos_ids || !cos_tab || !sin_tab || T < 1 || T > kMaxTokensLimit || !(theta > 0.f)) return FLUX3_ERR_INVALID_ARG;
   return cuda_status(launch_rope_tables(pos_ids, T, theta, cos_tab, sin_tab, static_cast<cudaStream_t>(stream)));
+}
+
+flux3_status flux3_prepare(const flux3_segment *segs, int n_segs, int T, const float *pos_ids, float theta,
+                           uint8_t *stream_id, float *cos_tab, float *sin_tab, void *stream) {
+  if (!stream_id || !pos_ids || !cos_tab || !sin_tab || !(theta > 0.f)) return FLUX3_ERR_INVALID_ARG;
+  if (T > kMaxTokensLimit) return FLUX3_ERR_INVALID_ARG;
+  F3_TRY(segments_ok(segs, n_segs, T));
+  return cuda_status(launch_prepare(segs, n_segs, T, stream_id, pos_ids, theta, cos_tab, sin_tab,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 flux3_status flux3_ln_modulate(const float *x, int T, const uint8_t *stream_id, const float *mod, float eps, void *hout,

@@ -87,15 +87,38 @@ cudaError_t set_smem_once(Kernel kernel, int bytes, std::atomic<bool> (&done)[kM
   return e;
 }
 
+// Launches `kernel` on stream s.  With pdl, as a programmatic dependent launch
+// of the previous kernel on s: the kernel may be scheduled while that one
+// finishes (its CTAs set up, then wait in griddep_wait), which hides the
+// launch gap between the kernels of a block.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K,
-                        const EpiParams &ep, cudaStream_t s);
+                        const EpiParams &ep, cudaStream_t s, bool pdl = false);
 
 cudaError_t launch_stream_ids(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, cudaStream_t s);
 cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_tab, float *sin_tab,
                                cudaStream_t s);
+// Stream ids and RoPE tables in one launch (the per-call preparation).
+cudaError_t launch_prepare(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, const float *pos, float theta,
+                           float *cos_tab, float *sin_tab, cudaStream_t s);
 cudaError_t launch_ln_modulate(const float *x, int T, const uint8_t *sid, const float *mod, float eps,
-                               __nv_bfloat16 *h, cudaStream_t s);
+                               __nv_bfloat16 *h, cudaStream_t s, bool pdl = false);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
-cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s);
+cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s, bool pdl = false);
 
 }  // namespace flux3

@@ -94,6 +94,9 @@ __global__ void __launch_bounds__(256)
     const float mag = e4m3_decode_f(c & 0x7Fu);
     value_of_code[c] = (c & 0x80u) ? -mag : mag;
   }
+  // the expanded weights overwrite what the previous block's GEMMs read
+  griddep_wait();
+  griddep_launch_dependents();
   __syncthreads();
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < kInChunks + kOutChunks; i += gridDim.x * blockDim.x) {
     const bool in = i < kInChunks;
@@ -134,9 +137,9 @@ cudaError_t launch_quantize_fp8r(const __nv_bfloat16 *w, int rows, int cols, uin
 }
 
 cudaError_t launch_dequantize_fp8r_block(const fp8r_detail::Fp8rBlockView &v, __nv_bfloat16 *w_in,
-                                         __nv_bfloat16 *w_out, cudaStream_t s) {
-  fp8r_detail::dequantize_fp8r_block_kernel<<<num_sms() * 8, 256, 0, s>>>(v, w_in, w_out);
-  return cudaGetLastError();
+                                         __nv_bfloat16 *w_out, cudaStream_t s, bool pdl = false) {
+  return launch_kernel(fp8r_detail::dequantize_fp8r_block_kernel, dim3(num_sms() * 8), dim3(256), 0, s, pdl, v,
+                       w_in, w_out);
 }
 
 }  // namespace flux3

@@ -29,8 +29,6 @@
 // along K into ranges (out-projection only): each range stores its float32
 // partial tile, and split_merge_residual_kernel sums a tile's ranges in a fixed
 // order (deterministic) and applies the gated residual.
-// L2: the operand that every round re-reads is loaded with evict_last, the
-// streamed one with evict_first.
 // Every wait is bounded (see mbar_wait); on a timeout the CTA drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 
@@ -391,16 +389,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
+  // set-up above overlaps the previous kernel when launched as its programmatic dependent
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer (both CTAs): this CTA's 128 A rows and
-      // 128 B rows of each stage, completing on the leader's full barrier.
-      // The operand the tile order re-reads in every round of tiles (B when
-      // consecutive pairs sweep the columns, else A) is kept in L2 with
-      // evict_last; the other one streams with evict_first.
-      const uint64_t keep = l2_policy_evict_last(), stream_once = l2_policy_evict_first();
-      const uint64_t pol_a = n_fast ? stream_once : keep, pol_b = n_fast ? keep : stream_once;
+      // 128 B rows of each stage, completing on the leader's full barrier
       int last_phase[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
@@ -417,8 +413,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t full_leader = map_to_cta(smem_addr(&ctl->full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&ctl->full[stage], kPairStageBytes);
-          tma_load_2d_pair_hint(smA + stage * kABytes, &tmA, full_leader, kb * kBK, a_row, pol_a);
-          tma_load_2d_pair_hint(smB + stage * kBBytes, &tmB, full_leader, kb * kBK, b_row, pol_b);
+          tma_load_2d_pair(smA + stage * kABytes, &tmA, full_leader, kb * kBK, a_row);
+          tma_load_2d_pair(smB + stage * kBBytes, &tmB, full_leader, kb * kBK, b_row);
           last_phase[stage] = (int)phase;
           if (++stage == kStages) {
             stage = 0;
@@ -533,6 +529,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 __global__ void split_merge_residual_kernel(const float *__restrict__ part, int n_full, int splits, int num_m,
                                             int num_n, int n_fast, int M, float *__restrict__ x,
                                             const uint8_t *__restrict__ sid, const float *__restrict__ mod) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int i = blockIdx.y;                                 // trailing tile
   const int r = blockIdx.x * 4 + threadIdx.x / 64;          // row in the tile
   const int c = (threadIdx.x % 64) * 4;                     // column in the tile
@@ -588,7 +586,7 @@ void split_plan(int EPI, int M, int N, int K, int pairs, size_t part_bytes, int 
 
 template <int EPI>
 cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K, const EpiParams &ep,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool pdl) {
   static std::atomic<bool> attr_set[kMaxDevices];
   const cudaError_t e = set_smem_once(gemm_kernel<EPI>, (int)kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
@@ -611,25 +609,25 @@ cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, i
     return cudaErrorInvalidValue;
   const int units = n_full + split_units;
   const int grid = 2 * (units < pairs ? units : pairs);
-  gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
-  cudaError_t le = cudaGetLastError();
+  cudaError_t le = launch_kernel(gemm_kernel<EPI>, dim3(grid), dim3(kThreads), kSmemBytes, s, pdl, tmA, tmB, tmO0,
+                                 tmO1, M, N, K, n_full, splits, ep);
   if (le != cudaSuccess || splits == 1) return le;
   const int num_m = (M + kTileM - 1) / kTileM, num_n = N / kBN;
-  split_merge_residual_kernel<<<dim3(kTileM / 4, tiles - n_full), 256, 0, s>>>(
-      ep.part, n_full, splits, num_m, num_n, M > N ? 1 : 0, M, ep.x, ep.sid, ep.mod);
-  return cudaGetLastError();
+  return launch_kernel(split_merge_residual_kernel, dim3(kTileM / 4, tiles - n_full), dim3(256), 0, s, pdl,
+                       static_cast<const float *>(ep.part), n_full, splits, num_m, num_n, M > N ? 1 : 0, M, ep.x,
+                       ep.sid, ep.mod);
 }
 
 }  // namespace gemm_detail
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K,
-                        const EpiParams &ep, cudaStream_t s) {
+                        const EpiParams &ep, cudaStream_t s, bool pdl) {
   using namespace gemm_detail;
   switch (mode) {
-    case EPI_STORE: return launch_mode<EPI_STORE>(tmA, tmB, M, N, K, ep, s);
-    case EPI_IN_PROJ: return launch_mode<EPI_IN_PROJ>(tmA, tmB, M, N, K, ep, s);
-    case EPI_OUT_RESIDUAL: return launch_mode<EPI_OUT_RESIDUAL>(tmA, tmB, M, N, K, ep, s);
-    case EPI_STORE_F32: return launch_mode<EPI_STORE_F32>(tmA, tmB, M, N, K, ep, s);
+    case EPI_STORE: return launch_mode<EPI_STORE>(tmA, tmB, M, N, K, ep, s, pdl);
+    case EPI_IN_PROJ: return launch_mode<EPI_IN_PROJ>(tmA, tmB, M, N, K, ep, s, pdl);
+    case EPI_OUT_RESIDUAL: return launch_mode<EPI_OUT_RESIDUAL>(tmA, tmB, M, N, K, ep, s, pdl);
+    case EPI_STORE_F32: return launch_mode<EPI_STORE_F32>(tmA, tmB, M, N, K, ep, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -173,6 +173,9 @@ __global__ void __launch_bounds__(256)
   __shared__ float2 pair_of_byte[256];
   __shared__ float gs[6];
   pair_of_byte[threadIdx.x] = make_float2(e2m1_decode(threadIdx.x & 0xFu), e2m1_decode(threadIdx.x >> 4));
+  // the expanded weights overwrite what the previous block's GEMMs read
+  griddep_wait();
+  griddep_launch_dependents();
   if (threadIdx.x < 6) gs[threadIdx.x] = v.globals[threadIdx.x];
   __syncthreads();
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < kInGroups + kOutGroups; i += gridDim.x * blockDim.x) {
@@ -225,10 +228,10 @@ cudaError_t launch_quantize_nvfp4(const __nv_bfloat16 *w, int rows, int cols, ui
 }
 
 cudaError_t launch_dequantize_block(const fp4_detail::Fp4BlockView &v, __nv_bfloat16 *w_in, __nv_bfloat16 *w_out,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, bool pdl = false) {
   using namespace fp4_detail;
-  fp4_detail::dequantize_block_kernel<<<num_sms() * 8, 256, 0, s>>>(v, w_in, w_out);
-  return cudaGetLastError();
+  return launch_kernel(fp4_detail::dequantize_block_kernel, dim3(num_sms() * 8), dim3(256), 0, s, pdl, v, w_in,
+                       w_out);
 }
 
 }  // namespace flux3

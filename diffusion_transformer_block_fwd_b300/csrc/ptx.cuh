@@ -30,6 +30,19 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched as a programmatic dependent of the previous kernel on its
+// stream may start while that kernel is still running; it must wait here
+// before it reads what the previous kernels wrote or writes what they read
+// (no-op for an ordinary launch).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream, if launched as a programmatic dependent,
+// be scheduled once every CTA of this grid has issued this (or exited); that
+// kernel still waits in griddep_wait for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
@@ -133,29 +146,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *t
       "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%3, "
       "%4}], [%2];" ::"r"(smem_addr(dst)),
       "l"(tm), "r"(bar_cluster), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-// L2 cache policies for TMA loads: evict_last keeps an operand that later
-// tiles read again resident in L2; evict_first lets a streamed operand leave
-// first.
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-// tma_load_2d_pair with an L2 cache policy.
-__device__ __forceinline__ void tma_load_2d_pair_hint(void *dst, const CUtensorMap *tm, uint32_t bar_cluster, int c0,
-                                                      int c1, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint "
-      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
-      "l"(tm), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
 

@@ -503,7 +503,10 @@ FLUX3_API void flux3_destroy(flux3_handle *h);
 
 /* ------------------------------------------------------------------------
  * Step entry points: the stages of one block, exposed so each can be checked
- * on its own.  flux3_block_forward is exactly these in sequence.
+ * on its own.  flux3_block_forward is flux3_prepare, flux3_ln_modulate,
+ * flux3_in_projection, flux3_attention and flux3_out_projection in sequence
+ * (its own launches after the first are programmatic dependents of the launch
+ * before them, so each kernel's set-up overlaps the previous one's tail).
  * ------------------------------------------------------------------------ */
 
 /* Per-token stream id from the segment table (validated as above).
@@ -518,6 +521,12 @@ FLUX3_API flux3_status flux3_stream_ids(const flux3_segment *segs, int n_segs, i
  *   pos_ids device float32 [T, 4]; cos_tab, sin_tab device float32 [T, 64] (outputs) */
 FLUX3_API flux3_status flux3_rope_tables(const float *pos_ids, int T, float theta,
                                          float *cos_tab, float *sin_tab, void *stream);
+
+/* flux3_stream_ids and flux3_rope_tables in one launch (what the forward
+ * calls run once per call): stream_id [T], cos_tab, sin_tab [T, 64] as above. */
+FLUX3_API flux3_status flux3_prepare(const flux3_segment *segs, int n_segs, int T, const float *pos_ids,
+                                     float theta, uint8_t *stream_id, float *cos_tab, float *sin_tab,
+                                     void *stream);
 
 /* LayerNorm (no affine) + per-stream modulation:
  *   h[t] = (1 + scale[s(t)]) * (x[t] - mean) / sqrt(var + eps) + shift[s(t)]

@@ -87,6 +87,8 @@ def test_segment_validation_rejects_bad_tables(segments, T):
     arr, n = _segs(segments)
     st = F3.lib().flux3_stream_ids(arr, n, T, ctypes.c_void_p(16), None)
     assert st == F3.FLUX3_ERR_INVALID_ARG
+    st = F3.lib().flux3_prepare(arr, n, T, 16, ctypes.c_float(1e4), 16, 16, 16, None)
+    assert st == F3.FLUX3_ERR_INVALID_ARG
 
 
 def test_forward_argument_validation_before_any_launch():
@@ -120,6 +122,8 @@ def test_forward_argument_validation_before_any_launch():
     assert L.flux3_attention(16, 0, 16, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_ln_modulate(16, 4, 16, 16, ctypes.c_float(0.0), 16, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_rope_tables(16, 4, ctypes.c_float(-1.0), 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_prepare(arr, n, 8, 16, ctypes.c_float(-1.0), 16, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_prepare(arr, n, 8, None, ctypes.c_float(1e4), 16, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_selftest_wait_timeout(0, None) == F3.FLUX3_ERR_INVALID_ARG
 
 

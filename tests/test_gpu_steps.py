@@ -51,6 +51,25 @@ def test_rope_tables_match_oracle_angles():
     assert np.abs(sn.cpu().numpy() - np.sin(ang)).max() < 1e-6
 
 
+def test_prepare_equals_stream_ids_and_rope_tables():
+    """The forward calls' one-launch preparation writes exactly what the two
+    separate step entry points write."""
+    for spec in (RAGGED, synth.WORKLOADS["stack28_nvfp4_1024sq_10ref512_t14848"]["spec"], [("image", (1, 1))]):
+        lay = synth.build_layout(spec)
+        T = lay.T
+        pd = torch.from_numpy(lay.pos).to(DEV)
+        sid = torch.full((T,), 255, dtype=torch.uint8, device=DEV)
+        cs, sn = torch.empty((T, 64), device=DEV), torch.empty((T, 64), device=DEV)
+        F3.flux3_prepare(lay.segments, T, pd.data_ptr(), 1e4, sid.data_ptr(), cs.data_ptr(), sn.data_ptr(), _stream())
+        sid2 = torch.full((T,), 255, dtype=torch.uint8, device=DEV)
+        cs2, sn2 = torch.empty((T, 64), device=DEV), torch.empty((T, 64), device=DEV)
+        F3.flux3_stream_ids(lay.segments, T, sid2.data_ptr(), _stream())
+        F3.flux3_rope_tables(pd.data_ptr(), T, 1e4, cs2.data_ptr(), sn2.data_ptr(), _stream())
+        assert F3.flux3_check_error(_stream()) == 0
+        assert np.array_equal(sid.cpu().numpy(), lay.stream_id)
+        assert torch.equal(sid, sid2) and torch.equal(cs, cs2) and torch.equal(sn, sn2)
+
+
 @pytest.mark.parametrize("T", [1, 37, 171, 4608])
 def test_ln_modulate(T):
     lay = synth.build_layout(RAGGED) if T == 171 else None
