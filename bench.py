@@ -79,6 +79,28 @@ def out_proj_splits(T, sms):
     return 1
 
 
+def attn_splits(T, sms):
+    """Key ranges the attention's trailing units take at T tokens on `sms`
+    SMs (1: no split), the plan the library takes: the units of the last,
+    partial wave of one CTA per SM are split into the most ranges (<= 8, each
+    of >= 4 key tiles) that fit in that wave and in the 24 MiB split buffer.
+    A split adds one merge launch."""
+    units = -(-T // 256) * 24
+    rem = units % sms if units >= sms else units
+    nt = -(-T // 128)
+    if rem == 0:
+        return 1
+    for S in range(8, 1, -1):
+        if rem * S <= sms and nt // S >= 4 and rem * S * 2 * 128 * 132 * 4 <= 96 * 256 * 256 * 4:
+            return S
+    return 1
+
+
+def merges(T, sms):
+    """Merge launches of one block at T tokens (out-projection, attention)."""
+    return (out_proj_splits(T, sms) > 1) + (attn_splits(T, sms) > 1)
+
+
 def kernel_bytes(T):
     """Algorithmic HBM bytes per launch of the memory-bound kernels."""
     return {"ln_modulate": T * (3072 * 4 + 3072 * 2), "rope_tables": T * (16 + 2 * 64 * 4), "stream_ids": T}
@@ -467,7 +489,7 @@ def run_ours(args):
                                cat.data_ptr(), sp)
         if evs is not None:
             evs[3].record(stream)
-        F3.flux3_attention(qkv.data_ptr(), T, cat.data_ptr(), sp)
+        F3.flux3_attention(qkv.data_ptr(), T, cat.data_ptr(), sp, split.data_ptr(), F3.FLUX3_SPLIT_BYTES)
         if evs is not None:
             evs[4].record(stream)
         F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), x.data_ptr(),
@@ -476,7 +498,7 @@ def run_ours(args):
             evs[5].record(stream)
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    launches_per_step = 5 + (1 if out_proj_splits(T, sms) > 1 else 0)
+    launches_per_step = 5 + merges(T, sms)
     torch.cuda.synchronize(dev)          # inputs were made on the default stream
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -678,7 +700,7 @@ def measure_stack(name, steps, warmup, dev, local, world):
             evs[1].record(stream)
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    per_call_launches = 2 + nb * (4 + (1 if fp4 or fp8 else 0) + (1 if out_proj_splits(T, sms) > 1 else 0))
+    per_call_launches = 1 + nb * (4 + (1 if fp4 or fp8 else 0) + merges(T, sms))
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             x.copy_(x0)
@@ -803,7 +825,7 @@ def run_modes(args, rank, world, local, dev):
             evs[1].record(stream)
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    launches = sum(2 + nb * (4 + (out_proj_splits(c, sms) > 1)) for c in counts if c)
+    launches = sum(1 + nb * (4 + merges(c, sms)) for c in counts if c)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             x.copy_(x0)
@@ -973,8 +995,8 @@ def run_model(args, rank, world, local, dev):
     hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
     tflops = world * flops / (step_ms * 1e-3) / 1e12
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    per_call_launches = (15 + sum(2 + nm * (4 + (out_proj_splits(c, sms) > 1)) for c in counts if c)
-                         + 2 + nb * (4 + (out_proj_splits(T, sms) > 1)) + 1
+    per_call_launches = (15 + sum(1 + nm * (4 + merges(c, sms)) for c in counts if c)
+                         + 1 + nb * (4 + merges(T, sms)) + 1
                          + sum(1 for s_ in lay.segments) + 2 + 1)
     line = {"metric": METRIC, "value": value, "unit": UNIT_MODEL,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -1088,10 +1110,11 @@ def run_cfg(args, rank, world, local, dev):
     # (2 + 4 per block, one more attention launch per block for each further sample); the guided update
     n_s = len(counts)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    launches = (sum(13 + len(lay.segments) + sum(2 + nm * (4 + (out_proj_splits(c[m], sms) > 1))
+    launches = (sum(13 + len(lay.segments) + sum(1 + nm * (4 + merges(c[m], sms))
                                                   for m in range(3) if c[m]) + 2
                     for c, lay in zip(counts, pack.layouts))
-                + 2 + nb * (4 + (out_proj_splits(pack.T, sms) > 1)) + nb * (n_s - 1) + 1)
+                + 1 + nb * (4 + (out_proj_splits(pack.T, sms) > 1)
+                            + sum(1 + (attn_splits(l.T, sms) > 1) for l in pack.layouts) - 1) + 1)
     flops = steps * per_call
     hbm, bf16_burst, bf16_sust, peak_src = load_peaks()
     tflops = world * flops / (step_ms * 1e-3) / 1e12

@@ -132,7 +132,7 @@ def lib():
             "flux3_prepare": (i, [segp, i, i, vp, f, vp, vp, vp, vp]),
             "flux3_ln_modulate": (i, [vp, i, vp, vp, f, vp, vp]),
             "flux3_in_projection": (i, [vp, i, vp, i, vp, vp, vp, vp, vp]),
-            "flux3_attention": (i, [vp, i, vp, vp]),
+            "flux3_attention": (i, [vp, i, vp, vp, sz, vp]),
             "flux3_out_projection": (i, [vp, i, vp, i, vp, vp, vp, vp, sz, vp]),
             "flux3_gemm_bf16": (i, [vp, vp, vp, i, i, i, vp]),
             "flux3_selftest_wait_timeout": (i, [i, vp]),
@@ -439,8 +439,8 @@ def flux3_in_projection(h, block_idx, hmod, T, cos_tab, sin_tab, qkv, cat, strea
            "flux3_in_projection")
 
 
-def flux3_attention(qkv, T, cat, stream=0):
-    _check(lib().flux3_attention(qkv, T, cat, stream), "flux3_attention")
+def flux3_attention(qkv, T, cat, stream=0, split_buf=None, split_bytes=0):
+    _check(lib().flux3_attention(qkv, T, cat, split_buf, split_bytes, stream), "flux3_attention")
 
 
 FLUX3_SPLIT_BYTES = 96 * 256 * 256 * 4

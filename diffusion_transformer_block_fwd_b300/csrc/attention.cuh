@@ -63,6 +63,19 @@ struct Ctl {
 
 constexpr size_t kSmem = 1024 + 2 * kTileBytes /*Q_A, Q_B*/ + 2 * kStages * kTileBytes /*K, V*/ + sizeof(Ctl);
 
+// Work items: item b < n_full is unit b (all keys); each later unit is split
+// into `splits` key ranges, item n_full + v covering unit n_full + v / splits
+// and its key tiles [ks * nt / splits, (ks + 1) * nt / splits), ks = v % splits.
+// Units run head-major: unit u is query-tile pair u % n_qp of head u / n_qp.
+// A split item writes its rows unnormalised to part[v] (kPartRowFloats floats
+// per query row: 128 output values, the row max in the log2 domain, the row sum).
+constexpr int kPartRowFloats = 132;
+constexpr size_t kPartItemBytes = (size_t)2 * kRows * kPartRowFloats * 4;
+struct Plan {
+  int n_full, splits, n_qp;
+  float *part;
+};
+
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   const unsigned long long t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -95,8 +108,36 @@ __device__ __forceinline__ void add2(float &s0, float &s1, float p0, float p1) {
       : "f"(p0), "f"(p1));
 }
 
+// The unit, key range and partial slot (-1: none) of work item b.
+struct Item {
+  int head, q0, j0, nt, slot;
+};
+__device__ __forceinline__ Item item_of(int b, int T, const Plan &plan) {
+  const int nt_all = (T + kRows - 1) / kRows;
+  Item it;
+  int unit;
+  if (b < plan.n_full) {
+    unit = b;
+    it.j0 = 0;
+    it.nt = nt_all;
+    it.slot = -1;
+  } else {
+    const int v = b - plan.n_full, ks = v % plan.splits;
+    unit = plan.n_full + v / plan.splits;
+    it.j0 = ks * nt_all / plan.splits;
+    it.nt = (ks + 1) * nt_all / plan.splits - it.j0;
+    it.slot = v;
+  }
+  it.head = unit / plan.n_qp;
+  it.q0 = (unit % plan.n_qp) * 2 * kRows;
+  return it;
+}
+
+// kSplit = false: grid (query-tile pairs, heads), every CTA a whole unit;
+// kSplit = true: one CTA per work item of `plan` (whole units, then key ranges).
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
-    attention_kernel(const __grid_constant__ CUtensorMap tm_qkv, int T, __nv_bfloat16 *__restrict__ out) {
+    attention_kernel(const __grid_constant__ CUtensorMap tm_qkv, int T, __nv_bfloat16 *__restrict__ out, Plan plan) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sQ = smem;                                       // [tile A, B][2 halves]
@@ -105,9 +146,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctl *ctl = reinterpret_cast<Ctl *>(sV + kStages * kTileBytes);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int head = blockIdx.y;
-  const int q0 = blockIdx.x * 2 * kRows;
-  const int nt = (T + kRows - 1) / kRows;
+  Item item;
+  if constexpr (kSplit) {
+    item = item_of(blockIdx.x, T, plan);
+  } else {
+    item = Item{(int)blockIdx.y, (int)blockIdx.x * 2 * kRows, 0, (T + kRows - 1) / kRows, -1};
+  }
+  const int j0 = item.j0, nt = item.nt;   // this CTA's key tiles [j0, j0 + nt)
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
@@ -148,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpTma) {
     if (lane == 0) {
       // ---------------- TMA producer: K_0, then per tile j: K_{j+1}, V_j
+      const int head = item.head, q0 = item.q0;
       const int xq = head * kHeadDim, xk = kHidden + head * kHeadDim, xv = 2 * kHidden + head * kHeadDim;
       mbar_arrive_expect_tx(&ctl->q_full, 2 * kTileBytes);
       for (int x = 0; x < 2; ++x) {
@@ -165,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(full, kTileBytes);
         uint8_t *dst = (is_k ? sK : sV) + s * kTileBytes;
         const int x = is_k ? xk : xv;
-        tma_load_2d(dst, &tm_qkv, full, x, j * kRows);
-        tma_load_2d(dst + kHalfBytes, &tm_qkv, full, x + 64, j * kRows);
+        tma_load_2d(dst, &tm_qkv, full, x, (j0 + j) * kRows);
+        tma_load_2d(dst + kHalfBytes, &tm_qkv, full, x + 64, (j0 + j) * kRows);
         (is_k ? k_last : v_last)[s] = (int)ph;
         return true;
       };
@@ -255,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // order); observing o_done here keeps its phases in step.
       if (j > 0 && !(ok = mbar_wait(&ctl->o_done[x], (j - 1) & 1, abort))) break;
       tc_fence_after();
-      const int valid = T - j * kRows;   // keys of this tile that exist (< 128 only in the last tile)
+      const int valid = T - (j0 + j) * kRows;   // keys of this tile that exist (< 128 only in the last tile)
       // the row's 128 scores in registers, one TMEM round trip
       uint32_t sv[128];
       tmem_ld128(t_s, sv);
@@ -307,7 +353,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&ctl->p_full[x]);
     }
-    if (ok && mbar_wait(&ctl->o_done[x], (nt - 1) & 1, abort)) {
+    // re-derived from the block index read afresh, so nothing of it is held
+    // through the loop above
+    Item it;
+    if constexpr (kSplit) {
+      uint32_t b;
+      asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(b));
+      it = item_of((int)b, T, plan);
+    } else {
+      it = Item{(int)blockIdx.y, (int)blockIdx.x * 2 * kRows, 0, nt, -1};
+    }
+    const int head = it.head, q0 = it.q0;
+    if (kSplit && ok && it.slot >= 0 && mbar_wait(&ctl->o_done[x], (nt - 1) & 1, abort)) {
+      // a key range of a split unit: unnormalised rows with their max and sum
+      tc_fence_after();
+      float4 *dst =
+          reinterpret_cast<float4 *>(plan.part + ((size_t)it.slot * 2 * kRows + x * kRows + row) * kPartRowFloats);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c * 32, o);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[c * 8 + q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                       __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+      }
+      dst[32] = make_float4(m, l, 0.f, 0.f);
+    } else if (ok && mbar_wait(&ctl->o_done[x], (nt - 1) & 1, abort)) {
       tc_fence_after();
       const float inv = 1.0f / l;
       const int t = q0 + x * kRows + row;
@@ -335,25 +407,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
+// Combines the key ranges of each split unit, in range order (deterministic):
+// with m* the largest range max, O = sum_r O_r 2^(m_r - m*) and
+// l = sum_r l_r 2^(m_r - m*), the output row is O / l in bf16.  One warp per
+// query row, four output values per lane.
+__global__ void __launch_bounds__(256)
+    attention_merge_kernel(const float *__restrict__ part, int T, Plan plan, __nv_bfloat16 *__restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int r = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int unit = plan.n_full + r / (2 * kRows), row_in_unit = r % (2 * kRows);
+  const int t = (unit % plan.n_qp) * 2 * kRows + row_in_unit;
+  if (t >= T) return;
+  const int head = unit / plan.n_qp;
+  const float *base = part + ((size_t)(unit - plan.n_full) * plan.splits * 2 * kRows + row_in_unit) * kPartRowFloats;
+  const size_t item_stride = (size_t)2 * kRows * kPartRowFloats;
+  float mx = -INFINITY;
+  for (int k = 0; k < plan.splits; ++k) mx = fmaxf(mx, __ldg(base + k * item_stride + 128));
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.f;
+  for (int k = 0; k < plan.splits; ++k) {
+    const float *p = base + k * item_stride;
+    const float w = ex2_approx(__ldg(p + 128) - mx);
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(p) + lane);
+    o.x = fmaf(v.x, w, o.x);
+    o.y = fmaf(v.y, w, o.y);
+    o.z = fmaf(v.z, w, o.z);
+    o.w = fmaf(v.w, w, o.w);
+    l = fmaf(__ldg(p + 129), w, l);
+  }
+  const float inv = 1.0f / l;
+  *reinterpret_cast<uint2 *>(out + (size_t)t * kCatCols + head * kHeadDim + lane * 4) =
+      make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
+}
+
+// Split plan: the units that fill whole waves of one CTA per SM run whole;
+// the units of the last, partial wave are split into the most key ranges (at
+// most 8, each of at least 4 key tiles) that still fit in one wave and in the
+// partial buffer.  No split without a buffer.
+Plan attention_plan(int T, int sms, float *part, size_t part_bytes) {
+  const int nt = (T + kRows - 1) / kRows;
+  Plan p{};
+  p.n_qp = (T + 2 * kRows - 1) / (2 * kRows);
+  const int units = p.n_qp * kHeads;
+  p.n_full = units;
+  p.splits = 1;
+  p.part = part;
+  if (!part || sms < 1) return p;
+  const int full = units / sms * sms, rem = units - full;
+  if (rem == 0) return p;
+  for (int S = 8; S >= 2; --S) {
+    if (rem * S > sms || nt / S < 4 || (size_t)rem * S * kPartItemBytes > part_bytes) continue;
+    p.n_full = full;
+    p.splits = S;
+    return p;
+  }
+  return p;
+}
+
 }  // namespace attn_tc
 
-cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s, bool pdl) {
+cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s, bool pdl,
+                             float *part, size_t part_bytes) {
   using namespace attn_tc;
-  static std::atomic<bool> attr_set[kMaxDevices];
+  static std::atomic<bool> attr_set[kMaxDevices], attr_set_split[kMaxDevices];
   const int slot = device_slot();
   if (slot < 0 || !attr_set[slot].load(std::memory_order_acquire)) {
     // the warpgroup register split assumes exactly kLaunchRegs per thread at launch
-    cudaFuncAttributes fa;
-    const cudaError_t e = cudaFuncGetAttributes(&fa, attention_kernel);
+    cudaFuncAttributes fa, fb;
+    cudaError_t e = cudaFuncGetAttributes(&fa, attention_kernel<false>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fb, attention_kernel<true>);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    if (fa.numRegs != kLaunchRegs || fb.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   }
-  const cudaError_t e = set_smem_once(attention_kernel, (int)kSmem, attr_set);
+  cudaError_t e = set_smem_once(attention_kernel<false>, (int)kSmem, attr_set);
+  if (e == cudaSuccess) e = set_smem_once(attention_kernel<true>, (int)kSmem, attr_set_split);
   if (e != cudaSuccess) return e;
   CUtensorMap tm;
   if (!make_tmap_bf16(&tm, qkv, (uint64_t)T, kQkvCols, kRows)) return cudaErrorInvalidValue;
-  dim3 grid((T + 2 * kRows - 1) / (2 * kRows), kHeads);
-  return launch_kernel(attention_kernel, grid, dim3(kThreads), kSmem, s, pdl, tm, T, cat);
+  const Plan plan = attention_plan(T, num_sms(), part, part_bytes);
+  const int units = plan.n_qp * kHeads;
+  if (plan.splits == 1)
+    return launch_kernel(attention_kernel<false>, dim3(plan.n_qp, kHeads), dim3(kThreads), kSmem, s, pdl, tm, T, cat,
+                         plan);
+  const int items = plan.n_full + (units - plan.n_full) * plan.splits;
+  const cudaError_t le =
+      launch_kernel(attention_kernel<true>, dim3(items), dim3(kThreads), kSmem, s, pdl, tm, T, cat, plan);
+  if (le != cudaSuccess) return le;
+  return launch_kernel(attention_merge_kernel, dim3((units - plan.n_full) * 2 * kRows / 8), dim3(256), 0, s, pdl,
+                       static_cast<const float *>(part), T, plan, cat);
 }
 
 }  // namespace flux3

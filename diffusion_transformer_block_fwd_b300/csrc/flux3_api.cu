@@ -255,6 +255,9 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
   if (fp4 && (!make_tmap_bf16(&tmWin, ws.w_in, kInRows, kHidden, kBoxB) ||
               !make_tmap_bf16(&tmWout, ws.w_out, kHidden, kCatCols, kBoxB)))
     return FLUX3_ERR_CUDA;
+  // attention's key-range partials may use only memory that is dead while it
+  // runs: h when the split region lies over h and qkv (attention reads qkv)
+  const size_t attn_part_bytes = split_in_place((size_t)T) ? ws_round((size_t)T * kHidden * 2) : kSplitBytes;
   for (int b = first; b < first + count; ++b) {
     if (h->cfg.wfmt == FLUX3_W_NVFP4) F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s, true));
     if (h->cfg.wfmt == FLUX3_W_FP8R) F3_CUDA(launch_dequantize_fp8r_block(h->fp8[b], ws.w_in, ws.w_out, s, true));
@@ -271,7 +274,7 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     for (int smp = 0; smp < n_samples; ++smp) {   // attention within each sample
       const int r0 = sample_start[smp];
       F3_CUDA(launch_attention(ws.qkv + (size_t)r0 * kQkvCols, sample_start[smp + 1] - r0,
-                               ws.cat + (size_t)r0 * kCatCols, s, true));
+                               ws.cat + (size_t)r0 * kCatCols, s, true, ws.part, attn_part_bytes));
     }
     EpiParams eo{};
     eo.x = x;
@@ -769,11 +772,12 @@ flux3_status flux3_in_projection(const flux3_handle *h, int block_idx, const voi
                            static_cast<cudaStream_t>(stream));
 }
 
-flux3_status flux3_attention(const void *qkv, int T, void *cat, void *stream) {
+flux3_status flux3_attention(const void *qkv, int T, void *cat, void *split_buf, size_t split_bytes, void *stream) {
   if (!qkv || !cat || T < 1 || T > kMaxTokensLimit) return FLUX3_ERR_INVALID_ARG;
-  if (!aligned16(qkv) || !aligned16(cat)) return FLUX3_ERR_ALIGNMENT;
+  if (!aligned16(qkv) || !aligned16(cat) || (split_buf && !aligned16(split_buf))) return FLUX3_ERR_ALIGNMENT;
   return cuda_status(launch_attention(static_cast<const __nv_bfloat16 *>(qkv), T, static_cast<__nv_bfloat16 *>(cat),
-                                      static_cast<cudaStream_t>(stream)));
+                                      static_cast<cudaStream_t>(stream), false, static_cast<float *>(split_buf),
+                                      split_buf ? split_bytes : 0));
 }
 
 flux3_status flux3_out_projection(const flux3_handle *h, int block_idx, const void *cat, int T,

@@ -119,6 +119,9 @@ cudaError_t launch_prepare(const flux3_segment *segs, int n_segs, int T, uint8_t
 cudaError_t launch_ln_modulate(const float *x, int T, const uint8_t *sid, const float *mod, float eps,
                                __nv_bfloat16 *h, cudaStream_t s, bool pdl = false);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
-cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s, bool pdl = false);
+// part / part_bytes: scratch for the key-range split of the last, partial
+// wave of units (null: no split).
+cudaError_t launch_attention(const __nv_bfloat16 *qkv, int T, __nv_bfloat16 *cat, cudaStream_t s, bool pdl = false,
+                             float *part = nullptr, size_t part_bytes = 0);
 
 }  // namespace flux3

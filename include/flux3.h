@@ -556,8 +556,16 @@ FLUX3_API flux3_status flux3_in_projection(const flux3_handle *h, int block_idx,
  * 1/sqrt(128), no mask:
  *   cat[t, 128 h : 128 h + 128] = softmax(q^_h k^_h^T / sqrt(128)) v_h
  *   qkv device bf16 [T, 9216] laid out as above; cat device bf16 [T, 12288]
- *   (only columns 0..3071 are written). */
-FLUX3_API flux3_status flux3_attention(const void *qkv, int T, void *cat, void *stream);
+ *   (only columns 0..3071 are written).
+ * split_buf: optional device scratch (16-byte aligned, split_bytes long, at
+ * most FLUX3_SPLIT_BYTES used; NULL for none).  With it, the (query-tile
+ * pair, head) units of the last, partial wave of one CTA per SM are split
+ * into key ranges that fill the wave; each range stores its unnormalised
+ * rows with their running max and sum there, and a merge combines the ranges
+ * in a fixed order.  The block forward calls do the same with their
+ * workspace.  Without it no unit is split. */
+FLUX3_API flux3_status flux3_attention(const void *qkv, int T, void *cat, void *split_buf, size_t split_bytes,
+                                       void *stream);
 
 /* Bytes of scratch the out-projection's K split can use (96 partial tiles of
  * 256 x 256 float32); the block workspace already holds it. */

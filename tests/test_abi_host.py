@@ -119,7 +119,8 @@ def test_forward_argument_validation_before_any_launch():
     assert L.flux3_gemm_bf16(16, 16, 16, 128, 200, 64, None) == F3.FLUX3_ERR_INVALID_ARG     # N % 256
     assert L.flux3_gemm_bf16(16, 16, 16, 128, 256, 96, None) == F3.FLUX3_ERR_INVALID_ARG     # K % 64
     assert L.flux3_gemm_bf16(18, 16, 16, 128, 256, 64, None) == F3.FLUX3_ERR_ALIGNMENT
-    assert L.flux3_attention(16, 0, 16, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_attention(16, 0, 16, None, 0, None) == F3.FLUX3_ERR_INVALID_ARG
+    assert L.flux3_attention(16, 8, 16, 24, 1 << 20, None) == F3.FLUX3_ERR_ALIGNMENT
     assert L.flux3_ln_modulate(16, 4, 16, 16, ctypes.c_float(0.0), 16, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_rope_tables(16, 4, ctypes.c_float(-1.0), 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG
     assert L.flux3_prepare(arr, n, 8, 16, ctypes.c_float(-1.0), 16, 16, 16, None) == F3.FLUX3_ERR_INVALID_ARG

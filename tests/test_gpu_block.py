@@ -48,10 +48,18 @@ def test_block_full_oracle(blk, name, spec):
 MAX_TOKENS_SPEC = [("txt", 1024), ("image", (64, 64))] + [("image_cond", (32, 32))] * 11
 
 
-@pytest.mark.parametrize("workload", ["block_1024sq_t4608", "block_1024sq_ref1_t8704", "max_tokens_t16384"])
+# 1792 and 2048 tokens (512 text + a 40x32 or 48x32 image): on 148 SMs attention splits the units of its last
+# wave into key ranges (3 and 2 ranges) whose partials must fit in h (6 KB per token: attention still reads qkv
+# behind it), and the out-projection splits its trailing 10 tiles in 6 ranges (1792) and 22 in 3 (2048)
+MID_SPECS = {"mid_t1792": [("txt", 512), ("image", (40, 32))], "mid_t2048": [("txt", 512), ("image", (48, 32))]}
+
+
+@pytest.mark.parametrize("workload", ["mid_t1792", "mid_t2048", "block_1024sq_t4608", "block_1024sq_ref1_t8704",
+                                      "max_tokens_t16384"])
 def test_block_full_size_sampled_rows(blk, workload):
     w, wf, blocks = blk
-    spec = MAX_TOKENS_SPEC if workload == "max_tokens_t16384" else synth.WORKLOADS[workload]["spec"]
+    spec = (MAX_TOKENS_SPEC if workload == "max_tokens_t16384" else MID_SPECS[workload] if workload in MID_SPECS
+            else synth.WORKLOADS[workload]["spec"])
     lay = synth.build_layout(spec)
     x = synth.activations(6, lay.T, device=DEV)
     mods = synth.modulation(6, device=DEV)
