@@ -111,10 +111,10 @@ def kernel_bytes(T):
 # before its host-launcher marker line, the whole file if it has none); null
 # otherwise.
 TRAFFIC = {
-    # gemm_kernel<EPI_IN_PROJ>, T = 4608: dram__bytes_read.sum 204.91 MB + dram__bytes_write.sum 154.32 MB
-    # (captured on the gemm.cuh whose whole-file sha256 began 8cee6e7fb6257e47; its device code hashes as below)
-    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "3ca0dc4bc3803578", "T": 4608,
-                      "bytes_per_launch": 359_235_584},
+    # gemm_kernel<EPI_IN_PROJ>, T = 4608: dram__bytes_read.sum 209.58 MB + dram__bytes_write.sum 154.05 MB
+    # (ncu --set full --clock-control none, one launch; profiles/gemm_tcgen05_block_1024sq_t4608.md)
+    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "5617501d99cfcb90", "T": 4608,
+                      "bytes_per_launch": 363_625_216},
 }
 
 HOST_MARKER = b"// ---------------------------------------------------------------- host launchers\n"
