@@ -64,17 +64,20 @@ def kernel_flops(T):
 
 def out_proj_splits(T, sms):
     """K ranges of the out-projection's trailing tiles at T tokens on `sms`
-    SMs (1: no split), the plan the library takes: the last, partial round of
-    256 x 256 tiles on the CTA pairs is split by the largest of 8, 6, 4, 3, 2
-    that divides the 192 k-blocks into ranges of >= 16 and keeps the units
-    within the pairs and 96 partial tiles.  A split adds one merge launch."""
-    pairs = sms // 2
-    tiles = -(-T // 256) * 12
-    rem = tiles % pairs if tiles >= pairs else tiles
-    if rem == 0:
+    SMs (1: no split), the plan the library takes: tiles are 128 x 256 on
+    single CTAs for T <= 128, else 256 x 256 on CTA pairs; the last, partial
+    round of tiles is split by the largest of 12, 8, 6, 4, 3, 2 that divides
+    the 192 k-blocks into ranges of >= 16 and keeps the units within the
+    workers and their partial tiles within the 24 MiB split buffer.  A split
+    adds one merge launch."""
+    tile_m, workers = (128, sms) if T <= 128 else (256, sms // 2)
+    tiles = -(-T // tile_m) * 12
+    rem = tiles % workers
+    if rem == 0 or workers < 2:
         return 1
-    for S in (8, 6, 4, 3, 2):
-        if 192 % S == 0 and 192 // S >= 16 and rem * S <= pairs and rem * S <= 96:
+    for S in (12, 8, 6, 4, 3, 2):
+        if 192 % S == 0 and 192 // S >= 16 and rem * S <= workers and \
+                rem * S * tile_m * 256 * 4 <= 96 * 256 * 256 * 4:
             return S
     return 1
 

@@ -47,12 +47,13 @@ struct EpiParams {
   const uint8_t *sid;   // [M]
   const float *mod;     // [3, 9216]
   // EPI_OUT_RESIDUAL with a K split of the trailing tiles: float32 partial
-  // tiles (256 x 256 per split unit); null / too small: no split
+  // tiles (tile rows x 256 per split unit); null / too small: no split
   float *part;
   size_t part_bytes;
 };
 
-// Most split units one GEMM launch uses (their partial tiles: 256 KB each).
+// Size of the split partial buffer: 96 partial tiles of the CTA-pair form
+// (256 x 256 float32, 256 KB each), or 192 of the one-CTA form.
 constexpr int kMaxSplitUnits = 96;
 constexpr size_t kSplitUnitBytes = 256 * 256 * 4;
 constexpr size_t kSplitBytes = kMaxSplitUnits * kSplitUnitBytes;

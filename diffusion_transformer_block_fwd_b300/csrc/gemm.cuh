@@ -15,6 +15,10 @@
 // the 256 B rows in shared memory, and its own 128 accumulator rows in tensor
 // memory.  Per SM that halves the B operand bytes the tensor core reads from
 // shared memory and the bytes TMA writes, against a one-CTA 128 x 256 tile.
+// For M <= 128 the one-CTA form runs instead (gemm1_kernel: 128 x 256 tiles,
+// cta_group::1, all 256 B rows of a k-block in the CTA's shared memory, a
+// 4-stage ring): a pair tile would be more than half padding there, and the
+// 148 CTAs take twice as many tiles per round as 74 pairs.
 //
 // Roles (320 threads per CTA): warp 0 issues the CTA's TMA loads (128 x 64
 // of A, 128 x 64 of B, 128-byte swizzle) into a 6-stage ring, completing on
@@ -24,7 +28,7 @@
 // accumulator through tcgen05.ld (one output row and one 128-column half per
 // thread) and run the epilogue, so the epilogue of tile i overlaps the MMAs
 // of tile i+1.
-// Units: the pairs take units round robin.  Whole tiles fill complete
+// Units: the pairs (or CTAs) take units round robin.  Whole tiles fill complete
 // rounds; when the last round would leave pairs idle, its tiles are split
 // along K into ranges (out-projection only): each range stores its float32
 // partial tile, and split_merge_residual_kernel sums a tile's ranges in a fixed
@@ -41,32 +45,40 @@ namespace flux3 {
 
 namespace gemm_detail {
 
-constexpr int kStages = 6;
 constexpr int kThreads = 320;
-constexpr int kRowsPerCta = 128;               // A rows and B rows each CTA of a pair holds
-constexpr int kTileM = 2 * kRowsPerCta;        // 256 output rows per pair tile
-constexpr uint32_t kABytes = kRowsPerCta * kBK * 2;   // 16 KB
-constexpr uint32_t kBBytes = kRowsPerCta * kBK * 2;   // 16 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kPairStageBytes = 2 * kStageBytes; // both CTAs' loads of one stage
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kBoxBytes = 32 * 128;              // one epilogue output box: 32 rows x 64 bf16
 constexpr uint32_t kTmemCols = 512;                   // two 128-lane x 256-column fp32 accumulators
 
+template <int kStages>
 struct SharedCtl {
-  uint64_t full[kStages];      // leader: both CTAs' TMA bytes of the stage landed
+  uint64_t full[kStages];      // issuing CTA: the stage's TMA bytes (both CTAs' for a pair) landed
   uint64_t empty[kStages];     // every CTA: the stage's MMAs are done
   uint64_t tmem_full[2];       // every CTA: the accumulator holds a finished tile
-  uint64_t tmem_empty[2];      // leader: all 512 epilogue threads of the pair drained it
+  uint64_t tmem_empty[2];      // issuing CTA: every epilogue thread (of the pair) drained it
   uint64_t drain;
   uint64_t xbar[8];            // per epilogue warp: its residual box landed (out-projection)
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr int kEpiWarps = 8;
-constexpr uint32_t kBoxBytes = 32 * 128;              // one epilogue output box: 32 rows x 64 bf16
-constexpr size_t kSmemBytes =
-    1024 /*alignment slack*/ + kStages * kStageBytes + kEpiWarps * kBoxBytes + sizeof(SharedCtl);
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+// The two forms of the kernel.  Pair (kPair): a cluster of two CTAs on one
+// TPC computes a 256 x 256 tile with cta_group::2 MMAs; each CTA stages 128 A
+// rows and 128 B rows per k-block.  Single: one CTA computes a 128 x 256 tile
+// with cta_group::1 MMAs and stages 128 A rows and all 256 B rows.  The
+// single form serves M <= 128, where a pair tile would be at most half rows.
+template <bool kPair>
+struct GemmCfg {
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kTileM = kPair ? 256 : 128;                     // output rows per tile
+  static constexpr uint32_t kABytes = 128 * kBK * 2;                   // 16 KB: 128 A rows per CTA
+  static constexpr uint32_t kBBytes = (kPair ? 128 : 256) * kBK * 2;   // B rows per CTA
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTxBytes = (kPair ? 2 : 1) * kStageBytes;  // completing on one stage barrier
+  static constexpr size_t kSmemBytes =
+      1024 /*alignment slack*/ + kStages * kStageBytes + kEpiWarps * kBoxBytes + sizeof(SharedCtl<kStages>);
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
@@ -318,10 +330,10 @@ __device__ __forceinline__ Unit unit_of(int u, int n_full, int splits, int num_m
   return r;
 }
 
-// A split unit's fp32 accumulator rows go to its partial buffer (256 x 256
+// A split unit's fp32 accumulator rows go to its partial buffer (tile_m x 256
 // float32 per unit, row = row in the tile) as four 32 x 32 boxes per half.
 __device__ __forceinline__ void store_partial_half(uint32_t taddr, int slot, int row_box0, int rows_valid, int half,
-                                                   const BoxWriter &bw, const CUtensorMap *tmP) {
+                                                   int tile_m, const BoxWriter &bw, const CUtensorMap *tmP) {
   if (row_box0 >= rows_valid) return;   // the merge reads no row past M
   uint32_t r[32];
 #pragma unroll 1
@@ -332,33 +344,37 @@ __device__ __forceinline__ void store_partial_half(uint32_t taddr, int slot, int
     for (int q = 0; q < 8; ++q)
       *reinterpret_cast<float4 *>(bw.buf + bw.lane * 128 + ((q ^ (bw.lane & 7)) * 16)) =
           make_float4(f32(r[4 * q]), f32(r[4 * q + 1]), f32(r[4 * q + 2]), f32(r[4 * q + 3]));
-    bw.store(tmP, half * 128 + c * 32, slot * kTileM + row_box0);
+    bw.store(tmP, half * 128 + c * 32, slot * tile_m + row_box0);
   }
 }
 
-template <int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
-                int K, int n_full, int splits, EpiParams ep) {
+template <int EPI, bool kPair>
+__device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmO0,
+                                          const CUtensorMap &tmO1, int M, int N, int K, int n_full, int splits,
+                                          const EpiParams &ep) {
+  using C = GemmCfg<kPair>;
+  constexpr int kStages = C::kStages;
+  constexpr int kTileM = C::kTileM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *smA = smem;
-  uint8_t *smB = smem + kStages * kABytes;
-  uint8_t *sOut = smem + kStages * kStageBytes;     // [epilogue warp] 4 KB output box
-  SharedCtl *ctl = reinterpret_cast<SharedCtl *>(sOut + kEpiWarps * kBoxBytes);
+  uint8_t *smB = smem + kStages * C::kABytes;
+  uint8_t *sOut = smem + kStages * C::kStageBytes;     // [epilogue warp] 4 KB output box
+  auto *ctl = reinterpret_cast<SharedCtl<kStages> *>(sOut + kEpiWarps * kBoxBytes);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const uint32_t rank = cluster_ctarank();          // 0 = leader, 1 = peer
+  const uint32_t rank = kPair ? cluster_ctarank() : 0;   // 0 = the CTA that issues the MMAs
   const bool leader = rank == 0;
-  const int pair = blockIdx.x / 2, num_pairs = gridDim.x / 2;
+  // a worker is a CTA pair or a single CTA
+  const int worker = kPair ? blockIdx.x / 2 : blockIdx.x;
+  const int num_workers = kPair ? gridDim.x / 2 : gridDim.x;
   const int num_m = (M + kTileM - 1) / kTileM;
   const int num_n = N / kBN;
   const int num_tiles = num_m * num_n;
   const int num_units = n_full + (num_tiles - n_full) * splits;
   const int num_kb = K / kBK;
-  // Tile order: consecutive pairs share the operand with more rows, so that
+  // Tile order: consecutive workers share the operand with more rows, so that
   // it is read from DRAM about once and the smaller one is re-read from L2.
   const bool n_fast = M > N;
 
@@ -369,7 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tmem_full[a], 1);
-      mbar_init(&ctl->tmem_empty[a], 2 * 256);
+      mbar_init(&ctl->tmem_empty[a], (kPair ? 2 : 1) * 256);
     }
     mbar_init(&ctl->drain, 1);
     for (int w = 0; w < kEpiWarps; ++w) mbar_init(&ctl->xbar[w], 1);
@@ -381,40 +397,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
-    tmem_relinquish_pair();
+    if constexpr (kPair) {
+      tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&ctl->tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  cluster_sync();          // both CTAs' barriers are initialised before any cross-CTA signal
+  if constexpr (kPair)
+    cluster_sync();        // both CTAs' barriers are initialised before any cross-CTA signal
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
+  // One-CTA form (small M, bound by streaming the weights B from DRAM): the
+  // B halves of the first ring stages are loaded before griddep_wait.  B is
+  // never written by the kernels this one may overlap (each kernel of the
+  // chain waits for its predecessor before releasing its own dependents, so
+  // everything before the previous kernel has completed), so the DRAM latency
+  // of the first tiles passes while the previous kernel finishes.  The A
+  // halves, which the previous kernel may write, follow after the wait.
+  int n_pre = 0;
+  if constexpr (!kPair) {
+    if (warp == 0 && lane == 0 && worker < num_units) {
+      const Unit un = unit_of(worker, n_full, splits, num_m, num_n, n_fast, num_kb);
+      n_pre = un.kb1 - un.kb0 < kStages ? un.kb1 - un.kb0 : kStages;
+      for (int i = 0; i < n_pre; ++i) {
+        uint8_t *b_dst = smB + i * C::kBBytes;
+        mbar_arrive_expect_tx(&ctl->full[i], C::kTxBytes);
+        tma_load_2d(b_dst, &tmB, &ctl->full[i], (un.kb0 + i) * kBK, un.n_blk * kBN);
+        tma_load_2d(b_dst + 128 * kBK * 2, &tmB, &ctl->full[i], (un.kb0 + i) * kBK, un.n_blk * kBN + 128);
+      }
+    }
+  }
   // set-up above overlaps the previous kernel when launched as its programmatic dependent
   griddep_wait();
   griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer (both CTAs): this CTA's 128 A rows and
-      // 128 B rows of each stage, completing on the leader's full barrier
+      // ---------------- TMA producer: this CTA's 128 A rows and its B rows
+      // (pair: 128, completing on the leader's full barrier; single: 256)
       int last_phase[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int u = pair; u < num_units && ok; u += num_pairs) {
+      int it = 0;   // k-blocks issued so far; the first n_pre have their B half in flight
+      for (int u = worker; u < num_units && ok; u += num_workers) {
         const Unit un = unit_of(u, n_full, splits, num_m, num_n, n_fast, num_kb);
-        const int a_row = un.m_blk * kTileM + (int)rank * kRowsPerCta;
-        const int b_row = un.n_blk * kBN + (int)rank * kRowsPerCta;
-        for (int kb = un.kb0; kb < un.kb1; ++kb) {
-          if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) {
+        const int a_row = un.m_blk * kTileM + (int)rank * 128;
+        const int b_row = un.n_blk * kBN + (int)rank * 128;
+        for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
+          const bool pre = it < n_pre;   // a fresh stage: no wait for it to drain
+          if (!pre && !mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) {
             ok = false;
             break;
           }
-          const uint32_t full_leader = map_to_cta(smem_addr(&ctl->full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&ctl->full[stage], kPairStageBytes);
-          tma_load_2d_pair(smA + stage * kABytes, &tmA, full_leader, kb * kBK, a_row);
-          tma_load_2d_pair(smB + stage * kBBytes, &tmB, full_leader, kb * kBK, b_row);
+          uint8_t *a_dst = smA + stage * C::kABytes;
+          uint8_t *b_dst = smB + stage * C::kBBytes;
+          if constexpr (kPair) {
+            const uint32_t full_leader = map_to_cta(smem_addr(&ctl->full[stage]), 0);
+            if (leader) mbar_arrive_expect_tx(&ctl->full[stage], C::kTxBytes);
+            tma_load_2d_pair(a_dst, &tmA, full_leader, kb * kBK, a_row);
+            tma_load_2d_pair(b_dst, &tmB, full_leader, kb * kBK, b_row);
+          } else {
+            if (!pre) {
+              mbar_arrive_expect_tx(&ctl->full[stage], C::kTxBytes);
+              tma_load_2d(b_dst, &tmB, &ctl->full[stage], kb * kBK, b_row);
+              tma_load_2d(b_dst + 128 * kBK * 2, &tmB, &ctl->full[stage], kb * kBK, b_row + 128);
+            }
+            tma_load_2d(a_dst, &tmA, &ctl->full[stage], kb * kBK, a_row);
+          }
           last_phase[stage] = (int)phase;
           if (++stage == kStages) {
             stage = 0;
@@ -422,22 +479,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok && leader) {  // both CTAs' copies complete on the leader's barriers
+      if (!ok && leader) {  // every copy of a stage completes on the issuing CTA's barrier
         for (int s = 0; s < kStages; ++s)
           if (last_phase[s] >= 0) drain_wait(&ctl->full[s], (uint32_t)last_phase[s]);
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
-      // ---------------- MMA issuer (leader only): 256 x 256 x 16 per instruction
+      // ---------------- MMA issuer: kTileM x 256 x 16 per instruction
       constexpr uint32_t idesc = idesc_bf16(kTileM, kBN, false);
-      // descriptors encoded once and moved by constant offsets per MMA
+      // descriptors encoded once and moved by constant offsets per MMA; a
+      // 256-row B stage is one operand (row groups of 8 at 1024-byte strides)
       const SmemDesc da = smem_desc_split(smem_addr(smA), 16, 1024, kSwizzle128B);
       const SmemDesc db = smem_desc_split(smem_addr(smB), 16, 1024, kSwizzle128B);
       uint32_t stage = 0, phase = 0;
       int local = 0;
       bool ok = true;
-      for (int u = pair; u < num_units && ok; u += num_pairs, ++local) {
+      for (int u = worker; u < num_units && ok; u += num_workers, ++local) {
         const Unit un = unit_of(u, n_full, splits, num_m, num_n, n_fast, num_kb);
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
@@ -451,27 +509,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_ss_pair_at(d_tmem, da, stage * kABytes + k * 32, db, stage * kBBytes + k * 32, idesc,
-                                (kb != un.kb0 || k != 0) ? 1u : 0u);
-          mma_commit_pair_mc(&ctl->empty[stage], 0x3);
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint32_t accumulate = (kb != un.kb0 || k != 0) ? 1u : 0u;
+            if constexpr (kPair)
+              mma_bf16_ss_pair_at(d_tmem, da, stage * C::kABytes + k * 32, db, stage * C::kBBytes + k * 32, idesc,
+                                  accumulate);
+            else
+              mma_bf16_ss_at(d_tmem, da, stage * C::kABytes + k * 32, db, stage * C::kBBytes + k * 32, idesc,
+                             accumulate);
+          }
+          if constexpr (kPair)
+            mma_commit_pair_mc(&ctl->empty[stage], 0x3);
+          else
+            mma_commit(&ctl->empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
-        if (ok) mma_commit_pair_mc(&ctl->tmem_full[acc], 0x3);
+        if (ok) {
+          if constexpr (kPair)
+            mma_commit_pair_mc(&ctl->tmem_full[acc], 0x3);
+          else
+            mma_commit(&ctl->tmem_full[acc]);
+        }
       }
       // all MMAs issued by this thread are complete once `drain` arrives
-      mma_commit_pair(&ctl->drain);
+      if constexpr (kPair)
+        mma_commit_pair(&ctl->drain);
+      else
+        mma_commit(&ctl->drain);
       drain_wait(&ctl->drain, 0);
     }
   } else {
-    // ---------------- epilogue warps 2..9 (both CTAs): this CTA's 128 rows;
-    // warp w reads TMEM lane quarter w % 4, and takes column half (w - 2) / 4
+    // ---------------- epilogue warps 2..9: this CTA's 128 rows; warp w reads
+    // TMEM lane quarter w % 4, and takes column half (w - 2) / 4
     const int quarter = warp & 3;
     const int half = (warp - 2) / 4;
-    const int row_in_tile = (int)rank * kRowsPerCta + quarter * 32 + lane;
+    const int row_in_tile = (int)rank * 128 + quarter * 32 + lane;
     const BoxWriter bw{sOut + (warp - 2) * kBoxBytes, (uint32_t)lane};
     if (lane == 0) {
       tma_prefetch_desc(&tmO0);
@@ -483,7 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t empty_leader0 = map_to_cta(smem_addr(&ctl->tmem_empty[0]), 0);
     const uint32_t empty_leader1 = map_to_cta(smem_addr(&ctl->tmem_empty[1]), 0);
     int local = 0;
-    for (int u = pair; u < num_units; u += num_pairs, ++local) {
+    for (int u = worker; u < num_units; u += num_workers, ++local) {
       const Unit un = unit_of(u, n_full, splits, num_m, num_n, n_fast, num_kb);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
@@ -502,14 +577,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kBN;
       if (un.slot >= 0) {
-        store_partial_half(taddr, un.slot, row_in_tile - lane, M - un.m_blk * kTileM, half, bw, &tmO1);
+        store_partial_half(taddr, un.slot, row_in_tile - lane, M - un.m_blk * kTileM, half, kTileM, bw, &tmO1);
       } else if (!epilogue_half<EPI>(taddr, un.m_blk * kTileM + row_in_tile, un.m_blk * kTileM + row_in_tile - lane,
                                      M, un.n_blk, half, ep, bw, &tmO0, &tmO1, xbar, xphase, abort)) {
         x_in_flight = true;   // only the residual box wait can fail
         break;
       }
       tc_fence_before();
-      mbar_arrive_cluster_relaxed(acc ? empty_leader1 : empty_leader0);
+      if constexpr (kPair)
+        mbar_arrive_cluster_relaxed(acc ? empty_leader1 : empty_leader0);
+      else
+        mbar_arrive(&ctl->tmem_empty[acc]);
     }
     if (lane == 0) bulk_wait_all();   // this warp's output stores are complete before the CTA exits
     if (x_in_flight && lane == 0) drain_wait(xbar, xphase);   // the box must land before the CTA exits
@@ -517,17 +595,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();          // neither CTA leaves while its pair may still touch its memory
+  if constexpr (kPair) cluster_sync();   // neither CTA leaves while its pair may still touch its memory
   tc_fence_after();
-  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
+                int K, int n_full, int splits, EpiParams ep) {
+  gemm_body<EPI, true>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm1_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
+                 int K, int n_full, int splits, EpiParams ep) {
+  gemm_body<EPI, false>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
 }
 
 // Sums the split units of each trailing tile in a fixed order (unit 0 first)
 // and applies the out-projection's epilogue: x[row, col] += gate[stream(row)]
 // [col] * sum.  One thread per 4 columns of a row; tile i of the trailing
 // tiles is tile n_full + i of the schedule.
-__global__ void split_merge_residual_kernel(const float *__restrict__ part, int n_full, int splits, int num_m,
-                                            int num_n, int n_fast, int M, float *__restrict__ x,
+__global__ void split_merge_residual_kernel(const float *__restrict__ part, int tile_m, int n_full, int splits,
+                                            int num_m, int num_n, int n_fast, int M, float *__restrict__ x,
                                             const uint8_t *__restrict__ sid, const float *__restrict__ mod) {
   griddep_wait();
   griddep_launch_dependents();
@@ -536,11 +635,11 @@ __global__ void split_merge_residual_kernel(const float *__restrict__ part, int 
   const int c = (threadIdx.x % 64) * 4;                     // column in the tile
   int m_blk, n_blk;
   tile_coords(n_full + i, num_m, num_n, n_fast != 0, m_blk, n_blk);
-  const int row = m_blk * kTileM + r;
-  if (row >= M) return;
+  const int row = m_blk * tile_m + r;
+  if (r >= tile_m || row >= M) return;
   float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int ks = 0; ks < splits; ++ks) {
-    const float4 p = __ldcs(reinterpret_cast<const float4 *>(part + ((size_t)(i * splits + ks) * kTileM + r) * kBN + c));
+    const float4 p = __ldcs(reinterpret_cast<const float4 *>(part + ((size_t)(i * splits + ks) * tile_m + r) * kBN + c));
     y.x += p.x;
     y.y += p.y;
     y.z += p.z;
@@ -558,42 +657,46 @@ __global__ void split_merge_residual_kernel(const float *__restrict__ part, int 
 }
 
 // ---------------------------------------------------------------- host launchers
-// Split plan of a launch: whole tiles fill complete rounds of the pairs; the
-// tiles of the last, partial round are split along K into `splits` ranges
-// (a divisor of the k-block count leaving at least 16 k-blocks per range) so
+// Split plan of a launch over `workers` (CTA pairs or single CTAs) with
+// tile_m-row tiles: whole tiles fill complete rounds of the workers; the
+// tiles of the last, partial round are split along K into `splits` ranges (a
+// divisor of the k-block count leaving at least 16 k-blocks per range) so
 // that their units fill that round.  Only the out-projection splits (its
 // epilogue is linear in the product, so partial sums merge exactly as a sum);
-// no split when there is no partial buffer, the round is full, or no divisor
-// fits.
-void split_plan(int EPI, int M, int N, int K, int pairs, size_t part_bytes, int &n_full, int &splits) {
-  const int tiles = ((M + kTileM - 1) / kTileM) * (N / kBN);
+// no split when the partial buffer is absent or too small, the round is
+// full, or no divisor fits.
+void split_plan(int EPI, int M, int N, int K, int tile_m, int workers, size_t part_bytes, int &n_full,
+                int &splits) {
+  const int tiles = ((M + tile_m - 1) / tile_m) * (N / kBN);
   const int num_kb = K / kBK;
   n_full = tiles;
   splits = 1;
-  if (EPI != EPI_OUT_RESIDUAL || pairs < 2) return;
-  const int full = tiles / pairs * pairs, rem = tiles - full;
+  if (EPI != EPI_OUT_RESIDUAL || workers < 2) return;
+  const int full = tiles / workers * workers, rem = tiles - full;
   if (rem == 0) return;
-  const int cand[5] = {8, 6, 4, 3, 2};
+  const int cand[6] = {12, 8, 6, 4, 3, 2};
   for (int S : cand) {
     const int units = rem * S;
-    if (num_kb % S != 0 || num_kb / S < 16 || units > pairs || units > kMaxSplitUnits) continue;
-    if ((size_t)units * kSplitUnitBytes > part_bytes) continue;
+    if (num_kb % S != 0 || num_kb / S < 16 || units > workers) continue;
+    if ((size_t)units * tile_m * kBN * sizeof(float) > part_bytes) continue;
     n_full = full;
     splits = S;
     return;
   }
 }
 
-template <int EPI>
-cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K, const EpiParams &ep,
+template <int EPI, bool kPair>
+cudaError_t launch_form(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K, const EpiParams &ep,
                         cudaStream_t s, bool pdl) {
+  using C = GemmCfg<kPair>;
+  auto kernel = kPair ? gemm_kernel<EPI> : gemm1_kernel<EPI>;
   static std::atomic<bool> attr_set[kMaxDevices];
-  const cudaError_t e = set_smem_once(gemm_kernel<EPI>, (int)kSmemBytes, attr_set);
+  const cudaError_t e = set_smem_once(kernel, (int)C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
-  const int tiles = ((M + kTileM - 1) / kTileM) * (N / kBN);
-  const int pairs = num_sms() / 2;
+  const int tiles = ((M + C::kTileM - 1) / C::kTileM) * (N / kBN);
+  const int workers = kPair ? num_sms() / 2 : num_sms();
   int n_full, splits;
-  split_plan(EPI, M, N, K, pairs, ep.part ? ep.part_bytes : 0, n_full, splits);
+  split_plan(EPI, M, N, K, C::kTileM, workers, ep.part ? ep.part_bytes : 0, n_full, splits);
   const int split_units = (tiles - n_full) * splits;
   // output boxes of 32 rows x 64 columns for the bf16 epilogues
   CUtensorMap tmO0 = tmA, tmO1 = tmA;
@@ -603,19 +706,28 @@ cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, i
     return cudaErrorInvalidValue;
   if (EPI == EPI_OUT_RESIDUAL && !make_tmap_f32_box32(&tmO0, ep.x, (uint64_t)M, kHidden)) return cudaErrorInvalidValue;
   if (EPI == EPI_OUT_RESIDUAL && splits > 1 &&
-      !make_tmap_f32_box32(&tmO1, ep.part, (uint64_t)split_units * kTileM, kBN))
+      !make_tmap_f32_box32(&tmO1, ep.part, (uint64_t)split_units * C::kTileM, kBN))
     return cudaErrorInvalidValue;
   if (EPI == EPI_STORE_F32 && !make_tmap_f32_box32(&tmO0, ep.x, (uint64_t)M, (uint64_t)ep.ldc))
     return cudaErrorInvalidValue;
   const int units = n_full + split_units;
-  const int grid = 2 * (units < pairs ? units : pairs);
-  cudaError_t le = launch_kernel(gemm_kernel<EPI>, dim3(grid), dim3(kThreads), kSmemBytes, s, pdl, tmA, tmB, tmO0,
-                                 tmO1, M, N, K, n_full, splits, ep);
+  const int grid = (kPair ? 2 : 1) * (units < workers ? units : workers);
+  cudaError_t le = launch_kernel(kernel, dim3(grid), dim3(kThreads), C::kSmemBytes, s, pdl, tmA, tmB, tmO0, tmO1, M,
+                                 N, K, n_full, splits, ep);
   if (le != cudaSuccess || splits == 1) return le;
-  const int num_m = (M + kTileM - 1) / kTileM, num_n = N / kBN;
-  return launch_kernel(split_merge_residual_kernel, dim3(kTileM / 4, tiles - n_full), dim3(256), 0, s, pdl,
-                       static_cast<const float *>(ep.part), n_full, splits, num_m, num_n, M > N ? 1 : 0, M, ep.x,
-                       ep.sid, ep.mod);
+  const int num_m = (M + C::kTileM - 1) / C::kTileM, num_n = N / kBN;
+  return launch_kernel(split_merge_residual_kernel, dim3(C::kTileM / 4, tiles - n_full), dim3(256), 0, s, pdl,
+                       static_cast<const float *>(ep.part), (int)C::kTileM, n_full, splits, num_m, num_n,
+                       M > N ? 1 : 0, M, ep.x, ep.sid, ep.mod);
+}
+
+// M <= 128: single CTAs with 128-row tiles (a 256-row pair tile would be
+// mostly padding, and twice the workers take the tiles); else CTA pairs.
+template <int EPI>
+cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K, const EpiParams &ep,
+                        cudaStream_t s, bool pdl) {
+  if (M <= GemmCfg<false>::kTileM) return launch_form<EPI, false>(tmA, tmB, M, N, K, ep, s, pdl);
+  return launch_form<EPI, true>(tmA, tmB, M, N, K, ep, s, pdl);
 }
 
 }  // namespace gemm_detail

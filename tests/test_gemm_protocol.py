@@ -11,8 +11,12 @@ transaction bytes, phase parity) and an in-order tensor pipe.  The model
 checks that every interleaving finishes, that each MMA reads the stage
 holding its (tile, k-block), that an accumulator is not restarted before the
 epilogue has drained its previous tile, and that the epilogue reads complete
-sums.  Planted mistakes (a stage released before its MMAs, a wrong
-accumulator phase) must be caught.
+sums.  Each stage is filled by two copies (the B and the A operand).  The
+one-CTA form runs a 4-stage ring and issues the B copies of its first stages
+before it may read A (before the programmatic-dependent wait); the loop then
+adds only their A copies.  Planted mistakes (a stage released before its MMAs,
+a wrong accumulator phase, more early stages than the ring holds) must be
+caught.
 """
 
 import random
@@ -21,20 +25,18 @@ import pytest
 
 from test_attention_protocol import Barrier
 
-STAGES = 6
-
 
 class Gemm:
-    def __init__(self, tiles, num_kb, seed, plant=None):
-        self.tiles, self.num_kb, self.plant = tiles, num_kb, plant
+    def __init__(self, tiles, num_kb, seed, plant=None, stages=6, pre=False):
+        self.tiles, self.num_kb, self.plant, self.stages, self.pre = tiles, num_kb, plant, stages, pre
         self.rng = random.Random(seed)
-        self.full = [Barrier(f"full{s}", 1) for s in range(STAGES)]
-        self.empty = [Barrier(f"empty{s}", 1) for s in range(STAGES)]
+        self.full = [Barrier(f"full{s}", 1) for s in range(stages)]
+        self.empty = [Barrier(f"empty{s}", 1) for s in range(stages)]
         self.tmem_full = [Barrier(f"tmem_full{a}", 1) for a in range(2)]
         self.tmem_empty = [Barrier(f"tmem_empty{a}", 1) for a in range(2)]   # the epilogue's arrivals, as one
         self.drain = Barrier("drain", 1)
         self.pipe, self.copies = [], []
-        self.stage_holds = [None] * STAGES
+        self.stage_holds = [{} for _ in range(stages)]   # operand -> (tile, k-block)
         self.acc = [None, None]            # (tile, k-blocks accumulated)
         self.drained = [set(), set()]      # tiles whose accumulator the epilogue has read out
         self.finished = set()
@@ -45,15 +47,27 @@ class Gemm:
             yield (bar, parity)
 
     def producer(self):
-        stage = phase = 0
+        n_pre = min(self.stages, self.num_kb) if self.pre else 0
+        if self.plant == "pre_overrun":
+            n_pre = min(self.stages + 1, self.num_kb)
+        for i in range(n_pre):                 # B halves of the first stages, before A may be read
+            s = i % self.stages
+            self.full[s].expect_tx(2)
+            self.full[s].arrive()
+            self.copies.append((s, "B", (self.tiles[0], i)))
+            yield None
+        stage = phase = it = 0
         for t in self.tiles:
             for kb in range(self.num_kb):
-                yield from self.wait(self.empty[stage], phase ^ 1)
-                self.full[stage].expect_tx(1)
-                self.full[stage].arrive()
-                self.copies.append((stage, (t, kb)))
+                if it >= n_pre:
+                    yield from self.wait(self.empty[stage], phase ^ 1)
+                    self.full[stage].expect_tx(2)
+                    self.full[stage].arrive()
+                    self.copies.append((stage, "B", (t, kb)))
+                self.copies.append((stage, "A", (t, kb)))
+                it += 1
                 stage += 1
-                if stage == STAGES:
+                if stage == self.stages:
                     stage, phase = 0, phase ^ 1
 
     def issuer(self):
@@ -72,7 +86,7 @@ class Gemm:
                 if self.plant != "stage_released_early":
                     self.pipe.append(("commit", self.empty[stage]))
                 stage += 1
-                if stage == STAGES:
+                if stage == self.stages:
                     stage, phase = 0, phase ^ 1
             self.pipe.append(("commit", self.tmem_full[a]))
         self.pipe.append(("commit", self.drain))
@@ -93,7 +107,8 @@ class Gemm:
             op[1].arrive()
             return
         _, a, stage, (t, kb) = op
-        assert self.stage_holds[stage] == (t, kb), f"MMA ({t}, {kb}) read stage {stage} = {self.stage_holds[stage]}"
+        held = self.stage_holds[stage]
+        assert held.get("A") == (t, kb) and held.get("B") == (t, kb), f"MMA ({t}, {kb}) read stage {stage} = {held}"
         if kb == 0:
             prev = self.acc[a]
             assert prev is None or prev[0] in self.drained[a], f"tile {t} restarted accumulator {a} over {prev}"
@@ -103,8 +118,8 @@ class Gemm:
             self.acc[a] = (t, kb + 1)
 
     def copy_step(self, i):
-        stage, tag = self.copies.pop(i)
-        self.stage_holds[stage] = tag
+        stage, operand, tag = self.copies.pop(i)
+        self.stage_holds[stage][operand] = tag
         self.full[stage].tx_done(1)
 
     def run(self):
@@ -138,19 +153,24 @@ class Gemm:
         raise AssertionError("step limit")
 
 
-@pytest.mark.parametrize("n_tiles,num_kb", [(1, 1), (1, 7), (2, 3), (3, 5), (5, 2), (6, 13)])
-def test_protocol_finishes_and_reads_the_right_stages(n_tiles, num_kb):
+FORMS = {"pair": dict(stages=6, pre=False), "one_cta": dict(stages=4, pre=True)}
+
+
+@pytest.mark.parametrize("form", sorted(FORMS))
+@pytest.mark.parametrize("n_tiles,num_kb", [(1, 1), (1, 3), (1, 7), (2, 3), (3, 5), (5, 2), (6, 13)])
+def test_protocol_finishes_and_reads_the_right_stages(form, n_tiles, num_kb):
     for seed in range(40):
-        Gemm(list(range(10, 10 + n_tiles)), num_kb, seed * 31 + n_tiles).run()
+        Gemm(list(range(10, 10 + n_tiles)), num_kb, seed * 31 + n_tiles, **FORMS[form]).run()
 
 
-@pytest.mark.parametrize("plant", ["stage_released_early", "wrong_acc_phase"])
-def test_planted_mistakes_are_caught(plant):
+@pytest.mark.parametrize("form,plant", [("pair", "stage_released_early"), ("pair", "wrong_acc_phase"),
+                                        ("one_cta", "stage_released_early"), ("one_cta", "pre_overrun")])
+def test_planted_mistakes_are_caught(form, plant):
     caught = 0
     for n_tiles, num_kb in ((3, 4), (4, 7), (2, 9)):
         for seed in range(40):
             try:
-                Gemm(list(range(n_tiles)), num_kb, seed, plant).run()
+                Gemm(list(range(n_tiles)), num_kb, seed, plant, **FORMS[form]).run()
             except AssertionError:
                 caught += 1
     assert caught > 0, f"the model missed the planted mistake {plant}"

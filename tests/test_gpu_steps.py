@@ -99,15 +99,20 @@ def test_gemm_bf16(M, N, K):
     assert_bf16_elementwise(f64(C)[rows], ref, 2e-5 * absprod, f"gemm {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("T", [96, 171, 4608])
+# Layouts of the projection tests by token count: up to 128 tokens the GEMM
+# runs one-CTA 128-row tiles, above it CTA-pair 256-row tiles.
+STEP_SPECS = {1: [("txt", 1)], 96: synth.WORKLOADS["block_t96"]["spec"], 128: [("txt", 64), ("image", (8, 8))],
+              129: [("txt", 65), ("image", (8, 8))], 171: RAGGED,
+              512: [("txt", 160), ("image", (16, 20)), ("image_cond", (4, 8))],
+              4608: synth.WORKLOADS["block_1024sq_t4608"]["spec"],
+              6656: synth.WORKLOADS["stack28_1024sq_2ref512_t6656"]["spec"]}
+
+
+@pytest.mark.parametrize("T", [1, 96, 128, 129, 171, 4608])
 def test_in_projection(block1, T):
     w, blocks = block1
-    if T == 171:
-        lay = synth.build_layout(RAGGED)
-    elif T == 96:
-        lay = synth.build_layout(synth.WORKLOADS["block_t96"]["spec"])
-    else:
-        lay = synth.build_layout(synth.WORKLOADS["block_1024sq_t4608"]["spec"])
+    lay = synth.build_layout(STEP_SPECS[T])
+    assert lay.T == T
     pos, _ = layout_tensors(lay)
     hmod = synth.bf16_matrix(5, T, 3072, device=DEV)
     cs = torch.empty((T, 64), device=DEV)
@@ -229,6 +234,72 @@ def test_attention_split_against_unsplit():
     ref_abs = O.attention(q[rows, 0], q[:, 1], np.abs(q[:, 2])).reshape(len(rows), 256)
     bound = 2 * 2.0 ** -8 * (ref_abs + np.abs(ref)) * 1.01 + 2e-5 * ref_abs + 2e-6
     assert (np.abs(fa[rows] - fb[rows]) <= bound).all()
+
+
+@pytest.mark.parametrize("T,split", [(1, True), (96, False), (96, True), (128, True), (129, True), (171, False),
+                                     (171, True), (512, True), (4608, True), (6656, False), (6656, True)])
+def test_out_projection(block1, T, split):
+    """With a split buffer, the tiles of the GEMM's last, partial round of
+    tiles are split along K: up to 128 tokens the 12 one-CTA tiles in 12 ranges
+    each, at 129 and 171 tokens the 12 pair tiles in 6, at 512 the 24 pair
+    tiles in 3, at 6656 the 16 trailing pair tiles in 4; none at 4608, whose
+    last round is nearly full.  Without the buffer no tile is split.  Both
+    against the float64 product."""
+    w, blocks = block1
+    lay = synth.build_layout(STEP_SPECS[T])
+    assert lay.T == T
+    _, sid = layout_tensors(lay)
+    cat = synth.bf16_matrix(9, T, 12288, device=DEV)
+    x = synth.activations(9, T, device=DEV)
+    x0 = x.clone()
+    mods = synth.modulation(9, device=DEV)
+    F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), x.data_ptr(),
+                            _stream(), *_split_args(split))
+    assert F3.flux3_check_error(_stream()) == 0
+    wf = weights_f64(w)
+    rows = np.arange(T) if T <= 600 else sample_rows(T, lay.segments)
+    if T == 6656:   # every row of the trailing tiles (row blocks 24 and 25)
+        rows = np.union1d(rows, np.arange(6144, 6656, 7))
+    c = f64(cat)[rows]
+    y = c[:, :3072] @ wf["attn_out"].T + c[:, 3072:] @ wf["mlp_out"].T
+    gate = f64(mods)[lay.stream_id[rows], 6144:]
+    ref_delta = gate * y
+    got_delta = f64(x)[rows] - f64(x0)[rows]
+    assert_close(got_delta, ref_delta, 1e-3, 0.999999, f"out_projection T={T} split={split}")
+
+
+@pytest.mark.parametrize("T,row0", [(6656, 6144), (96, 0)])
+def test_out_projection_split_matches_unsplit_up_to_summation_order(block1, T, row0):
+    """The split changes only the order of the float32 sums of the trailing
+    tiles (rows row0 and on): the two results agree to float32 rounding, and
+    rows outside the trailing tiles are equal bit for bit."""
+    _, blocks = block1
+    lay = synth.build_layout(STEP_SPECS[T])
+    _, sid = layout_tensors(lay)
+    cat = synth.bf16_matrix(10, T, 12288, device=DEV)
+    x = synth.activations(10, T, device=DEV)
+    mods = synth.modulation(10, device=DEV)
+    a, b = x.clone(), x.clone()
+    F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), a.data_ptr(),
+                            _stream(), *_split_args(False))
+    F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), b.data_ptr(),
+                            _stream(), *_split_args(True))
+    assert F3.flux3_check_error(_stream()) == 0
+    assert torch.equal(a[:row0], b[:row0])
+    da, db = f64(a[row0:]) - f64(x[row0:]), f64(b[row0:]) - f64(x[row0:])
+    assert not np.array_equal(da, db)
+    # float32 sums of 12288 products in another grouping: ~1e-5 of RMS per
+    # element, its maximum over up to 1.5 M elements a few times that; both
+    # bounds are far inside the 1e-3 the oracle comparison above allows
+    rms = np.sqrt(np.mean(da * da))
+    assert np.abs(da - db).max() <= 5e-4 * rms
+    assert np.sqrt(np.mean((da - db) ** 2)) <= 5e-5 * rms
+    # and twice the same split call: bit for bit (fixed merge order)
+    c = x.clone()
+    F3.flux3_out_projection(blocks.handle, 0, cat.data_ptr(), T, sid.data_ptr(), mods.data_ptr(), c.data_ptr(),
+                            _stream(), *_split_args(True))
+    assert F3.flux3_check_error(_stream()) == 0
+    assert torch.equal(b, c)
 
 
 def test_timeout_path_reports_and_context_survives():
