@@ -70,6 +70,7 @@ constexpr size_t kSmem = 1024 + 2 * kTileBytes /*Q_A, Q_B*/ + 2 * kStages * kTil
 // A split item writes its rows unnormalised to part[v] (kPartRowFloats floats
 // per query row: 128 output values, the row max in the log2 domain, the row sum).
 constexpr int kPartRowFloats = 132;
+constexpr int kMaxSplits = 8;   // most key ranges a unit is split into
 constexpr size_t kPartItemBytes = (size_t)2 * kRows * kPartRowFloats * 4;
 struct Plan {
   int n_full, splits, n_qp;
@@ -181,9 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
-  // set-up above overlaps the previous kernel when launched as its programmatic dependent
-  griddep_wait();
+  // set-up above overlaps the previous kernel when launched as its programmatic
+  // dependent.  The out-projection after attention is released before the
+  // wait: before its own wait it only sets up and loads weights, which no
+  // kernel of the block writes after the in-projection has started (and this
+  // kernel starts only after that), so its CTAs can take SMs as the
+  // in-projection's CTAs leave.
   griddep_launch_dependents();
+  griddep_wait();
 
   if (warp >= kWarpTma) {
     // third warpgroup: one register share for all four of its warps (the
@@ -422,19 +428,35 @@ __global__ void __launch_bounds__(256)
   const int head = unit / plan.n_qp;
   const float *base = part + ((size_t)(unit - plan.n_full) * plan.splits * 2 * kRows + row_in_unit) * kPartRowFloats;
   const size_t item_stride = (size_t)2 * kRows * kPartRowFloats;
+  // every range's (m, l, O slice) is loaded before any is used (one round
+  // trip, not one per range); the sums run in range order
+  float m[kMaxSplits], lk[kMaxSplits];
+  float4 v[kMaxSplits];
+#pragma unroll
+  for (int k = 0; k < kMaxSplits; ++k) {
+    if (k < plan.splits) {
+      const float *p = base + k * item_stride;
+      m[k] = __ldg(p + 128);
+      lk[k] = __ldg(p + 129);
+      v[k] = __ldg(reinterpret_cast<const float4 *>(p) + lane);
+    }
+  }
   float mx = -INFINITY;
-  for (int k = 0; k < plan.splits; ++k) mx = fmaxf(mx, __ldg(base + k * item_stride + 128));
+#pragma unroll
+  for (int k = 0; k < kMaxSplits; ++k)
+    if (k < plan.splits) mx = fmaxf(mx, m[k]);
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float l = 0.f;
-  for (int k = 0; k < plan.splits; ++k) {
-    const float *p = base + k * item_stride;
-    const float w = ex2_approx(__ldg(p + 128) - mx);
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(p) + lane);
-    o.x = fmaf(v.x, w, o.x);
-    o.y = fmaf(v.y, w, o.y);
-    o.z = fmaf(v.z, w, o.z);
-    o.w = fmaf(v.w, w, o.w);
-    l = fmaf(__ldg(p + 129), w, l);
+#pragma unroll
+  for (int k = 0; k < kMaxSplits; ++k) {
+    if (k < plan.splits) {
+      const float w = ex2_approx(m[k] - mx);
+      o.x = fmaf(v[k].x, w, o.x);
+      o.y = fmaf(v[k].y, w, o.y);
+      o.z = fmaf(v[k].z, w, o.z);
+      o.w = fmaf(v[k].w, w, o.w);
+      l = fmaf(lk[k], w, l);
+    }
   }
   const float inv = 1.0f / l;
   *reinterpret_cast<uint2 *>(out + (size_t)t * kCatCols + head * kHeadDim + lane * 4) =
@@ -456,7 +478,7 @@ Plan attention_plan(int T, int sms, float *part, size_t part_bytes) {
   if (!part || sms < 1) return p;
   const int full = units / sms * sms, rem = units - full;
   if (rem == 0) return p;
-  for (int S = 8; S >= 2; --S) {
+  for (int S = kMaxSplits; S >= 2; --S) {
     if (rem * S > sms || nt / S < 4 || (size_t)rem * S * kPartItemBytes > part_bytes) continue;
     p.n_full = full;
     p.splits = S;

@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kLnWarps * 32, 2)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * kLnWarps + warp;
   if (t >= T) return;
+  const int s = sid[t];   // issued with the row's loads: one round trip fewer before the modulation rows
   const float4 *xr = reinterpret_cast<const float4 *>(x + (size_t)t * kHidden);
   float4 v[kVec];
   float sum = 0.f;
@@ -105,6 +106,8 @@ __global__ void __launch_bounds__(kLnWarps * 32, 2)
     v[i] = __ldcs(xr + i * 32 + lane);
     sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
   }
+  const float4 *shift = reinterpret_cast<const float4 *>(mod + (size_t)s * kModLen);
+  const float4 *scale = reinterpret_cast<const float4 *>(mod + (size_t)s * kModLen + kHidden);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   const float mean = sum * (1.0f / kHidden);
@@ -117,9 +120,6 @@ __global__ void __launch_bounds__(kLnWarps * 32, 2)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
   const float rstd = rsqrtf(sq * (1.0f / kHidden) + eps);
-  const int s = sid[t];
-  const float4 *shift = reinterpret_cast<const float4 *>(mod + (size_t)s * kModLen);
-  const float4 *scale = reinterpret_cast<const float4 *>(mod + (size_t)s * kModLen + kHidden);
   uint2 *hr = reinterpret_cast<uint2 *>(h + (size_t)t * kHidden);
 #pragma unroll
   for (int i = 0; i < kVec; ++i) {

@@ -46,6 +46,7 @@ namespace flux3 {
 namespace gemm_detail {
 
 constexpr int kThreads = 320;
+constexpr int kMaxSplitK = 12;   // most K ranges a split tile takes
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kBoxBytes = 32 * 128;              // one epilogue output box: 32 rows x 64 bf16
 constexpr uint32_t kTmemCols = 512;                   // two 128-lane x 256-column fp32 accumulators
@@ -414,11 +415,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int *abort = &ctl->abort;
   // One-CTA form (small M, bound by streaming the weights B from DRAM): the
-  // B halves of the first ring stages are loaded before griddep_wait.  B is
-  // never written by the kernels this one may overlap (each kernel of the
-  // chain waits for its predecessor before releasing its own dependents, so
-  // everything before the previous kernel has completed), so the DRAM latency
-  // of the first tiles passes while the previous kernel finishes.  The A
+  // B halves of the first ring stages are loaded before griddep_wait, so the
+  // DRAM latency of the first tiles passes while the previous kernel
+  // finishes.  No kernel this one may overlap writes B: the weights are
+  // constant or expanded at the start of the block, and the in-projection
+  // starts only after its predecessor (LayerNorm) has waited for everything
+  // before it, the out-projection only after the in-projection has.  The A
   // halves, which the previous kernel may write, follow after the wait.
   int n_pre = 0;
   if constexpr (!kPair) {
@@ -637,18 +639,27 @@ __global__ void split_merge_residual_kernel(const float *__restrict__ part, int 
   tile_coords(n_full + i, num_m, num_n, n_fast != 0, m_blk, n_blk);
   const int row = m_blk * tile_m + r;
   if (r >= tile_m || row >= M) return;
-  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int ks = 0; ks < splits; ++ks) {
-    const float4 p = __ldcs(reinterpret_cast<const float4 *>(part + ((size_t)(i * splits + ks) * tile_m + r) * kBN + c));
-    y.x += p.x;
-    y.y += p.y;
-    y.z += p.z;
-    y.w += p.w;
-  }
+  // every partial, x and the gate are loaded before any is used (one round
+  // trip, not one per range); the sum runs in range order
   const int col = n_blk * kBN + c;
-  const float4 g = __ldg(reinterpret_cast<const float4 *>(mod + (size_t)sid[row] * kModLen + 2 * kHidden + col));
   float4 *xp = reinterpret_cast<float4 *>(x + (size_t)row * kHidden + col);
   float4 xv = *xp;
+  const float4 g = __ldg(reinterpret_cast<const float4 *>(mod + (size_t)sid[row] * kModLen + 2 * kHidden + col));
+  float4 p[kMaxSplitK];
+#pragma unroll
+  for (int ks = 0; ks < kMaxSplitK; ++ks)
+    if (ks < splits)
+      p[ks] = __ldcs(reinterpret_cast<const float4 *>(part + ((size_t)(i * splits + ks) * tile_m + r) * kBN + c));
+  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int ks = 0; ks < kMaxSplitK; ++ks) {
+    if (ks < splits) {
+      y.x += p[ks].x;
+      y.y += p[ks].y;
+      y.z += p[ks].z;
+      y.w += p[ks].w;
+    }
+  }
   xv.x = fmaf(g.x, y.x, xv.x);
   xv.y = fmaf(g.y, y.y, xv.y);
   xv.z = fmaf(g.z, y.z, xv.z);
@@ -674,7 +685,7 @@ void split_plan(int EPI, int M, int N, int K, int tile_m, int workers, size_t pa
   if (EPI != EPI_OUT_RESIDUAL || workers < 2) return;
   const int full = tiles / workers * workers, rem = tiles - full;
   if (rem == 0) return;
-  const int cand[6] = {12, 8, 6, 4, 3, 2};
+  const int cand[6] = {kMaxSplitK, 8, 6, 4, 3, 2};
   for (int S : cand) {
     const int units = rem * S;
     if (num_kb % S != 0 || num_kb / S < 16 || units > workers) continue;

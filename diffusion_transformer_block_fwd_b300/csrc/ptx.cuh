@@ -101,11 +101,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
 }
 // 2-D tiled store of a shared-memory box to global memory (bulk-group
 // completion); boxes past the tensor's extent are clipped.
-// Hint: fetch `bytes` (a multiple of 16) of global memory at `p` (16-byte
-// aligned) into L2; no shared memory, no completion signal.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, const void *src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tm),
                "r"(smem_addr(src)), "r"(c0), "r"(c1)
