@@ -258,8 +258,17 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
   // attention's key-range partials may use only memory that is dead while it
   // runs: h when the split region lies over h and qkv (attention reads qkv)
   const size_t attn_part_bytes = split_in_place((size_t)T) ? ws_round((size_t)T * kHidden * 2) : kSplitBytes;
+  // NVFP4 at small T: the GEMMs read the e2m1 codes and expand them in shared
+  // memory (the weight stream bounds them there); otherwise the block's
+  // weights are expanded to bf16 in the workspace first
+  const bool fp4_in_gemm = h->cfg.wfmt == FLUX3_W_NVFP4 && T <= kFp4GemmMaxRows;
   for (int b = first; b < first + count; ++b) {
-    if (h->cfg.wfmt == FLUX3_W_NVFP4) F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s, true));
+    CUtensorMap tmCin, tmCout;
+    if (fp4_in_gemm && (!make_tmap_u8(&tmCin, h->fp4[b].in_codes, kInRows, kHidden / 2, kBK / 2, 256) ||
+                        !make_tmap_u8(&tmCout, h->fp4[b].out_codes, kHidden, kCatCols / 2, kBK / 2, 256)))
+      return FLUX3_ERR_CUDA;
+    if (h->cfg.wfmt == FLUX3_W_NVFP4 && !fp4_in_gemm)
+      F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s, true));
     if (h->cfg.wfmt == FLUX3_W_FP8R) F3_CUDA(launch_dequantize_fp8r_block(h->fp8[b], ws.w_in, ws.w_out, s, true));
     F3_CUDA(launch_ln_modulate(x, T, ws.sid, mod, h->cfg.eps_ln, ws.h, s, true));
     EpiParams ep{};
@@ -270,7 +279,13 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     ep.qnorm = block_norms(h, b);
     ep.knorm = block_norms(h, b) + kHeadDim;
     ep.eps_rms = h->cfg.eps_rms;
-    F3_CUDA(launch_gemm(EPI_IN_PROJ, tmH, fp4 ? tmWin : h->tm_in[b], T, kInRows, kHidden, ep, s, true));
+    if (fp4_in_gemm) {
+      ep.w_scales = h->fp4[b].in_scales;
+      ep.w_globals = h->fp4[b].globals;
+      F3_CUDA(launch_gemm_fp4(EPI_IN_PROJ, tmH, tmCin, T, kInRows, kHidden, ep, s, true));
+    } else {
+      F3_CUDA(launch_gemm(EPI_IN_PROJ, tmH, fp4 ? tmWin : h->tm_in[b], T, kInRows, kHidden, ep, s, true));
+    }
     for (int smp = 0; smp < n_samples; ++smp) {   // attention within each sample
       const int r0 = sample_start[smp];
       F3_CUDA(launch_attention(ws.qkv + (size_t)r0 * kQkvCols, sample_start[smp + 1] - r0,
@@ -282,7 +297,13 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     eo.mod = mod;
     eo.part = ws.part;
     eo.part_bytes = kSplitBytes;
-    F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, fp4 ? tmWout : h->tm_out[b], T, kHidden, kCatCols, eo, s, true));
+    if (fp4_in_gemm) {
+      eo.w_scales = h->fp4[b].out_scales;
+      eo.w_globals = h->fp4[b].globals;
+      F3_CUDA(launch_gemm_fp4(EPI_OUT_RESIDUAL, tmCat, tmCout, T, kHidden, kCatCols, eo, s, true));
+    } else {
+      F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, fp4 ? tmWout : h->tm_out[b], T, kHidden, kCatCols, eo, s, true));
+    }
   }
   return FLUX3_OK;
 }
@@ -318,6 +339,20 @@ bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t c
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_u8(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                  uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !aligned16(base) || cols % 16 != 0 || box_cols % 16 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -50,6 +50,11 @@ struct EpiParams {
   // tiles (tile rows x 256 per split unit); null / too small: no split
   float *part;
   size_t part_bytes;
+  // NVFP4 weights expanded inside the GEMM (launch_gemm_fp4): the e4m3 block
+  // scales [N, K / 16] (4-byte aligned) and the block's float32 tensor scales
+  // (q, k, v, mlp_in, attn_out, mlp_out)
+  const uint8_t *w_scales;
+  const float *w_globals;
 };
 
 // Size of the split partial buffer: 96 partial tiles of the CTA-pair form
@@ -62,6 +67,11 @@ static_assert(kSplitBytes == FLUX3_SPLIT_BYTES, "split scratch size of the heade
 // Encodes a 2-D bf16 tensor map over a row-major [rows, cols] matrix with a
 // {64 cols, box_rows} box and 128-byte swizzle.  Returns false on failure.
 bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// Encodes a 2-D uint8 tensor map over a row-major [rows, cols] byte matrix
+// with a {box_cols, box_rows} box and no swizzle.  Returns false on failure.
+bool make_tmap_u8(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                  uint32_t box_rows);
 
 // Encodes a 2-D float32 tensor map over a row-major [rows, cols] matrix with a
 // {32 cols, 32 rows} box and 128-byte swizzle.  Returns false on failure.
@@ -110,6 +120,15 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K,
                         const EpiParams &ep, cudaStream_t s, bool pdl = false);
+
+// The block GEMMs (EPI_IN_PROJ, EPI_OUT_RESIDUAL) over NVFP4 weights for M <=
+// kFp4GemmMaxRows (one-CTA tiles): tmCodes maps the e2m1 code bytes [N, K / 2]
+// (make_tmap_u8 with 32-byte x 256-row boxes); ep.w_scales / ep.w_globals
+// hold the block scales and tensor scales.  The weights are expanded to bf16
+// in shared memory, never in HBM.
+constexpr int kFp4GemmMaxRows = 128;
+cudaError_t launch_gemm_fp4(int mode, const CUtensorMap &tmA, const CUtensorMap &tmCodes, int M, int N, int K,
+                            const EpiParams &ep, cudaStream_t s, bool pdl = false);
 
 cudaError_t launch_stream_ids(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, cudaStream_t s);
 cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_tab, float *sin_tab,

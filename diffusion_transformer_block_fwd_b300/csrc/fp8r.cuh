@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(256)
       const uint32_t word = words[k / 2];
       float a = value_of_code[(word >> (16 * (k % 2))) & 0xFFu];
       float b = value_of_code[(word >> (16 * (k % 2) + 8)) & 0xFFu];
-      fp4_detail::mul2(a, b, s);
+      mul2(a, b, s);
       o[k] = pack_bf16x2(a, b);
     }
     uint4 *dst = reinterpret_cast<uint4 *>((in ? w_in : w_out) + (size_t)ci * kChunk);

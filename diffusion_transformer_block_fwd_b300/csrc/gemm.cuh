@@ -38,6 +38,8 @@
 
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "flux3_internal.h"
 #include "ptx.cuh"
 
@@ -51,7 +53,7 @@ constexpr int kEpiWarps = 8;
 constexpr uint32_t kBoxBytes = 32 * 128;              // one epilogue output box: 32 rows x 64 bf16
 constexpr uint32_t kTmemCols = 512;                   // two 128-lane x 256-column fp32 accumulators
 
-template <int kStages>
+template <int kStages, int kCodeStages, int kBStages>
 struct SharedCtl {
   uint64_t full[kStages];      // issuing CTA: the stage's TMA bytes (both CTAs' for a pair) landed
   uint64_t empty[kStages];     // every CTA: the stage's MMAs are done
@@ -59,29 +61,86 @@ struct SharedCtl {
   uint64_t tmem_empty[2];      // issuing CTA: every epilogue thread (of the pair) drained it
   uint64_t drain;
   uint64_t xbar[8];            // per epilogue warp: its residual box landed (out-projection)
+  // NVFP4 weights (one-CTA form): the code ring and the converted B stages
+  uint64_t cfull[kCodeStages];    // a k-block's e2m1 codes landed
+  uint64_t cempty[kCodeStages];   // every converting thread has read them
+  uint64_t bready[kBStages];      // every converting thread has written its B row of the stage
+  uint64_t bempty[kBStages];      // the stage's MMAs are done (its B rows may be rewritten)
   uint32_t tmem_base;
   int abort;
 };
 
-// The two forms of the kernel.  Pair (kPair): a cluster of two CTAs on one
-// TPC computes a 256 x 256 tile with cta_group::2 MMAs; each CTA stages 128 A
+// The forms of the kernel.  Pair (kPair): a cluster of two CTAs on one TPC
+// computes a 256 x 256 tile with cta_group::2 MMAs; each CTA stages 128 A
 // rows and 128 B rows per k-block.  Single: one CTA computes a 128 x 256 tile
 // with cta_group::1 MMAs and stages 128 A rows and all 256 B rows.  The
 // single form serves M <= 128, where a pair tile would be at most half rows.
-template <bool kPair>
+// kFp4 (single form only): B arrives as NVFP4 e2m1 codes (a quarter of the
+// bf16 bytes) in a ring of its own, and the epilogue warps, idle while the
+// tile accumulates, expand each k-block into the bf16 B stage the MMA reads.
+// The A and B stages then form separate rings: A (from L2) five deep, the
+// expanded B two deep (the expansion works out of shared memory, so one stage
+// in hand while the MMAs read the other is enough).
+template <bool kPair, bool kFp4 = false>
 struct GemmCfg {
-  static constexpr int kStages = kPair ? 6 : 4;
+  static_assert(!(kPair && kFp4), "NVFP4 weights are expanded in the one-CTA form only");
+  static constexpr int kStages = kPair ? 6 : (kFp4 ? 5 : 4);   // A stages (and B stages without kFp4)
+  static constexpr int kBStages = kFp4 ? 2 : kStages;
+  static constexpr int kCodeStages = kFp4 ? 5 : 1;
   static constexpr int kTileM = kPair ? 256 : 128;                     // output rows per tile
   static constexpr uint32_t kABytes = 128 * kBK * 2;                   // 16 KB: 128 A rows per CTA
   static constexpr uint32_t kBBytes = (kPair ? 128 : 256) * kBK * 2;   // B rows per CTA
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kTxBytes = (kPair ? 2 : 1) * kStageBytes;  // completing on one stage barrier
-  static constexpr size_t kSmemBytes =
-      1024 /*alignment slack*/ + kStages * kStageBytes + kEpiWarps * kBoxBytes + sizeof(SharedCtl<kStages>);
+  static constexpr uint32_t kCodeBytes = kFp4 ? 256 * kBK / 2 : 0;     // 8 KB: 256 rows x 64 e2m1 codes
+  // bytes completing on one stage barrier (with NVFP4 weights: A only)
+  static constexpr uint32_t kTxBytes = kFp4 ? kABytes : (kPair ? 2 : 1) * kStageBytes;
+  static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kABytes + kBStages * kBBytes +
+                                       (kFp4 ? kCodeStages * kCodeBytes : 0) + kEpiWarps * kBoxBytes +
+                                       sizeof(SharedCtl<kStages, kCodeStages, kBStages>);
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
+
+// One B row of a k-block from NVFP4: 64 e2m1 codes (32 bytes at `codes`, two
+// per byte, the lower nibble first), their four e4m3 block scales (one per 16
+// inputs, byte j of `scales4`) and the tensor's float32 scale g.  Each weight
+// is e2m1 * e4m3 (exact in f16: at most 6 significant bits, within 2^-10 ..
+// 2688), widened to float32, times g (rounded to float32), rounded to bf16 --
+// the expansion kernel's arithmetic, so the MMA sees the same bf16 values.
+// The row's eight 16-byte chunks go to the 128-byte-swizzled K-major layout
+// of the B stage (row r of the stage at (r / 8) * 1024 + (r % 8) * 128).
+__device__ __forceinline__ void expand_fp4_row(const uint8_t *codes, uint32_t scales4, float g, uint8_t *b_stage,
+                                               int r) {
+  const uint4 c0 = *reinterpret_cast<const uint4 *>(codes);
+  const uint4 c1 = *reinterpret_cast<const uint4 *>(codes + 16);
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  uint32_t s01, s23;   // f16x2 pairs of the four block scales
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+      : "=r"(s01), "=r"(s23)
+      : "r"(scales4));
+  const __half2 sp[2] = {*reinterpret_cast<const __half2 *>(&s01), *reinterpret_cast<const __half2 *>(&s23)};
+  uint8_t *row = b_stage + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {   // chunk q: inputs 8q .. 8q+7 of group q / 2
+    uint32_t h[4];
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+        " cvt.rn.f16x2.e2m1x2 %1, b1;\n cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w[q]));
+    const int grp = q >> 1;
+    const __half2 s = (grp & 1) ? __high2half2(sp[grp >> 1]) : __low2half2(sp[grp >> 1]);
+    uint32_t o[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h[b]), s);   // exact
+      float lo = __low2float(v), hi = __high2float(v);
+      mul2(lo, hi, g);
+      o[b] = pack_bf16x2(lo, hi);
+    }
+    *reinterpret_cast<uint4 *>(row + ((q ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
 
 // Waits for `bar` to pass `parity`, with a time limit only (used while
 // draining after an abort, when the abort flag is already set).
@@ -353,19 +412,25 @@ __device__ __forceinline__ void store_partial_half(uint32_t taddr, int slot, int
   }
 }
 
-template <int EPI, bool kPair>
+// tmB: the bf16 weight, or with kFp4 the e2m1 code bytes of the weight
+// ([N, K / 2] uint8, boxes of 32 bytes x 256 rows; ep.w_scales and
+// ep.w_globals hold the block scales and the tensors' float32 scales).
+template <int EPI, bool kPair, bool kFp4>
 __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmO0,
                                           const CUtensorMap &tmO1, int M, int N, int K, int n_full, int splits,
                                           const EpiParams &ep) {
-  using C = GemmCfg<kPair>;
+  using C = GemmCfg<kPair, kFp4>;
   constexpr int kStages = C::kStages;
+  constexpr int kBStages = C::kBStages;
+  constexpr int kCodeStages = C::kCodeStages;
   constexpr int kTileM = C::kTileM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *smA = smem;
   uint8_t *smB = smem + kStages * C::kABytes;
-  uint8_t *sOut = smem + kStages * C::kStageBytes;     // [epilogue warp] 4 KB output box
-  auto *ctl = reinterpret_cast<SharedCtl<kStages> *>(sOut + kEpiWarps * kBoxBytes);
+  uint8_t *smC = smB + kBStages * C::kBBytes;                        // NVFP4 code ring
+  uint8_t *sOut = smC + (kFp4 ? kCodeStages * C::kCodeBytes : 0);   // [epilogue warp] 4 KB output box
+  auto *ctl = reinterpret_cast<SharedCtl<kStages, kCodeStages, kBStages> *>(sOut + kEpiWarps * kBoxBytes);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -394,6 +459,16 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
     }
     mbar_init(&ctl->drain, 1);
     for (int w = 0; w < kEpiWarps; ++w) mbar_init(&ctl->xbar[w], 1);
+    if constexpr (kFp4) {
+      for (int s = 0; s < kCodeStages; ++s) {
+        mbar_init(&ctl->cfull[s], 1);
+        mbar_init(&ctl->cempty[s], kEpiWarps * 32);
+      }
+      for (int s = 0; s < kBStages; ++s) {
+        mbar_init(&ctl->bready[s], kEpiWarps * 32);
+        mbar_init(&ctl->bempty[s], 1);
+      }
+    }
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -427,7 +502,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
   // before it, the out-projection only after the in-projection has.  The A
   // halves, which the previous kernel may write, follow after the wait.
   int n_pre = 0;
-  if constexpr (!kPair) {
+  if constexpr (kFp4) {
+    // the codes of the first k-blocks (lane 1 runs the code ring)
+    if (warp == 0 && lane == 1 && worker < num_units) {
+      const Unit un = unit_of(worker, n_full, splits, num_m, num_n, n_fast, num_kb);
+      n_pre = un.kb1 - un.kb0 < kCodeStages ? un.kb1 - un.kb0 : kCodeStages;
+      for (int i = 0; i < n_pre; ++i) {
+        mbar_arrive_expect_tx(&ctl->cfull[i], C::kCodeBytes);
+        tma_load_2d(smC + i * C::kCodeBytes, &tmB, &ctl->cfull[i], (un.kb0 + i) * (kBK / 2), un.n_blk * kBN);
+      }
+    }
+  } else if constexpr (!kPair) {
     if (warp == 0 && lane == 0 && worker < num_units) {
       const Unit un = unit_of(worker, n_full, splits, num_m, num_n, n_fast, num_kb);
       n_pre = un.kb1 - un.kb0 < kStages ? un.kb1 - un.kb0 : kStages;
@@ -458,7 +543,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
         const int a_row = un.m_blk * kTileM + (int)rank * 128;
         const int b_row = un.n_blk * kBN + (int)rank * 128;
         for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
-          const bool pre = it < n_pre;   // a fresh stage: no wait for it to drain
+          const bool pre = !kFp4 && it < n_pre;   // a fresh stage: no wait for it to drain
           if (!pre && !mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) {
             ok = false;
             break;
@@ -470,6 +555,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
             if (leader) mbar_arrive_expect_tx(&ctl->full[stage], C::kTxBytes);
             tma_load_2d_pair(a_dst, &tmA, full_leader, kb * kBK, a_row);
             tma_load_2d_pair(b_dst, &tmB, full_leader, kb * kBK, b_row);
+          } else if constexpr (kFp4) {
+            mbar_arrive_expect_tx(&ctl->full[stage], C::kTxBytes);   // B is written by the converting warps
+            tma_load_2d(a_dst, &tmA, &ctl->full[stage], kb * kBK, a_row);
           } else {
             if (!pre) {
               mbar_arrive_expect_tx(&ctl->full[stage], C::kTxBytes);
@@ -489,6 +577,35 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
         for (int s = 0; s < kStages; ++s)
           if (last_phase[s] >= 0) drain_wait(&ctl->full[s], (uint32_t)last_phase[s]);
       }
+    } else if (kFp4 && lane == 1) {
+      // ---------------- NVFP4 code ring: each k-block's 256 x 32 code bytes
+      int last_phase[kCodeStages];
+#pragma unroll
+      for (int s = 0; s < kCodeStages; ++s) last_phase[s] = -1;
+      uint32_t cs = 0, cphase = 0;
+      bool ok = true;
+      int it = 0;   // the first n_pre k-blocks went out before griddep_wait
+      for (int u = worker; u < num_units && ok; u += num_workers) {
+        const Unit un = unit_of(u, n_full, splits, num_m, num_n, n_fast, num_kb);
+        for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
+          if (it >= n_pre) {
+            if (!mbar_wait(&ctl->cempty[cs], cphase ^ 1, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&ctl->cfull[cs], C::kCodeBytes);
+            tma_load_2d(smC + cs * C::kCodeBytes, &tmB, &ctl->cfull[cs], kb * (kBK / 2), un.n_blk * kBN);
+          }
+          last_phase[cs] = (int)cphase;
+          if (++cs == kCodeStages) {
+            cs = 0;
+            cphase ^= 1;
+          }
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < kCodeStages; ++s)
+          if (last_phase[s] >= 0) drain_wait(&ctl->cfull[s], (uint32_t)last_phase[s]);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -499,6 +616,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
       const SmemDesc da = smem_desc_split(smem_addr(smA), 16, 1024, kSwizzle128B);
       const SmemDesc db = smem_desc_split(smem_addr(smB), 16, 1024, kSwizzle128B);
       uint32_t stage = 0, phase = 0;
+      uint32_t bstage = 0, bphase = 0;   // the B ring (its own with kFp4, else the same as the A ring)
       int local = 0;
       bool ok = true;
       for (int u = worker; u < num_units && ok; u += num_workers, ++local) {
@@ -509,28 +627,34 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
-          if (!mbar_wait(&ctl->full[stage], phase, abort)) {
+          if (!mbar_wait(&ctl->full[stage], phase, abort) ||
+              (kFp4 && !mbar_wait(&ctl->bready[bstage], bphase, abort))) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint32_t boff = (kFp4 ? bstage : stage) * C::kBBytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint32_t accumulate = (kb != un.kb0 || k != 0) ? 1u : 0u;
             if constexpr (kPair)
-              mma_bf16_ss_pair_at(d_tmem, da, stage * C::kABytes + k * 32, db, stage * C::kBBytes + k * 32, idesc,
-                                  accumulate);
+              mma_bf16_ss_pair_at(d_tmem, da, stage * C::kABytes + k * 32, db, boff + k * 32, idesc, accumulate);
             else
-              mma_bf16_ss_at(d_tmem, da, stage * C::kABytes + k * 32, db, stage * C::kBBytes + k * 32, idesc,
-                             accumulate);
+              mma_bf16_ss_at(d_tmem, da, stage * C::kABytes + k * 32, db, boff + k * 32, idesc, accumulate);
           }
-          if constexpr (kPair)
+          if constexpr (kPair) {
             mma_commit_pair_mc(&ctl->empty[stage], 0x3);
-          else
+          } else {
             mma_commit(&ctl->empty[stage]);
+            if constexpr (kFp4) mma_commit(&ctl->bempty[bstage]);
+          }
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
+          }
+          if (++bstage == kBStages) {
+            bstage = 0;
+            bphase ^= 1;
           }
         }
         if (ok) {
@@ -563,6 +687,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
     bool x_in_flight = false;   // broke out with a residual box load outstanding
     const uint32_t empty_leader0 = map_to_cta(smem_addr(&ctl->tmem_empty[0]), 0);
     const uint32_t empty_leader1 = map_to_cta(smem_addr(&ctl->tmem_empty[1]), 0);
+    // NVFP4: this thread expands B row conv_r of every k-block, following the
+    // code ring (cs) and the A / B stage ring (stage) in the producer's order
+    const int conv_r = (warp - 2) * 32 + lane;
+    uint32_t cs = 0, cphase = 0, bstage = 0, bphase = 0;
     int local = 0;
     for (int u = worker; u < num_units; u += num_workers, ++local) {
       const Unit un = unit_of(u, n_full, splits, num_m, num_n, n_fast, num_kb);
@@ -574,6 +702,46 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
         if (un.slot < 0) {
           bw.begin();
           load_x_box(bw, &tmO0, xbar, un.n_blk * kBN + half * 128, un.m_blk * kTileM + row_in_tile - lane);
+        }
+      }
+      if constexpr (kFp4) {
+        static_assert(EPI == EPI_IN_PROJ || EPI == EPI_OUT_RESIDUAL, "NVFP4 weights of the block GEMMs only");
+        const uint32_t *srow = reinterpret_cast<const uint32_t *>(ep.w_scales + (size_t)(un.n_blk * kBN + conv_r) * (K / 16));
+        // the tensor's float32 scale: by row block (q, k, v, mlp_in) for the
+        // in-projection, by input column (attn_out, mlp_out) for the out-projection
+        const int gi_q = un.n_blk / (kHidden / kBN);
+        const float g_lo = __ldg(ep.w_globals + (EPI == EPI_IN_PROJ ? (gi_q < 3 ? gi_q : 3) : 4));
+        const float g_hi = EPI == EPI_IN_PROJ ? g_lo : __ldg(ep.w_globals + 5);
+        // the row's four block scales of a k-block are one 32-bit word; the
+        // words go out two k-blocks ahead of their use
+        uint32_t s_cur = un.kb0 < un.kb1 ? __ldg(srow + un.kb0) : 0u;
+        uint32_t s_nxt = un.kb0 + 1 < un.kb1 ? __ldg(srow + un.kb0 + 1) : 0u;
+        bool conv_ok = true;
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+          const float g = (EPI == EPI_OUT_RESIDUAL && kb * kBK >= kHidden) ? g_hi : g_lo;
+          const uint32_t s4 = s_cur;
+          s_cur = s_nxt;
+          s_nxt = kb + 2 < un.kb1 ? __ldg(srow + kb + 2) : 0u;
+          if (!mbar_wait(&ctl->cfull[cs], cphase, abort) || !mbar_wait(&ctl->bempty[bstage], bphase ^ 1, abort)) {
+            conv_ok = false;
+            break;
+          }
+          expand_fp4_row(smC + cs * C::kCodeBytes + conv_r * (kBK / 2), s4, g, smB + bstage * C::kBBytes, conv_r);
+          fence_proxy_async_smem();       // the MMA reads the row through the async proxy
+          mbar_arrive(&ctl->bready[bstage]);
+          mbar_arrive(&ctl->cempty[cs]);
+          if (++cs == kCodeStages) {
+            cs = 0;
+            cphase ^= 1;
+          }
+          if (++bstage == kBStages) {
+            bstage = 0;
+            bphase ^= 1;
+          }
+        }
+        if (!conv_ok) {
+          x_in_flight = EPI == EPI_OUT_RESIDUAL && un.slot < 0;
+          break;
         }
       }
       if (!mbar_wait(&ctl->tmem_full[acc], acc_phase, abort)) {
@@ -616,7 +784,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
                 int K, int n_full, int splits, EpiParams ep) {
-  gemm_body<EPI, true>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
+  gemm_body<EPI, true, false>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
 }
 
 template <int EPI>
@@ -624,7 +792,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm1_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
                  int K, int n_full, int splits, EpiParams ep) {
-  gemm_body<EPI, false>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
+  gemm_body<EPI, false, false>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
+}
+
+// The one-CTA form over NVFP4 weights (tmB: the e2m1 code bytes).
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm1_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
+                     int K, int n_full, int splits, EpiParams ep) {
+  gemm_body<EPI, false, true>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
 }
 
 // Sums the split units of each trailing tile in a fixed order (unit 0 first)
@@ -700,11 +877,16 @@ void split_plan(int EPI, int M, int N, int K, int tile_m, int workers, size_t pa
   }
 }
 
-template <int EPI, bool kPair>
+template <int EPI, bool kPair, bool kFp4 = false>
 cudaError_t launch_form(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K, const EpiParams &ep,
                         cudaStream_t s, bool pdl) {
-  using C = GemmCfg<kPair>;
-  auto kernel = kPair ? gemm_kernel<EPI> : gemm1_kernel<EPI>;
+  using C = GemmCfg<kPair, kFp4>;
+  auto kernel = [] {
+    if constexpr (kFp4)
+      return gemm1_fp4_kernel<EPI>;
+    else
+      return kPair ? gemm_kernel<EPI> : gemm1_kernel<EPI>;
+  }();
   static std::atomic<bool> attr_set[kMaxDevices];
   const cudaError_t e = set_smem_once(kernel, (int)C::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
@@ -745,6 +927,17 @@ cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, i
   return launch_form<EPI, true>(tmA, tmB, M, N, K, ep, s, pdl);
 }
 
+// Wraps the EPI_IN_PROJ / EPI_OUT_RESIDUAL NVFP4 forms (the only EPIs the
+// expansion in the epilogue warps serves) for the mode switch below.
+template <int EPI>
+cudaError_t launch_fp4_mode(const CUtensorMap &tmA, const CUtensorMap &tmCodes, int M, int N, int K,
+                            const EpiParams &ep, cudaStream_t s, bool pdl) {
+  if constexpr (EPI == EPI_IN_PROJ || EPI == EPI_OUT_RESIDUAL)
+    return launch_form<EPI, false, true>(tmA, tmCodes, M, N, K, ep, s, pdl);
+  else
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace gemm_detail
 
 cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K,
@@ -755,6 +948,17 @@ cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB
     case EPI_IN_PROJ: return launch_mode<EPI_IN_PROJ>(tmA, tmB, M, N, K, ep, s, pdl);
     case EPI_OUT_RESIDUAL: return launch_mode<EPI_OUT_RESIDUAL>(tmA, tmB, M, N, K, ep, s, pdl);
     case EPI_STORE_F32: return launch_mode<EPI_STORE_F32>(tmA, tmB, M, N, K, ep, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm_fp4(int mode, const CUtensorMap &tmA, const CUtensorMap &tmCodes, int M, int N, int K,
+                            const EpiParams &ep, cudaStream_t s, bool pdl) {
+  using namespace gemm_detail;
+  if (M < 1 || M > kFp4GemmMaxRows || !ep.w_scales || !ep.w_globals) return cudaErrorInvalidValue;
+  switch (mode) {
+    case EPI_IN_PROJ: return launch_fp4_mode<EPI_IN_PROJ>(tmA, tmCodes, M, N, K, ep, s, pdl);
+    case EPI_OUT_RESIDUAL: return launch_fp4_mode<EPI_OUT_RESIDUAL>(tmA, tmCodes, M, N, K, ep, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

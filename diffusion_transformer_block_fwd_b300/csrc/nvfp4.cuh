@@ -156,13 +156,6 @@ struct Fp4BlockView {
 constexpr uint32_t kInGroups = (uint32_t)kInRows * (kHidden / kGroup);     // 5,308,416
 constexpr uint32_t kOutGroups = (uint32_t)kHidden * (kCatCols / kGroup);   // 2,359,296
 
-// (a, b) *= (m, m) as one packed float-pair multiply (round to nearest even).
-__device__ __forceinline__ void mul2(float &a, float &b, float m) {
-  asm("{\n .reg .b64 x, y, d;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %2};\n mul.rn.f32x2 d, x, y;\n"
-      " mov.b64 {%0, %1}, d;\n}"
-      : "+f"(a), "+f"(b)
-      : "f"(m));
-}
 
 // One thread per 16-weight group: the 8 code bytes are decoded through a
 // 256-entry shared table (byte -> the two e2m1 values), scaled by the group's

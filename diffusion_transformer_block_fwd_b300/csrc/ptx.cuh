@@ -327,6 +327,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
 }
 
 // ---------------------------------------------------------------- misc
+// (a, b) *= (m, m) as one packed float-pair multiply (round to nearest even).
+__device__ __forceinline__ void mul2(float &a, float &b, float m) {
+  asm("{\n .reg .b64 x, y, d;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %2};\n mul.rn.f32x2 d, x, y;\n"
+      " mov.b64 {%0, %1}, d;\n}"
+      : "+f"(a), "+f"(b)
+      : "f"(m));
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);

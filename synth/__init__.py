@@ -146,6 +146,10 @@ WORKLOADS = {
     "stack28_nvfp4_1024sq_10ref512_t14848": dict(
         spec=[("txt", 512), ("image", (64, 64))] + [("image_cond", (32, 32))] * 10,
         blocks=28, calls=1, wfmt="nvfp4"),
+    # the 28-block stack at the small block's 96 tokens, bf16 and NVFP4 weights:
+    # the weight stream bounds it (245 MB of bf16 weights per block, 69 MB NVFP4)
+    "stack28_t96": dict(spec=[("txt", 32), ("image", (8, 8))], blocks=28, calls=1, wfmt="bf16"),
+    "stack28_nvfp4_t96": dict(spec=[("txt", 32), ("image", (8, 8))], blocks=28, calls=1, wfmt="nvfp4"),
 }
 
 

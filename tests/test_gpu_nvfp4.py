@@ -6,6 +6,9 @@
 * flux3_dequantize_block: each bf16 weight equals e2m1 * e4m3 (exact) times
   the global scale rounded to float32, then rounded to bf16 (both nearest
   even), from the oracle's codes and scales.
+* Up to 128 tokens the GEMMs expand the codes in shared memory: the block
+  equals a bf16 handle holding the expanded weights bit for bit (also at 129
+  tokens, where the expansion goes through HBM).
 * The block with NVFP4 weights: the oracle runs on the exactly dequantised
   weights (quantised by the oracle itself; no GPU value feeds the oracle);
   criterion max|err| <= 5e-2 RMS(x'), cosine >= 0.998 on x', plus the bf16
@@ -165,6 +168,59 @@ def test_nvfp4_block_matches_oracle(fp4_block, name, spec):
     parts = O.single_block_parts(f64(x), wdq, m, lay.stream_id, lay.pos.astype(np.float64))
     assert_close(f64(y), parts["out"], 5e-2, 0.998, name + " x' (NVFP4 criterion)")
     assert_block_output(f64(y), parts["out"], f64(x), m[lay.stream_id, 6144:], parts["y"], name)
+
+
+@pytest.fixture(scope="module")
+def bf16_twin(fp4_block):
+    """A bf16 handle whose weights are the NVFP4 block's exact expansion."""
+    _, _, raw = fp4_block
+    w = synth.block_weights(2468, 0)
+    dev = {k: dequant_f32_then_bf16(*raw[k]).to(DEV) for k in MATS}
+    dev.update({k: w[k].to(DEV) for k in ("query_norm", "key_norm")})
+    return F3.Flux3Blocks([dev], max_tokens=1024)
+
+
+@pytest.mark.parametrize("name,spec", [("one_token", [("txt", 1)]), ("block_t96", synth.WORKLOADS["block_t96"]["spec"]),
+                                       ("t128", [("txt", 64), ("image", (8, 8))]),
+                                       ("t129_expanded", [("txt", 65), ("image", (8, 8))])])
+def test_nvfp4_block_equals_bf16_block_on_expanded_weights(fp4_block, bf16_twin, name, spec):
+    """Up to 128 tokens the NVFP4 GEMMs read the e2m1 codes and expand them in
+    shared memory; from 129 on the block's weights are expanded in HBM first.
+    Both feed the tensor cores the same bf16 values as a bf16 handle holding
+    the expanded weights, so the block output equals that handle's bit for
+    bit."""
+    blocks, _, _ = fp4_block
+    lay = synth.build_layout(spec)
+    x = synth.activations(44, lay.T, device=DEV)
+    mods = synth.modulation(44, device=DEV)
+    a = _run(blocks, lay, x, mods)
+    b = _run(bf16_twin, lay, x, mods)
+    assert not torch.equal(a, x)
+    assert torch.equal(a, b), f"{name}: max |diff| {float((a - b).abs().max())}"
+
+
+def test_nvfp4_stack_small_t_equals_blocks_one_by_one(fp4_block):
+    """Two NVFP4 blocks at 96 tokens (codes expanded inside the GEMMs, the
+    kernels chained by programmatic dependent launches across the blocks):
+    the stack call equals the blocks called one at a time bit for bit."""
+    _, _, raw = fp4_block
+    w = synth.block_weights(2468, 0)
+    dev = {k: tuple(torch.from_numpy(v).to(DEV) if isinstance(v, np.ndarray)
+                    else torch.tensor([v], dtype=torch.float32, device=DEV) for v in raw[k]) for k in MATS}
+    dev.update({k: w[k].to(DEV) for k in ("query_norm", "key_norm")})
+    blocks = F3.Flux3Blocks([dev, dev], max_tokens=256, wfmt="nvfp4")
+    lay = synth.build_layout(synth.WORKLOADS["block_t96"]["spec"])
+    pos, _ = layout_tensors(lay)
+    x = synth.activations(45, lay.T, device=DEV)
+    mods = synth.modulation(45, device=DEV)
+    a = x.clone()
+    blocks.forward(a, lay.segments, pos, mods)
+    b = x.clone()
+    for i in range(2):
+        blocks.forward(b, lay.segments, pos, mods, first_block=i, n_blocks=1)
+    assert F3.flux3_check_error(_stream()) == 0
+    assert torch.isfinite(a).all() and torch.equal(a, b)
+    blocks.close()
 
 
 def test_nvfp4_block_full_size_sampled_rows(fp4_block):
