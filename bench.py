@@ -744,7 +744,7 @@ def measure_stack(name, steps, warmup, dev, local, world):
             evs[1].record(stream)
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    expand = fp8 or (fp4 and T > 128)   # NVFP4 up to 128 tokens is expanded inside the GEMMs
+    expand = (fp4 or fp8) and T > 128   # up to 128 tokens the codes are expanded inside the GEMMs
     per_call_launches = 1 + nb * (4 + (1 if expand else 0) + merges(T, sms))
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -790,7 +790,7 @@ def run_stack(args, rank, world, local, dev):
     small = m["T"] <= 128          # one-CTA GEMMs, bound by the weight stream
     if small:
         # weight bytes one block streams: bf16 [27648 + 3072 rows]; NVFP4 e2m1 codes + e4m3 scales
-        wbytes = (27648 * 3072 + 3072 * 12288) * (2 if not fp4 else 9 / 16)
+        wbytes = (27648 * 3072 + 3072 * 12288) * (9 / 16 if fp4 else 1 if fp8 else 2)
         gbs = world * wbytes * nb * calls / (step_ms * 1e-3) / 1e9
         hbm = load_peaks()[0]
         roof = {"kernel": "whole stack (weight stream)", "bound": "hbm", "achieved": gbs / world, "peak": hbm,
@@ -806,7 +806,8 @@ def run_stack(args, rank, world, local, dev):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" + ((" (NVFP4 weights expanded inside the GEMMs)" if small else
                                 " (NVFP4 weights dequantised per block)") if fp4 else
-                               " (fp8r weights expanded per block)" if fp8 else ""),
+                               (" (fp8r weights expanded inside the GEMMs)" if small else
+                                " (fp8r weights expanded per block)") if fp8 else ""),
             "data": "synthetic (random-init N(0,0.02) weights" + (", NVFP4-quantised on the device)" if fp4 else
                                                                     ", fp8r-quantised on the device)" if fp8 else ")"),
             "config": {"workload": args.workload, "T": m["T"], "blocks": nb, "calls_per_step": calls,

@@ -258,18 +258,30 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
   // attention's key-range partials may use only memory that is dead while it
   // runs: h when the split region lies over h and qkv (attention reads qkv)
   const size_t attn_part_bytes = split_in_place((size_t)T) ? ws_round((size_t)T * kHidden * 2) : kSplitBytes;
-  // NVFP4 at small T: the GEMMs read the e2m1 codes and expand them in shared
-  // memory (the weight stream bounds them there); otherwise the block's
+  // NVFP4 / fp8r at small T: the GEMMs read the codes and expand them in
+  // shared memory (the weight stream bounds them there); otherwise the block's
   // weights are expanded to bf16 in the workspace first
-  const bool fp4_in_gemm = h->cfg.wfmt == FLUX3_W_NVFP4 && T <= kFp4GemmMaxRows;
+  const bool lowp_in_gemm = fp4 && T <= kLowpGemmMaxRows;
+  const bool nv = h->cfg.wfmt == FLUX3_W_NVFP4;
   for (int b = first; b < first + count; ++b) {
     CUtensorMap tmCin, tmCout;
-    if (fp4_in_gemm && (!make_tmap_u8(&tmCin, h->fp4[b].in_codes, kInRows, kHidden / 2, kBK / 2, 256) ||
-                        !make_tmap_u8(&tmCout, h->fp4[b].out_codes, kHidden, kCatCols / 2, kBK / 2, 256)))
-      return FLUX3_ERR_CUDA;
-    if (h->cfg.wfmt == FLUX3_W_NVFP4 && !fp4_in_gemm)
+    const void *in_scales = nullptr, *out_scales = nullptr;
+    const float *globals = nullptr;
+    if (lowp_in_gemm) {
+      const uint8_t *in_codes = nv ? h->fp4[b].in_codes : h->fp8[b].in_codes;
+      const uint8_t *out_codes = nv ? h->fp4[b].out_codes : h->fp8[b].out_codes;
+      const uint32_t cols = nv ? kBK / 2 : kBK;   // code bytes per row of a k-block
+      if (!make_tmap_u8(&tmCin, in_codes, kInRows, (uint64_t)kHidden * cols / kBK, cols, 256) ||
+          !make_tmap_u8(&tmCout, out_codes, kHidden, (uint64_t)kCatCols * cols / kBK, cols, 256))
+        return FLUX3_ERR_CUDA;
+      in_scales = nv ? static_cast<const void *>(h->fp4[b].in_scales) : static_cast<const void *>(h->fp8[b].in_scales);
+      out_scales = nv ? static_cast<const void *>(h->fp4[b].out_scales) : static_cast<const void *>(h->fp8[b].out_scales);
+      globals = nv ? h->fp4[b].globals : nullptr;
+    } else if (nv) {
       F3_CUDA(launch_dequantize_block(h->fp4[b], ws.w_in, ws.w_out, s, true));
-    if (h->cfg.wfmt == FLUX3_W_FP8R) F3_CUDA(launch_dequantize_fp8r_block(h->fp8[b], ws.w_in, ws.w_out, s, true));
+    } else if (h->cfg.wfmt == FLUX3_W_FP8R) {
+      F3_CUDA(launch_dequantize_fp8r_block(h->fp8[b], ws.w_in, ws.w_out, s, true));
+    }
     F3_CUDA(launch_ln_modulate(x, T, ws.sid, mod, h->cfg.eps_ln, ws.h, s, true));
     EpiParams ep{};
     ep.qkv = ws.qkv;
@@ -279,10 +291,10 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     ep.qnorm = block_norms(h, b);
     ep.knorm = block_norms(h, b) + kHeadDim;
     ep.eps_rms = h->cfg.eps_rms;
-    if (fp4_in_gemm) {
-      ep.w_scales = h->fp4[b].in_scales;
-      ep.w_globals = h->fp4[b].globals;
-      F3_CUDA(launch_gemm_fp4(EPI_IN_PROJ, tmH, tmCin, T, kInRows, kHidden, ep, s, true));
+    if (lowp_in_gemm) {
+      ep.w_scales = in_scales;
+      ep.w_globals = globals;
+      F3_CUDA(launch_gemm_lowp(EPI_IN_PROJ, h->cfg.wfmt, tmH, tmCin, T, kInRows, kHidden, ep, s, true));
     } else {
       F3_CUDA(launch_gemm(EPI_IN_PROJ, tmH, fp4 ? tmWin : h->tm_in[b], T, kInRows, kHidden, ep, s, true));
     }
@@ -297,10 +309,10 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     eo.mod = mod;
     eo.part = ws.part;
     eo.part_bytes = kSplitBytes;
-    if (fp4_in_gemm) {
-      eo.w_scales = h->fp4[b].out_scales;
-      eo.w_globals = h->fp4[b].globals;
-      F3_CUDA(launch_gemm_fp4(EPI_OUT_RESIDUAL, tmCat, tmCout, T, kHidden, kCatCols, eo, s, true));
+    if (lowp_in_gemm) {
+      eo.w_scales = out_scales;
+      eo.w_globals = globals;
+      F3_CUDA(launch_gemm_lowp(EPI_OUT_RESIDUAL, h->cfg.wfmt, tmCat, tmCout, T, kHidden, kCatCols, eo, s, true));
     } else {
       F3_CUDA(launch_gemm(EPI_OUT_RESIDUAL, tmCat, fp4 ? tmWout : h->tm_out[b], T, kHidden, kCatCols, eo, s, true));
     }

@@ -50,10 +50,11 @@ struct EpiParams {
   // tiles (tile rows x 256 per split unit); null / too small: no split
   float *part;
   size_t part_bytes;
-  // NVFP4 weights expanded inside the GEMM (launch_gemm_fp4): the e4m3 block
-  // scales [N, K / 16] (4-byte aligned) and the block's float32 tensor scales
-  // (q, k, v, mlp_in, attn_out, mlp_out)
-  const uint8_t *w_scales;
+  // Low-precision weights expanded inside the GEMM (launch_gemm_lowp): NVFP4
+  // e4m3 block scales [N, K / 16] (4-byte aligned) and the block's float32
+  // tensor scales (q, k, v, mlp_in, attn_out, mlp_out); fp8r float32 row scales
+  // ([N], or [N][2] (attn_out, mlp_out) for the out-projection), no w_globals
+  const void *w_scales;
   const float *w_globals;
 };
 
@@ -121,14 +122,15 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K,
                         const EpiParams &ep, cudaStream_t s, bool pdl = false);
 
-// The block GEMMs (EPI_IN_PROJ, EPI_OUT_RESIDUAL) over NVFP4 weights for M <=
-// kFp4GemmMaxRows (one-CTA tiles): tmCodes maps the e2m1 code bytes [N, K / 2]
-// (make_tmap_u8 with 32-byte x 256-row boxes); ep.w_scales / ep.w_globals
-// hold the block scales and tensor scales.  The weights are expanded to bf16
-// in shared memory, never in HBM.
-constexpr int kFp4GemmMaxRows = 128;
-cudaError_t launch_gemm_fp4(int mode, const CUtensorMap &tmA, const CUtensorMap &tmCodes, int M, int N, int K,
-                            const EpiParams &ep, cudaStream_t s, bool pdl = false);
+// The block GEMMs (EPI_IN_PROJ, EPI_OUT_RESIDUAL) over NVFP4 or fp8r weights
+// (fmt: FLUX3_W_NVFP4 / FLUX3_W_FP8R) for M <= kLowpGemmMaxRows (one-CTA
+// tiles): tmCodes maps the code bytes (make_tmap_u8 with 256-row boxes of 32
+// bytes for the e2m1 codes [N, K / 2], 64 bytes for the e4m3 codes [N, K]);
+// ep.w_scales / ep.w_globals hold the scales.  The weights are expanded to
+// bf16 in shared memory, never in HBM.
+constexpr int kLowpGemmMaxRows = 128;
+cudaError_t launch_gemm_lowp(int mode, int fmt, const CUtensorMap &tmA, const CUtensorMap &tmCodes, int M, int N,
+                             int K, const EpiParams &ep, cudaStream_t s, bool pdl = false);
 
 cudaError_t launch_stream_ids(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, cudaStream_t s);
 cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_tab, float *sin_tab,

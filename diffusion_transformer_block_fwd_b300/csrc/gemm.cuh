@@ -70,32 +70,39 @@ struct SharedCtl {
   int abort;
 };
 
+// Weight formats of the B operand: bf16 through TMA, or codes expanded in
+// shared memory by the epilogue warps (one-CTA form only).
+enum : int { kWBf16 = 0, kWNvfp4 = 1, kWFp8r = 2 };
+
 // The forms of the kernel.  Pair (kPair): a cluster of two CTAs on one TPC
 // computes a 256 x 256 tile with cta_group::2 MMAs; each CTA stages 128 A
 // rows and 128 B rows per k-block.  Single: one CTA computes a 128 x 256 tile
 // with cta_group::1 MMAs and stages 128 A rows and all 256 B rows.  The
 // single form serves M <= 128, where a pair tile would be at most half rows.
-// kFp4 (single form only): B arrives as NVFP4 e2m1 codes (a quarter of the
-// bf16 bytes) in a ring of its own, and the epilogue warps, idle while the
-// tile accumulates, expand each k-block into the bf16 B stage the MMA reads.
-// The A and B stages then form separate rings: A (from L2) five deep, the
-// expanded B two deep (the expansion works out of shared memory, so one stage
-// in hand while the MMAs read the other is enough).
-template <bool kPair, bool kFp4 = false>
+// Low-precision weights (single form only): B arrives as NVFP4 e2m1 codes (a
+// quarter of the bf16 bytes) or fp8r e4m3 codes (half) in a ring of its own,
+// and the epilogue warps, idle while the tile accumulates, expand each k-block
+// into the bf16 B stage the MMA reads.  The A and B stages then form separate
+// rings: A (from L2) four or five deep, the expanded B two deep (the expansion
+// works out of shared memory, so one stage in hand while the MMAs read the
+// other is enough).
+template <bool kPair, int kWFmt = kWBf16>
 struct GemmCfg {
-  static_assert(!(kPair && kFp4), "NVFP4 weights are expanded in the one-CTA form only");
-  static constexpr int kStages = kPair ? 6 : (kFp4 ? 5 : 4);   // A stages (and B stages without kFp4)
-  static constexpr int kBStages = kFp4 ? 2 : kStages;
-  static constexpr int kCodeStages = kFp4 ? 5 : 1;
+  static constexpr bool kConv = kWFmt != kWBf16;
+  static_assert(!(kPair && kConv), "low-precision weights are expanded in the one-CTA form only");
+  static constexpr int kStages = kPair ? 6 : (kWFmt == kWNvfp4 ? 5 : 4);   // A stages (and B stages for bf16)
+  static constexpr int kBStages = kConv ? 2 : kStages;
+  static constexpr int kCodeStages = kWFmt == kWNvfp4 ? 5 : (kWFmt == kWFp8r ? 4 : 1);
+  static constexpr int kCodeCols = kWFmt == kWNvfp4 ? kBK / 2 : kBK;        // code bytes per row of a k-block
   static constexpr int kTileM = kPair ? 256 : 128;                     // output rows per tile
   static constexpr uint32_t kABytes = 128 * kBK * 2;                   // 16 KB: 128 A rows per CTA
   static constexpr uint32_t kBBytes = (kPair ? 128 : 256) * kBK * 2;   // B rows per CTA
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kCodeBytes = kFp4 ? 256 * kBK / 2 : 0;     // 8 KB: 256 rows x 64 e2m1 codes
-  // bytes completing on one stage barrier (with NVFP4 weights: A only)
-  static constexpr uint32_t kTxBytes = kFp4 ? kABytes : (kPair ? 2 : 1) * kStageBytes;
+  static constexpr uint32_t kCodeBytes = kConv ? 256 * kCodeCols : 0;   // 8 KB (e2m1) or 16 KB (e4m3)
+  // bytes completing on one stage barrier (with codes: A only)
+  static constexpr uint32_t kTxBytes = kConv ? kABytes : (kPair ? 2 : 1) * kStageBytes;
   static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kABytes + kBStages * kBBytes +
-                                       (kFp4 ? kCodeStages * kCodeBytes : 0) + kEpiWarps * kBoxBytes +
+                                       (kConv ? kCodeStages * kCodeBytes : 0) + kEpiWarps * kBoxBytes +
                                        sizeof(SharedCtl<kStages, kCodeStages, kBStages>);
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
@@ -139,6 +146,35 @@ __device__ __forceinline__ void expand_fp4_row(const uint8_t *codes, uint32_t sc
       o[b] = pack_bf16x2(lo, hi);
     }
     *reinterpret_cast<uint4 *>(row + ((q ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// One B row of a k-block from fp8r: 64 e4m3 codes (64 bytes at `codes`) and
+// the row's float32 scale s.  Each weight is e4m3 (exact in f16, and so in
+// float32) times s, rounded to float32, then to bf16 -- the expansion kernel's
+// arithmetic.  Same swizzled layout as expand_fp4_row.
+__device__ __forceinline__ void expand_fp8_row(const uint8_t *codes, float s, uint8_t *b_stage, int r) {
+  uint8_t *row = b_stage + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {   // 16 codes: chunks 2h, 2h+1
+    const uint4 c = *reinterpret_cast<const uint4 *>(codes + 16 * h);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t p01, p23;   // f16x2 of codes (0, 1) and (2, 3) of word k
+      asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+          : "=r"(p01), "=r"(p23)
+          : "r"(w[k]));
+      const __half2 v01 = *reinterpret_cast<const __half2 *>(&p01), v23 = *reinterpret_cast<const __half2 *>(&p23);
+      float a = __low2float(v01), b = __high2float(v01), c2 = __low2float(v23), d = __high2float(v23);
+      mul2(a, b, s);
+      mul2(c2, d, s);
+      o[2 * k] = pack_bf16x2(a, b);
+      o[2 * k + 1] = pack_bf16x2(c2, d);
+    }
+    *reinterpret_cast<uint4 *>(row + (((2 * h) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(row + (((2 * h + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -412,14 +448,18 @@ __device__ __forceinline__ void store_partial_half(uint32_t taddr, int slot, int
   }
 }
 
-// tmB: the bf16 weight, or with kFp4 the e2m1 code bytes of the weight
-// ([N, K / 2] uint8, boxes of 32 bytes x 256 rows; ep.w_scales and
-// ep.w_globals hold the block scales and the tensors' float32 scales).
-template <int EPI, bool kPair, bool kFp4>
+// tmB: the bf16 weight, or the code bytes of a low-precision weight: NVFP4
+// e2m1 codes [N, K / 2] (boxes of 32 bytes x 256 rows; ep.w_scales holds the
+// e4m3 block scales [N, K / 16], ep.w_globals the tensors' float32 scales) or
+// fp8r e4m3 codes [N, K] (boxes of 64 bytes x 256 rows; ep.w_scales holds the
+// float32 row scales: [N] for the in-projection, [N][2] (attn_out, mlp_out)
+// for the out-projection).
+template <int EPI, bool kPair, int kWFmt>
 __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmO0,
                                           const CUtensorMap &tmO1, int M, int N, int K, int n_full, int splits,
                                           const EpiParams &ep) {
-  using C = GemmCfg<kPair, kFp4>;
+  using C = GemmCfg<kPair, kWFmt>;
+  constexpr bool kConv = C::kConv;   // B from codes expanded by the epilogue warps
   constexpr int kStages = C::kStages;
   constexpr int kBStages = C::kBStages;
   constexpr int kCodeStages = C::kCodeStages;
@@ -429,7 +469,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
   uint8_t *smA = smem;
   uint8_t *smB = smem + kStages * C::kABytes;
   uint8_t *smC = smB + kBStages * C::kBBytes;                        // NVFP4 code ring
-  uint8_t *sOut = smC + (kFp4 ? kCodeStages * C::kCodeBytes : 0);   // [epilogue warp] 4 KB output box
+  uint8_t *sOut = smC + (kConv ? kCodeStages * C::kCodeBytes : 0);   // [epilogue warp] 4 KB output box
   auto *ctl = reinterpret_cast<SharedCtl<kStages, kCodeStages, kBStages> *>(sOut + kEpiWarps * kBoxBytes);
 
   const int warp = threadIdx.x / 32;
@@ -459,7 +499,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
     }
     mbar_init(&ctl->drain, 1);
     for (int w = 0; w < kEpiWarps; ++w) mbar_init(&ctl->xbar[w], 1);
-    if constexpr (kFp4) {
+    if constexpr (kConv) {
       for (int s = 0; s < kCodeStages; ++s) {
         mbar_init(&ctl->cfull[s], 1);
         mbar_init(&ctl->cempty[s], kEpiWarps * 32);
@@ -502,14 +542,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
   // before it, the out-projection only after the in-projection has.  The A
   // halves, which the previous kernel may write, follow after the wait.
   int n_pre = 0;
-  if constexpr (kFp4) {
+  if constexpr (kConv) {
     // the codes of the first k-blocks (lane 1 runs the code ring)
     if (warp == 0 && lane == 1 && worker < num_units) {
       const Unit un = unit_of(worker, n_full, splits, num_m, num_n, n_fast, num_kb);
       n_pre = un.kb1 - un.kb0 < kCodeStages ? un.kb1 - un.kb0 : kCodeStages;
       for (int i = 0; i < n_pre; ++i) {
         mbar_arrive_expect_tx(&ctl->cfull[i], C::kCodeBytes);
-        tma_load_2d(smC + i * C::kCodeBytes, &tmB, &ctl->cfull[i], (un.kb0 + i) * (kBK / 2), un.n_blk * kBN);
+        tma_load_2d(smC + i * C::kCodeBytes, &tmB, &ctl->cfull[i], (un.kb0 + i) * C::kCodeCols, un.n_blk * kBN);
       }
     }
   } else if constexpr (!kPair) {
@@ -543,7 +583,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
         const int a_row = un.m_blk * kTileM + (int)rank * 128;
         const int b_row = un.n_blk * kBN + (int)rank * 128;
         for (int kb = un.kb0; kb < un.kb1; ++kb, ++it) {
-          const bool pre = !kFp4 && it < n_pre;   // a fresh stage: no wait for it to drain
+          const bool pre = !kConv && it < n_pre;   // a fresh stage: no wait for it to drain
           if (!pre && !mbar_wait(&ctl->empty[stage], phase ^ 1, abort)) {
             ok = false;
             break;
@@ -555,7 +595,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
             if (leader) mbar_arrive_expect_tx(&ctl->full[stage], C::kTxBytes);
             tma_load_2d_pair(a_dst, &tmA, full_leader, kb * kBK, a_row);
             tma_load_2d_pair(b_dst, &tmB, full_leader, kb * kBK, b_row);
-          } else if constexpr (kFp4) {
+          } else if constexpr (kConv) {
             mbar_arrive_expect_tx(&ctl->full[stage], C::kTxBytes);   // B is written by the converting warps
             tma_load_2d(a_dst, &tmA, &ctl->full[stage], kb * kBK, a_row);
           } else {
@@ -577,8 +617,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
         for (int s = 0; s < kStages; ++s)
           if (last_phase[s] >= 0) drain_wait(&ctl->full[s], (uint32_t)last_phase[s]);
       }
-    } else if (kFp4 && lane == 1) {
-      // ---------------- NVFP4 code ring: each k-block's 256 x 32 code bytes
+    } else if (kConv && lane == 1) {
+      // ---------------- code ring: each k-block's 256 rows of code bytes
       int last_phase[kCodeStages];
 #pragma unroll
       for (int s = 0; s < kCodeStages; ++s) last_phase[s] = -1;
@@ -594,7 +634,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
               break;
             }
             mbar_arrive_expect_tx(&ctl->cfull[cs], C::kCodeBytes);
-            tma_load_2d(smC + cs * C::kCodeBytes, &tmB, &ctl->cfull[cs], kb * (kBK / 2), un.n_blk * kBN);
+            tma_load_2d(smC + cs * C::kCodeBytes, &tmB, &ctl->cfull[cs], kb * C::kCodeCols, un.n_blk * kBN);
           }
           last_phase[cs] = (int)cphase;
           if (++cs == kCodeStages) {
@@ -616,7 +656,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
       const SmemDesc da = smem_desc_split(smem_addr(smA), 16, 1024, kSwizzle128B);
       const SmemDesc db = smem_desc_split(smem_addr(smB), 16, 1024, kSwizzle128B);
       uint32_t stage = 0, phase = 0;
-      uint32_t bstage = 0, bphase = 0;   // the B ring (its own with kFp4, else the same as the A ring)
+      uint32_t bstage = 0, bphase = 0;   // the B ring (its own with codes, else the same as the A ring)
       int local = 0;
       bool ok = true;
       for (int u = worker; u < num_units && ok; u += num_workers, ++local) {
@@ -628,12 +668,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
         const uint32_t d_tmem = tmem_base + acc * kBN;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           if (!mbar_wait(&ctl->full[stage], phase, abort) ||
-              (kFp4 && !mbar_wait(&ctl->bready[bstage], bphase, abort))) {
+              (kConv && !mbar_wait(&ctl->bready[bstage], bphase, abort))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t boff = (kFp4 ? bstage : stage) * C::kBBytes;
+          const uint32_t boff = (kConv ? bstage : stage) * C::kBBytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint32_t accumulate = (kb != un.kb0 || k != 0) ? 1u : 0u;
@@ -646,7 +686,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
             mma_commit_pair_mc(&ctl->empty[stage], 0x3);
           } else {
             mma_commit(&ctl->empty[stage]);
-            if constexpr (kFp4) mma_commit(&ctl->bempty[bstage]);
+            if constexpr (kConv) mma_commit(&ctl->bempty[bstage]);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -704,29 +744,46 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
           load_x_box(bw, &tmO0, xbar, un.n_blk * kBN + half * 128, un.m_blk * kTileM + row_in_tile - lane);
         }
       }
-      if constexpr (kFp4) {
-        static_assert(EPI == EPI_IN_PROJ || EPI == EPI_OUT_RESIDUAL, "NVFP4 weights of the block GEMMs only");
-        const uint32_t *srow = reinterpret_cast<const uint32_t *>(ep.w_scales + (size_t)(un.n_blk * kBN + conv_r) * (K / 16));
-        // the tensor's float32 scale: by row block (q, k, v, mlp_in) for the
-        // in-projection, by input column (attn_out, mlp_out) for the out-projection
-        const int gi_q = un.n_blk / (kHidden / kBN);
-        const float g_lo = __ldg(ep.w_globals + (EPI == EPI_IN_PROJ ? (gi_q < 3 ? gi_q : 3) : 4));
-        const float g_hi = EPI == EPI_IN_PROJ ? g_lo : __ldg(ep.w_globals + 5);
-        // the row's four block scales of a k-block are one 32-bit word; the
-        // words go out two k-blocks ahead of their use
-        uint32_t s_cur = un.kb0 < un.kb1 ? __ldg(srow + un.kb0) : 0u;
-        uint32_t s_nxt = un.kb0 + 1 < un.kb1 ? __ldg(srow + un.kb0 + 1) : 0u;
+      if constexpr (kConv) {
+        static_assert(EPI == EPI_IN_PROJ || EPI == EPI_OUT_RESIDUAL, "low-precision weights of the block GEMMs only");
+        const int brow = un.n_blk * kBN + conv_r;   // the weight row this thread expands
+        // NVFP4: the tensor's float32 scale, by row block (q, k, v, mlp_in) for
+        // the in-projection, by input column (attn_out, mlp_out) for the
+        // out-projection; fp8r: the row's scale, for the out-projection one per
+        // input half (attn_out, mlp_out)
+        float g_lo, g_hi;
+        const uint32_t *srow = nullptr;
+        uint32_t s_cur = 0u, s_nxt = 0u;
+        if constexpr (kWFmt == kWNvfp4) {
+          srow = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(ep.w_scales) + (size_t)brow * (K / 16));
+          const int gi_q = un.n_blk / (kHidden / kBN);
+          g_lo = __ldg(ep.w_globals + (EPI == EPI_IN_PROJ ? (gi_q < 3 ? gi_q : 3) : 4));
+          g_hi = EPI == EPI_IN_PROJ ? g_lo : __ldg(ep.w_globals + 5);
+          // the row's four block scales of a k-block are one 32-bit word; the
+          // words go out two k-blocks ahead of their use
+          s_cur = un.kb0 < un.kb1 ? __ldg(srow + un.kb0) : 0u;
+          s_nxt = un.kb0 + 1 < un.kb1 ? __ldg(srow + un.kb0 + 1) : 0u;
+        } else {
+          const float *rs = static_cast<const float *>(ep.w_scales);
+          g_lo = __ldg(rs + (EPI == EPI_IN_PROJ ? (size_t)brow : 2 * (size_t)brow));
+          g_hi = EPI == EPI_IN_PROJ ? g_lo : __ldg(rs + 2 * (size_t)brow + 1);
+        }
         bool conv_ok = true;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           const float g = (EPI == EPI_OUT_RESIDUAL && kb * kBK >= kHidden) ? g_hi : g_lo;
           const uint32_t s4 = s_cur;
-          s_cur = s_nxt;
-          s_nxt = kb + 2 < un.kb1 ? __ldg(srow + kb + 2) : 0u;
+          if constexpr (kWFmt == kWNvfp4) {
+            s_cur = s_nxt;
+            s_nxt = kb + 2 < un.kb1 ? __ldg(srow + kb + 2) : 0u;
+          }
           if (!mbar_wait(&ctl->cfull[cs], cphase, abort) || !mbar_wait(&ctl->bempty[bstage], bphase ^ 1, abort)) {
             conv_ok = false;
             break;
           }
-          expand_fp4_row(smC + cs * C::kCodeBytes + conv_r * (kBK / 2), s4, g, smB + bstage * C::kBBytes, conv_r);
+          if constexpr (kWFmt == kWNvfp4)
+            expand_fp4_row(smC + cs * C::kCodeBytes + conv_r * C::kCodeCols, s4, g, smB + bstage * C::kBBytes, conv_r);
+          else
+            expand_fp8_row(smC + cs * C::kCodeBytes + conv_r * C::kCodeCols, g, smB + bstage * C::kBBytes, conv_r);
           fence_proxy_async_smem();       // the MMA reads the row through the async proxy
           mbar_arrive(&ctl->bready[bstage]);
           mbar_arrive(&ctl->cempty[cs]);
@@ -784,7 +841,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
                 int K, int n_full, int splits, EpiParams ep) {
-  gemm_body<EPI, true, false>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
+  gemm_body<EPI, true, kWBf16>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
 }
 
 template <int EPI>
@@ -792,16 +849,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm1_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
                  int K, int n_full, int splits, EpiParams ep) {
-  gemm_body<EPI, false, false>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
+  gemm_body<EPI, false, kWBf16>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
 }
 
-// The one-CTA form over NVFP4 weights (tmB: the e2m1 code bytes).
+// The one-CTA form over NVFP4 / fp8r weights (tmB: the code bytes).
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm1_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
                      int K, int n_full, int splits, EpiParams ep) {
-  gemm_body<EPI, false, true>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
+  gemm_body<EPI, false, kWNvfp4>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
+}
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm1_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1, int M, int N,
+                     int K, int n_full, int splits, EpiParams ep) {
+  gemm_body<EPI, false, kWFp8r>(tmA, tmB, tmO0, tmO1, M, N, K, n_full, splits, ep);
 }
 
 // Sums the split units of each trailing tile in a fixed order (unit 0 first)
@@ -877,13 +941,15 @@ void split_plan(int EPI, int M, int N, int K, int tile_m, int workers, size_t pa
   }
 }
 
-template <int EPI, bool kPair, bool kFp4 = false>
+template <int EPI, bool kPair, int kWFmt = kWBf16>
 cudaError_t launch_form(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, int N, int K, const EpiParams &ep,
                         cudaStream_t s, bool pdl) {
-  using C = GemmCfg<kPair, kFp4>;
+  using C = GemmCfg<kPair, kWFmt>;
   auto kernel = [] {
-    if constexpr (kFp4)
+    if constexpr (kWFmt == kWNvfp4)
       return gemm1_fp4_kernel<EPI>;
+    else if constexpr (kWFmt == kWFp8r)
+      return gemm1_fp8_kernel<EPI>;
     else
       return kPair ? gemm_kernel<EPI> : gemm1_kernel<EPI>;
   }();
@@ -927,15 +993,16 @@ cudaError_t launch_mode(const CUtensorMap &tmA, const CUtensorMap &tmB, int M, i
   return launch_form<EPI, true>(tmA, tmB, M, N, K, ep, s, pdl);
 }
 
-// Wraps the EPI_IN_PROJ / EPI_OUT_RESIDUAL NVFP4 forms (the only EPIs the
-// expansion in the epilogue warps serves) for the mode switch below.
+// Wraps the EPI_IN_PROJ / EPI_OUT_RESIDUAL low-precision forms (the only
+// EPIs the expansion in the epilogue warps serves) for the switch below.
 template <int EPI>
-cudaError_t launch_fp4_mode(const CUtensorMap &tmA, const CUtensorMap &tmCodes, int M, int N, int K,
-                            const EpiParams &ep, cudaStream_t s, bool pdl) {
-  if constexpr (EPI == EPI_IN_PROJ || EPI == EPI_OUT_RESIDUAL)
-    return launch_form<EPI, false, true>(tmA, tmCodes, M, N, K, ep, s, pdl);
-  else
-    return cudaErrorInvalidValue;
+cudaError_t launch_lowp_mode(int fmt, const CUtensorMap &tmA, const CUtensorMap &tmCodes, int M, int N, int K,
+                             const EpiParams &ep, cudaStream_t s, bool pdl) {
+  if constexpr (EPI == EPI_IN_PROJ || EPI == EPI_OUT_RESIDUAL) {
+    if (fmt == FLUX3_W_NVFP4) return launch_form<EPI, false, kWNvfp4>(tmA, tmCodes, M, N, K, ep, s, pdl);
+    if (fmt == FLUX3_W_FP8R) return launch_form<EPI, false, kWFp8r>(tmA, tmCodes, M, N, K, ep, s, pdl);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace gemm_detail
@@ -952,13 +1019,14 @@ cudaError_t launch_gemm(int mode, const CUtensorMap &tmA, const CUtensorMap &tmB
   }
 }
 
-cudaError_t launch_gemm_fp4(int mode, const CUtensorMap &tmA, const CUtensorMap &tmCodes, int M, int N, int K,
-                            const EpiParams &ep, cudaStream_t s, bool pdl) {
+cudaError_t launch_gemm_lowp(int mode, int fmt, const CUtensorMap &tmA, const CUtensorMap &tmCodes, int M, int N,
+                             int K, const EpiParams &ep, cudaStream_t s, bool pdl) {
   using namespace gemm_detail;
-  if (M < 1 || M > kFp4GemmMaxRows || !ep.w_scales || !ep.w_globals) return cudaErrorInvalidValue;
+  if (M < 1 || M > kLowpGemmMaxRows || !ep.w_scales || (fmt == FLUX3_W_NVFP4 && !ep.w_globals))
+    return cudaErrorInvalidValue;
   switch (mode) {
-    case EPI_IN_PROJ: return launch_fp4_mode<EPI_IN_PROJ>(tmA, tmCodes, M, N, K, ep, s, pdl);
-    case EPI_OUT_RESIDUAL: return launch_fp4_mode<EPI_OUT_RESIDUAL>(tmA, tmCodes, M, N, K, ep, s, pdl);
+    case EPI_IN_PROJ: return launch_lowp_mode<EPI_IN_PROJ>(fmt, tmA, tmCodes, M, N, K, ep, s, pdl);
+    case EPI_OUT_RESIDUAL: return launch_lowp_mode<EPI_OUT_RESIDUAL>(fmt, tmA, tmCodes, M, N, K, ep, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

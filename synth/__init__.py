@@ -150,6 +150,7 @@ WORKLOADS = {
     # the weight stream bounds it (245 MB of bf16 weights per block, 69 MB NVFP4)
     "stack28_t96": dict(spec=[("txt", 32), ("image", (8, 8))], blocks=28, calls=1, wfmt="bf16"),
     "stack28_nvfp4_t96": dict(spec=[("txt", 32), ("image", (8, 8))], blocks=28, calls=1, wfmt="nvfp4"),
+    "stack28_fp8r_t96": dict(spec=[("txt", 32), ("image", (8, 8))], blocks=28, calls=1, wfmt="fp8r"),
     # two NVFP4 blocks at 96 tokens: a small case of the above for kernel captures
     "stack2_nvfp4_t96": dict(spec=[("txt", 32), ("image", (8, 8))], blocks=2, calls=1, wfmt="nvfp4"),
 }

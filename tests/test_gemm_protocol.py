@@ -14,9 +14,9 @@ epilogue has drained its previous tile, and that the epilogue reads complete
 sums.  Each stage is filled by two copies (the B and the A operand).  The
 one-CTA form runs a 4-stage ring and issues the B copies of its first stages
 before it may read A (before the programmatic-dependent wait); the loop then
-adds only their A copies.  With NVFP4 weights the one-CTA form keeps three
-rings: A (five stages), the e2m1 codes (five, fed by a second producer
-thread) and the expanded B stages (two); the epilogue warps expand each
+adds only their A copies.  With NVFP4 (fp8r) weights the one-CTA form keeps
+three rings: A (five (four) stages), the codes (five (four), fed by a second
+producer thread) and the expanded B stages (two); the epilogue warps expand each
 k-block's codes into a B stage (after the MMAs have released it) before they
 drain the unit's accumulator.  Planted mistakes (a stage released before its
 MMAs, a wrong accumulator phase, more early stages than the ring holds, a B
@@ -31,10 +31,10 @@ from test_attention_protocol import Barrier
 
 
 class Gemm:
-    def __init__(self, tiles, num_kb, seed, plant=None, stages=6, pre=False, fp4=False):
+    def __init__(self, tiles, num_kb, seed, plant=None, stages=6, pre=False, fp4=False, cstages=5):
         self.tiles, self.num_kb, self.plant, self.stages, self.pre = tiles, num_kb, plant, stages, pre
-        self.fp4 = fp4
-        self.bstages, self.cstages = (2, 5) if fp4 else (stages, 0)
+        self.fp4 = fp4                                   # codes expanded by the epilogue (NVFP4 or fp8r)
+        self.bstages, self.cstages = (2, cstages) if fp4 else (stages, 0)
         self.cfull = [Barrier(f"cfull{s}", 1) for s in range(self.cstages)]
         self.cempty = [Barrier(f"cempty{s}", 1) for s in range(self.cstages)]
         self.bready = [Barrier(f"bready{s}", 1) for s in range(self.bstages)]
@@ -229,7 +229,7 @@ class Gemm:
 
 
 FORMS = {"pair": dict(stages=6, pre=False), "one_cta": dict(stages=4, pre=True),
-         "one_cta_nvfp4": dict(stages=5, fp4=True)}
+         "one_cta_nvfp4": dict(stages=5, fp4=True), "one_cta_fp8r": dict(stages=4, fp4=True, cstages=4)}
 
 
 @pytest.mark.parametrize("form", sorted(FORMS))
@@ -242,7 +242,7 @@ def test_protocol_finishes_and_reads_the_right_stages(form, n_tiles, num_kb):
 @pytest.mark.parametrize("form,plant", [("pair", "stage_released_early"), ("pair", "wrong_acc_phase"),
                                         ("one_cta", "stage_released_early"), ("one_cta", "pre_overrun"),
                                         ("one_cta_nvfp4", "stage_released_early"),
-                                        ("one_cta_nvfp4", "b_rewritten_early")])
+                                        ("one_cta_nvfp4", "b_rewritten_early"), ("one_cta_fp8r", "b_rewritten_early")])
 def test_planted_mistakes_are_caught(form, plant):
     caught = 0
     for n_tiles, num_kb in ((3, 4), (4, 7), (2, 9)):

@@ -7,6 +7,9 @@
 * The expansion of a packed block to bf16: bit-exact against the oracle's
   codes and scales expanded the same way (e4m3 * s rounded to float32, then to
   bf16).
+* Up to 128 tokens the GEMMs expand the codes in shared memory: the block
+  equals a bf16 handle holding the expanded weights bit for bit (also at 129
+  tokens, where the expansion goes through HBM).
 * The block with fp8r weights: the oracle runs on the exactly dequantised
   weights (quantised by the oracle itself; no GPU value feeds the oracle);
   the block criterion of the bf16 path on x' and on the update (the GPU's only
@@ -149,6 +152,57 @@ def test_fp8r_block_against_oracle(fp8_block, name, spec):
     m = f64(mods)
     parts = O.single_block_parts(f64(x), wdq, m, lay.stream_id, lay.pos.astype(np.float64))
     assert_block_output(f64(y), parts["out"], f64(x), m[lay.stream_id, 6144:], parts["y"], name)
+
+
+@pytest.fixture(scope="module")
+def bf16_twin(fp8_block):
+    """A bf16 handle whose weights are the fp8r block's exact expansion."""
+    _, _, raw = fp8_block
+    w = synth.block_weights(1357, 0)
+    dev = {k: expand_f32_then_bf16(*raw[k]).to(DEV) for k in MATS}
+    dev.update({k: w[k].to(DEV) for k in ("query_norm", "key_norm")})
+    return F3.Flux3Blocks([dev], max_tokens=1024)
+
+
+@pytest.mark.parametrize("name,spec", [("one_token", [("txt", 1)]), ("block_t96", synth.WORKLOADS["block_t96"]["spec"]),
+                                       ("t128", [("txt", 64), ("image", (8, 8))]),
+                                       ("t129_expanded", [("txt", 65), ("image", (8, 8))])])
+def test_fp8r_block_equals_bf16_block_on_expanded_weights(fp8_block, bf16_twin, name, spec):
+    """Up to 128 tokens the fp8r GEMMs read the e4m3 codes and expand them in
+    shared memory; from 129 on the block's weights are expanded in HBM first.
+    Both feed the tensor cores the same bf16 values as a bf16 handle holding
+    the expanded weights, so the block output equals that handle's bit for
+    bit."""
+    blocks, _, _ = fp8_block
+    lay = synth.build_layout(spec)
+    x = synth.activations(63, lay.T, device=DEV)
+    mods = synth.modulation(63, device=DEV)
+    a = _run(blocks, lay, x, mods)
+    b = _run(bf16_twin, lay, x, mods)
+    assert not torch.equal(a, x)
+    assert torch.equal(a, b), f"{name}: max |diff| {float((a - b).abs().max())}"
+
+
+def test_fp8r_stack_small_t_equals_blocks_one_by_one(fp8_block):
+    """Two fp8r blocks at 96 tokens (codes expanded inside the GEMMs): the
+    stack call equals the blocks called one at a time bit for bit."""
+    _, _, raw = fp8_block
+    w = synth.block_weights(1357, 0)
+    dev = {k: (torch.from_numpy(raw[k][0]).to(DEV), torch.from_numpy(raw[k][1]).to(DEV)) for k in MATS}
+    dev.update({k: w[k].to(DEV) for k in ("query_norm", "key_norm")})
+    blocks = F3.Flux3Blocks([dev, dev], max_tokens=256, wfmt="fp8r")
+    lay = synth.build_layout(synth.WORKLOADS["block_t96"]["spec"])
+    pos, _ = layout_tensors(lay)
+    x = synth.activations(64, lay.T, device=DEV)
+    mods = synth.modulation(64, device=DEV)
+    a = x.clone()
+    blocks.forward(a, lay.segments, pos, mods)
+    b = x.clone()
+    for i in range(2):
+        blocks.forward(b, lay.segments, pos, mods, first_block=i, n_blocks=1)
+    assert F3.flux3_check_error(_stream()) == 0
+    assert torch.isfinite(a).all() and torch.equal(a, b)
+    blocks.close()
 
 
 def test_fp8r_block_full_size_sampled_rows(fp8_block):
