@@ -181,8 +181,9 @@ FLUX3_API size_t flux3_packed_weight_bytes(const flux3_config *cfg);
 
 /* Bytes of workspace a forward call with T tokens needs (stream ids, RoPE
  * tables, modulated input, q/k/v, attention + SwiGLU output; with NVFP4 or
- * fp8r weights also one block's weights expanded to bf16, 245.4 MB).  0 if
- * cfg is invalid or T is out of range. */
+ * fp8r weights also one block's weights expanded to bf16, 245.4 MB, which
+ * calls of up to 128 tokens leave unused).  0 if cfg is invalid or T is out of
+ * range. */
 FLUX3_API size_t flux3_workspace_bytes(const flux3_config *cfg, int T);
 
 /* Creates a handle for n_blocks blocks (n_blocks == cfg->n_blocks).
@@ -198,10 +199,12 @@ FLUX3_API flux3_status flux3_block_init(flux3_handle **out, const flux3_config *
 /* flux3_block_init for NVFP4 weights (cfg->wfmt == FLUX3_W_NVFP4): packs the
  * codes, block scales, global scales and norm scales into `packed`
  * (flux3_packed_weight_bytes(cfg) bytes).  Every forward call then expands
- * each block's weights to bf16 in the workspace (e2m1 * e4m3, exact in float32,
- * times the global scale rounded to float32, then to bf16; both nearest even) just before
- * the block runs, and the projections run as bf16 tensor-core GEMMs with bf16
- * activations.  Same errors as flux3_block_init. */
+ * each block's weights to bf16 (e2m1 * e4m3, exact in float32, times the
+ * global scale rounded to float32, then to bf16; both nearest even) and the
+ * projections run as bf16 tensor-core GEMMs with bf16 activations: above 128
+ * tokens the expansion goes to the workspace just before the block runs, up to
+ * 128 tokens the GEMMs expand the codes in shared memory (the same values).
+ * Same errors as flux3_block_init. */
 FLUX3_API flux3_status flux3_block_init_nvfp4(flux3_handle **out, const flux3_config *cfg,
                                               const flux3_block_weights_nvfp4 *w, int n_blocks,
                                               void *packed, size_t packed_bytes, void *stream);
@@ -232,9 +235,9 @@ FLUX3_API flux3_status flux3_dequantize_block(const flux3_handle *h, int block_i
 /* A handle over fp8r weights (cfg->wfmt = FLUX3_W_FP8R), same conventions as
  * flux3_block_init_nvfp4: the codes and scales are copied into `packed`
  * (flux3_packed_weight_bytes(cfg) bytes: 122.9 MB per block), and every
- * forward call expands the running block's weights to bf16 in the workspace
- * (e4m3 * scale rounded to float32, then to bf16, both nearest even) before
- * the bf16 GEMMs. */
+ * forward call expands the running block's weights to bf16 (e4m3 * scale
+ * rounded to float32, then to bf16, both nearest even) for the bf16 GEMMs: in
+ * the workspace above 128 tokens, inside the GEMMs in shared memory up to 128. */
 FLUX3_API flux3_status flux3_block_init_fp8r(flux3_handle **out, const flux3_config *cfg,
                                              const flux3_block_weights_fp8r *w, int n_blocks, void *packed,
                                              size_t packed_bytes, void *stream);
