@@ -549,7 +549,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
       n_pre = un.kb1 - un.kb0 < kCodeStages ? un.kb1 - un.kb0 : kCodeStages;
       for (int i = 0; i < n_pre; ++i) {
         mbar_arrive_expect_tx(&ctl->cfull[i], C::kCodeBytes);
-        tma_load_2d(smC + i * C::kCodeBytes, &tmB, &ctl->cfull[i], (un.kb0 + i) * C::kCodeCols, un.n_blk * kBN);
+        tma_load_2d_hint(smC + i * C::kCodeBytes, &tmB, &ctl->cfull[i], (un.kb0 + i) * C::kCodeCols, un.n_blk * kBN,
+                         l2_policy_evict_first());
       }
     }
   } else if constexpr (!kPair) {
@@ -559,8 +560,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
       for (int i = 0; i < n_pre; ++i) {
         uint8_t *b_dst = smB + i * C::kBBytes;
         mbar_arrive_expect_tx(&ctl->full[i], C::kTxBytes);
-        tma_load_2d(b_dst, &tmB, &ctl->full[i], (un.kb0 + i) * kBK, un.n_blk * kBN);
-        tma_load_2d(b_dst + 128 * kBK * 2, &tmB, &ctl->full[i], (un.kb0 + i) * kBK, un.n_blk * kBN + 128);
+        const uint64_t pol = l2_policy_evict_first();
+        tma_load_2d_hint(b_dst, &tmB, &ctl->full[i], (un.kb0 + i) * kBK, un.n_blk * kBN, pol);
+        tma_load_2d_hint(b_dst + 128 * kBK * 2, &tmB, &ctl->full[i], (un.kb0 + i) * kBK, un.n_blk * kBN + 128, pol);
       }
     }
   }
@@ -571,7 +573,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer: this CTA's 128 A rows and its B rows
-      // (pair: 128, completing on the leader's full barrier; single: 256)
+      // (pair: 128, completing on the leader's full barrier; single: 256).
+      // The one-CTA form reads each weight line once: its B loads are
+      // evicted from L2 first, so they do not push out the small tensors the
+      // epilogues and the next kernels read (RoPE tables, residual rows).
+      uint64_t b_policy = 0;
+      if constexpr (!kPair) b_policy = l2_policy_evict_first();
       int last_phase[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
@@ -601,8 +608,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
           } else {
             if (!pre) {
               mbar_arrive_expect_tx(&ctl->full[stage], C::kTxBytes);
-              tma_load_2d(b_dst, &tmB, &ctl->full[stage], kb * kBK, b_row);
-              tma_load_2d(b_dst + 128 * kBK * 2, &tmB, &ctl->full[stage], kb * kBK, b_row + 128);
+              tma_load_2d_hint(b_dst, &tmB, &ctl->full[stage], kb * kBK, b_row, b_policy);
+              tma_load_2d_hint(b_dst + 128 * kBK * 2, &tmB, &ctl->full[stage], kb * kBK, b_row + 128, b_policy);
             }
             tma_load_2d(a_dst, &tmA, &ctl->full[stage], kb * kBK, a_row);
           }
@@ -619,6 +626,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
       }
     } else if (kConv && lane == 1) {
       // ---------------- code ring: each k-block's 256 rows of code bytes
+      const uint64_t b_policy = l2_policy_evict_first();
       int last_phase[kCodeStages];
 #pragma unroll
       for (int s = 0; s < kCodeStages; ++s) last_phase[s] = -1;
@@ -634,7 +642,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
               break;
             }
             mbar_arrive_expect_tx(&ctl->cfull[cs], C::kCodeBytes);
-            tma_load_2d(smC + cs * C::kCodeBytes, &tmB, &ctl->cfull[cs], kb * C::kCodeCols, un.n_blk * kBN);
+            tma_load_2d_hint(smC + cs * C::kCodeBytes, &tmB, &ctl->cfull[cs], kb * C::kCodeCols, un.n_blk * kBN,
+                             b_policy);
           }
           last_phase[cs] = (int)cphase;
           if (++cs == kCodeStages) {
