@@ -90,10 +90,14 @@ constexpr int kLnWarps = 8;
 
 __global__ void __launch_bounds__(kLnWarps * 32, 2)
     ln_modulate_kernel(const float *__restrict__ x, int T, const uint8_t *__restrict__ sid,
-                       const float *__restrict__ mod, float eps, __nv_bfloat16 *__restrict__ h) {
+                       const float *__restrict__ mod, float eps, __nv_bfloat16 *__restrict__ h, int early_release) {
   constexpr int kVec = kHidden / (32 * 4);  // 24 float4 per lane
+  // early_release: the dependent (the in-projection) may start before this
+  // kernel's own wait -- when nothing it reads before its wait (constant
+  // weights) is written by a kernel still running
+  if (early_release) griddep_launch_dependents();
   griddep_wait();
-  griddep_launch_dependents();
+  if (!early_release) griddep_launch_dependents();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * kLnWarps + warp;
   if (t >= T) return;
@@ -200,10 +204,10 @@ cudaError_t launch_prepare(const flux3_segment *segs, int n_segs, int T, uint8_t
 }
 
 cudaError_t launch_ln_modulate(const float *x, int T, const uint8_t *sid, const float *mod, float eps,
-                               __nv_bfloat16 *h, cudaStream_t s, bool pdl) {
+                               __nv_bfloat16 *h, cudaStream_t s, bool pdl, bool early_release) {
   using namespace ew_detail;
   return launch_kernel(ln_modulate_kernel, dim3((T + kLnWarps - 1) / kLnWarps), dim3(kLnWarps * 32), 0, s, pdl, x,
-                       T, sid, mod, eps, h);
+                       T, sid, mod, eps, h, early_release ? 1 : 0);
 }
 
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, cudaStream_t s) {

@@ -282,7 +282,10 @@ flux3_status forward_common(const flux3_handle *h, int first, int count, float *
     } else if (h->cfg.wfmt == FLUX3_W_FP8R) {
       F3_CUDA(launch_dequantize_fp8r_block(h->fp8[b], ws.w_in, ws.w_out, s, true));
     }
-    F3_CUDA(launch_ln_modulate(x, T, ws.sid, mod, h->cfg.eps_ln, ws.h, s, true));
+    // LayerNorm releases the in-projection before its own wait unless this
+    // block's weights were just expanded in HBM (the in-projection loads its
+    // first weight stages before its wait)
+    F3_CUDA(launch_ln_modulate(x, T, ws.sid, mod, h->cfg.eps_ln, ws.h, s, true, !fp4 || lowp_in_gemm));
     EpiParams ep{};
     ep.qkv = ws.qkv;
     ep.cat = ws.cat;

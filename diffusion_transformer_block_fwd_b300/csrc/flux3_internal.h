@@ -138,8 +138,11 @@ cudaError_t launch_rope_tables(const float *pos, int T, float theta, float *cos_
 // Stream ids and RoPE tables in one launch (the per-call preparation).
 cudaError_t launch_prepare(const flux3_segment *segs, int n_segs, int T, uint8_t *sid, const float *pos, float theta,
                            float *cos_tab, float *sin_tab, cudaStream_t s);
+// early_release (with pdl): the next kernel may be scheduled before this one's
+// programmatic-dependent wait; only where that kernel reads nothing before its
+// own wait that a still-running kernel writes.
 cudaError_t launch_ln_modulate(const float *x, int T, const uint8_t *sid, const float *mod, float eps,
-                               __nv_bfloat16 *h, cudaStream_t s, bool pdl = false);
+                               __nv_bfloat16 *h, cudaStream_t s, bool pdl = false, bool early_release = false);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, cudaStream_t s);
 // part / part_bytes: scratch for the key-range split of the last, partial
 // wave of units (null: no split).

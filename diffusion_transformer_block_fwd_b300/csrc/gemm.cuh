@@ -536,11 +536,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
   // One-CTA form (small M, bound by streaming the weights B from DRAM): the
   // B halves of the first ring stages are loaded before griddep_wait, so the
   // DRAM latency of the first tiles passes while the previous kernel
-  // finishes.  No kernel this one may overlap writes B: the weights are
-  // constant or expanded at the start of the block, and the in-projection
-  // starts only after its predecessor (LayerNorm) has waited for everything
-  // before it, the out-projection only after the in-projection has.  The A
-  // halves, which the previous kernel may write, follow after the wait.
+  // finishes.  No kernel this one may overlap writes B: the weights (or their
+  // codes) are constant, or expanded in HBM at the start of the block -- and
+  // then LayerNorm releases the in-projection only after its own wait, so the
+  // expansion has completed; the out-projection starts only after the
+  // in-projection has.  The A halves, which the previous kernel may write,
+  // follow after the wait.
   int n_pre = 0;
   if constexpr (kConv) {
     // the codes of the first k-blocks (lane 1 runs the code ring)
