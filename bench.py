@@ -114,10 +114,10 @@ def kernel_bytes(T):
 # before its host-launcher marker line, the whole file if it has none); null
 # otherwise.
 TRAFFIC = {
-    # gemm_kernel<EPI_IN_PROJ>, T = 4608: dram__bytes_read.sum 215.15 MB + dram__bytes_write.sum 154.88 MB
+    # gemm_kernel<EPI_IN_PROJ>, T = 4608: dram__bytes_read.sum 210.07 MB + dram__bytes_write.sum 154.33 MB
     # (ncu --metrics ... --clock-control none, one launch; profiles/gemm_tcgen05_block_1024sq_t4608.md)
-    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "2d2b95892193d561", "T": 4608,
-                      "bytes_per_launch": 370_039_552},
+    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "dc2f07cdc7a39599", "T": 4608,
+                      "bytes_per_launch": 364_397_056},
 }
 
 HOST_MARKER = b"// ---------------------------------------------------------------- host launchers\n"
