@@ -109,3 +109,19 @@ def test_traffic_key_covers_device_code_only():
     for tr in b.TRAFFIC.values():
         with open(os.path.join(ROOT, tr["src"]), "rb") as f:
             assert f.read().count(b.HOST_MARKER) == 1, tr["src"]
+
+
+def test_split_plan_mirrors():
+    """bench.py counts each launch of the timed region, so it mirrors the
+    library's split plans on 148 SMs: the out-projection's K ranges (one-CTA
+    128-row tiles up to 128 tokens, CTA-pair 256-row tiles above) and
+    attention's key ranges of a partial last wave; a split adds one merge
+    launch.  The values are those the step tests name for each size."""
+    b = _bench()
+    out = {1: 12, 96: 12, 128: 12, 129: 6, 171: 6, 512: 3, 4608: 1, 6656: 4, 14848: 2}
+    for T, S in out.items():
+        assert b.out_proj_splits(T, 148) == S, (T, b.out_proj_splits(T, 148), S)
+    attn = {2048: 3, 4256: 1, 4608: 1, 6656: 4, 8704: 1, 14848: 2, 16384: 2}
+    for T, S in attn.items():
+        assert b.attn_splits(T, 148) == S, (T, b.attn_splits(T, 148), S)
+    assert b.merges(96, 148) == 1 and b.merges(4608, 148) == 0 and b.merges(6656, 148) == 2
