@@ -111,12 +111,12 @@ def kernel_bytes(T):
 
 # DRAM traffic per launch from an ncu capture, valid only for the kernel
 # source it was taken on: the sha256 of the file's device code (the text
-# before its host-launcher marker line, the whole file if it has none); null
-# otherwise.
+# before its host-launcher marker line, the whole file if it has none; comments
+# stripped); null otherwise.
 TRAFFIC = {
     # gemm_kernel<EPI_IN_PROJ>, T = 4608: dram__bytes_read.sum 210.07 MB + dram__bytes_write.sum 154.33 MB
     # (ncu --metrics ... --clock-control none, one launch; profiles/gemm_tcgen05_block_1024sq_t4608.md)
-    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "dc2f07cdc7a39599", "T": 4608,
+    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "9f4753bd68c5839b", "T": 4608,
                       "bytes_per_launch": 364_397_056},
 }
 
@@ -129,9 +129,36 @@ def device_part(text):
     return text if i < 0 else text[:i]
 
 
+def strip_comments(text):
+    """C / C++ source bytes without their // and /* */ comments (string and
+    character literals kept), runs of blanks collapsed, empty lines dropped: a
+    comment or layout edit leaves a kernel's key unchanged, a code edit does
+    not."""
+    out, i, n = bytearray(), 0, len(text)
+    while i < n:
+        c = text[i:i + 1]
+        if c in (b'"', b"'"):
+            j = i + 1
+            while j < n and text[j:j + 1] != c:
+                j += 2 if text[j:j + 1] == b"\\" else 1
+            out += text[i:j + 1]
+            i = j + 1
+        elif text.startswith(b"//", i):
+            j = text.find(b"\n", i)
+            i = n if j < 0 else j
+        elif text.startswith(b"/*", i):
+            j = text.find(b"*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out += c
+            i += 1
+    lines = [b" ".join(l.split()) for l in bytes(out).split(b"\n")]   # blanks collapsed
+    return b"\n".join(l for l in lines if l)
+
+
 def src_sha(path):
     with open(os.path.join(ROOT, path), "rb") as f:
-        return hashlib.sha256(device_part(f.read())).hexdigest()[:16]
+        return hashlib.sha256(strip_comments(device_part(f.read()))).hexdigest()[:16]
 
 
 class L2Flush:

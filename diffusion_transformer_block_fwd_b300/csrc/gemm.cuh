@@ -18,7 +18,11 @@
 // For M <= 128 the one-CTA form runs instead (gemm1_kernel: 128 x 256 tiles,
 // cta_group::1, all 256 B rows of a k-block in the CTA's shared memory, a
 // 4-stage ring): a pair tile would be more than half padding there, and the
-// 148 CTAs take twice as many tiles per round as 74 pairs.
+// 148 CTAs take twice as many tiles per round as 74 pairs.  Its weight loads
+// carry an evict-first L2 policy (each weight line is read once).  Over NVFP4
+// or fp8r weights (gemm1_fp4_kernel, gemm1_fp8_kernel) the codes arrive in a
+// ring of their own and the epilogue warps expand each k-block into the bf16
+// B stage in shared memory (see GemmCfg).
 //
 // Roles (320 threads per CTA): warp 0 issues the CTA's TMA loads (128 x 64
 // of A, 128 x 64 of B, 128-byte swizzle) into a 6-stage ring, completing on

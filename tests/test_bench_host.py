@@ -105,6 +105,13 @@ def test_traffic_key_covers_device_code_only():
     assert b.device_part(dev + b.HOST_MARKER + host) == dev
     assert b.device_part(dev + b.HOST_MARKER + host + b"// edited\n") == dev
     assert b.device_part(dev + host) == dev + host          # no marker: the whole file
+    # comments do not enter the key; code does; literals holding // or /* stay code
+    code = b'__global__ void k(int *p) {  // store\n  /* one */ *p = 1;\n  const char *s = "// x";\n}\n'
+    recommented = b'__global__ void k(int *p) {\n  // the store\n  *p = 1;  /* two */\n  const char *s = "// x";\n}\n'
+    edited = code.replace(b"*p = 1", b"*p = 2")
+    assert b.strip_comments(code) == b.strip_comments(recommented)
+    assert b.strip_comments(code) != b.strip_comments(edited)
+    assert b'"// x"' in b.strip_comments(code)
     # every kernel source a traffic figure is keyed to has the marker once
     for tr in b.TRAFFIC.values():
         with open(os.path.join(ROOT, tr["src"]), "rb") as f:
