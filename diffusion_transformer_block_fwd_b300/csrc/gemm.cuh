@@ -244,7 +244,27 @@ __device__ __forceinline__ void put_chunk_bf16(const BoxWriter &bw, int q0, cons
 // bf16 outputs leave through the warp's staging box and TMA stores (tm0: C or
 // qkv, tm1: cat); row0 is the first of the warp's 32 rows (stores clip rows
 // past M).
-template <int EPI>
+// One 32-column chunk c of a q / k head: RMSNorm (inv, per-dim scales ns)
+// then RoPE on the 16 adjacent pairs (cs, sn), packed to bf16 into the warp's
+// box (chunk c fills the box's columns 32 * (c & 1) .. +31).
+__device__ __forceinline__ void qk_rope_chunk(const BoxWriter &bw, const uint32_t (&r)[32], float inv,
+                                              const float (&ns)[32], const float (&cs)[16], const float (&sn)[16],
+                                              int c) {
+  uint32_t o[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float x0 = f32(r[2 * j]) * inv * ns[2 * j];
+    const float x1 = f32(r[2 * j + 1]) * inv * ns[2 * j + 1];
+    o[j] = pack_bf16x2(x0 * cs[j] - x1 * sn[j], x0 * sn[j] + x1 * cs[j]);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) bw.put(4 * (c & 1) + q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+
+// kPipeTables: the q / k tiles' RoPE rows are loaded one chunk ahead with
+// in-order loads (the forms whose epilogue warps hold no code-expansion state;
+// in the others the extra registers would spill).
+template <int EPI, bool kPipeTables = true>
 __device__ __forceinline__ bool epilogue_half(uint32_t taddr, int row, int row0, int M, int n_blk, int half,
                                               const EpiParams &ep, const BoxWriter &bw, const CUtensorMap *tm0,
                                               const CUtensorMap *tm1, uint64_t *xbar, uint32_t &xphase,
@@ -317,41 +337,74 @@ __device__ __forceinline__ bool epilogue_half(uint32_t taddr, int row, int row0,
       const float4 *cs4 = reinterpret_cast<const float4 *>(ep.cos_tab + (size_t)rrow * kRopePairs);
       const float4 *sn4 = reinterpret_cast<const float4 *>(ep.sin_tab + (size_t)rrow * kRopePairs);
       float ss = 0.f;
+      if constexpr (kPipeTables) {
+        // The row's RoPE pairs stream one chunk ahead through in-order loads:
+        // chunk 0's go out before the sum-of-squares pass, chunk c+1's before
+        // chunk c's TMEM read, so no chunk waits a full memory round trip.
+        float4 ca[4], sa[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ca[q] = ldg_f4_in_order(cs4 + q), sa[q] = ldg_f4_in_order(sn4 + q);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(th + c * 32, r);
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(th + c * 32, r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ss = fmaf(f32(r[i]), f32(r[i]), ss);
-      }
-      const float inv = rsqrtf(ss * (1.0f / kHeadDim) + ep.eps_rms);
+          for (int i = 0; i < 32; ++i) ss = fmaf(f32(r[i]), f32(r[i]), ss);
+        }
+        const float inv = rsqrtf(ss * (1.0f / kHeadDim) + ep.eps_rms);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        if ((c & 1) == 0) bw.begin();
-        // this chunk's 16 RoPE pairs and 32 norm scales, 16-byte loads issued
-        // ahead of the TMEM read
-        float cs[16], sn[16], ns[32];
+        for (int c = 0; c < 4; ++c) {
+          if ((c & 1) == 0) bw.begin();
+          // this chunk's 16 RoPE pairs (loaded one chunk earlier) and 32 norm
+          // scales (the same for every row: L1 hits after the first warp)
+          float cs[16], sn[16], ns[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 a = __ldg(cs4 + c * 4 + q), b = __ldg(sn4 + c * 4 + q);
-          cs[4 * q] = a.x, cs[4 * q + 1] = a.y, cs[4 * q + 2] = a.z, cs[4 * q + 3] = a.w;
-          sn[4 * q] = b.x, sn[4 * q + 1] = b.y, sn[4 * q + 2] = b.z, sn[4 * q + 3] = b.w;
+          for (int q = 0; q < 4; ++q) {
+            cs[4 * q] = ca[q].x, cs[4 * q + 1] = ca[q].y, cs[4 * q + 2] = ca[q].z, cs[4 * q + 3] = ca[q].w;
+            sn[4 * q] = sa[q].x, sn[4 * q + 1] = sa[q].y, sn[4 * q + 2] = sa[q].z, sn[4 * q + 3] = sa[q].w;
+          }
+          if (c < 3) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              ca[q] = ldg_f4_in_order(cs4 + (c + 1) * 4 + q), sa[q] = ldg_f4_in_order(sn4 + (c + 1) * 4 + q);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 a = ldg_f4_in_order(nscale4 + c * 8 + q);
+            ns[4 * q] = a.x, ns[4 * q + 1] = a.y, ns[4 * q + 2] = a.z, ns[4 * q + 3] = a.w;
+          }
+          tmem_ld32(th + c * 32, r);
+          qk_rope_chunk(bw, r, inv, ns, cs, sn, c);
+          if (c & 1) bw.store(tm0, n0 + 64 * (c >> 1), row0);
         }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(th + c * 32, r);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 a = __ldg(nscale4 + c * 8 + q);
-          ns[4 * q] = a.x, ns[4 * q + 1] = a.y, ns[4 * q + 2] = a.z, ns[4 * q + 3] = a.w;
+          for (int i = 0; i < 32; ++i) ss = fmaf(f32(r[i]), f32(r[i]), ss);
         }
-        tmem_ld32(th + c * 32, r);
-        uint32_t o[16];
+        const float inv = rsqrtf(ss * (1.0f / kHeadDim) + ep.eps_rms);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          if ((c & 1) == 0) bw.begin();
+          // this chunk's 16 RoPE pairs and 32 norm scales, 16-byte loads issued
+          // ahead of the TMEM read
+          float cs[16], sn[16], ns[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float x0 = f32(r[2 * j]) * inv * ns[2 * j];
-          const float x1 = f32(r[2 * j + 1]) * inv * ns[2 * j + 1];
-          o[j] = pack_bf16x2(x0 * cs[j] - x1 * sn[j], x0 * sn[j] + x1 * cs[j]);
+          for (int q = 0; q < 4; ++q) {
+            const float4 a = __ldg(cs4 + c * 4 + q), b = __ldg(sn4 + c * 4 + q);
+            cs[4 * q] = a.x, cs[4 * q + 1] = a.y, cs[4 * q + 2] = a.z, cs[4 * q + 3] = a.w;
+            sn[4 * q] = b.x, sn[4 * q + 1] = b.y, sn[4 * q + 2] = b.z, sn[4 * q + 3] = b.w;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 a = __ldg(nscale4 + c * 8 + q);
+            ns[4 * q] = a.x, ns[4 * q + 1] = a.y, ns[4 * q + 2] = a.z, ns[4 * q + 3] = a.w;
+          }
+          tmem_ld32(th + c * 32, r);
+          qk_rope_chunk(bw, r, inv, ns, cs, sn, c);
+          if (c & 1) bw.store(tm0, n0 + 64 * (c >> 1), row0);
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) bw.put(4 * (c & 1) + q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        if (c & 1) bw.store(tm0, n0 + 64 * (c >> 1), row0);
       }
     } else if (n_blk < kVEnd) {
 #pragma unroll 1
@@ -823,7 +876,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap &tmA, const CUtensor
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kBN;
       if (un.slot >= 0) {
         store_partial_half(taddr, un.slot, row_in_tile - lane, M - un.m_blk * kTileM, half, kTileM, bw, &tmO1);
-      } else if (!epilogue_half<EPI>(taddr, un.m_blk * kTileM + row_in_tile, un.m_blk * kTileM + row_in_tile - lane,
+      } else if (!epilogue_half<EPI, !kConv>(taddr, un.m_blk * kTileM + row_in_tile, un.m_blk * kTileM + row_in_tile - lane,
                                      M, un.n_blk, half, ep, bw, &tmO0, &tmO1, xbar, xphase, abort)) {
         x_in_flight = true;   // only the residual box wait can fail
         break;

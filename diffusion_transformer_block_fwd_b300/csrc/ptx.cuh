@@ -116,6 +116,15 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *t
       "l"(tm), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
+// 16-byte read-only global load as volatile asm: it keeps its place among the
+// other volatile asm statements (a plain load may be scheduled after a later
+// tcgen05.ld and its wait, exposing its latency); its result is still waited
+// for only at first use.  For data no running kernel writes.
+__device__ __forceinline__ float4 ldg_f4_in_order(const float4 *p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, const void *src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tm),
                "r"(smem_addr(src)), "r"(c0), "r"(c1)
