@@ -114,10 +114,10 @@ def kernel_bytes(T):
 # before its host-launcher marker line, the whole file if it has none; comments
 # stripped); null otherwise.
 TRAFFIC = {
-    # gemm_kernel<EPI_IN_PROJ>, T = 4608: dram__bytes_read.sum 210.07 MB + dram__bytes_write.sum 154.33 MB
+    # gemm_kernel<EPI_IN_PROJ>, T = 4608: dram__bytes_read.sum 207.53 MB + dram__bytes_write.sum 154.16 MB
     # (ncu --metrics ... --clock-control none, one launch; profiles/gemm_tcgen05_block_1024sq_t4608.md)
-    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "9f4753bd68c5839b", "T": 4608,
-                      "bytes_per_launch": 364_397_056},
+    "in_projection": {"src": "diffusion_transformer_block_fwd_b300/csrc/gemm.cuh", "src_sha": "118222b384e5fa29", "T": 4608,
+                      "bytes_per_launch": 361_686_016},
 }
 
 HOST_MARKER = b"// ---------------------------------------------------------------- host launchers\n"
